@@ -1,0 +1,168 @@
+/* Oracle: LM head, row statistics and acceptance (test infrastructure only;
+ * see oracle.h).
+ *
+ * Steps, in the pages' order:
+ *  1. Logits_i = H_i x W_o for every verify row ("Multi Token Prediction"
+ *     note, K=3 flow, step 4). The sum runs in double and is rounded to
+ *     binary32; sampling rows are then multiplied by 1/T in binary32
+ *     (p = softmax(logits / T); temperature 0 means the argmax rule,
+ *     "Speculative decoding and MTP" §4.4).
+ *  2. Softmax statistics per row (same note, step 5): max, log-sum-exp (in
+ *     double over the binary32 logits), argmax (lowest index on ties).
+ *  3. Acceptance, scanning the drafts in order and stopping at the first
+ *     failure ("MTP principles" §三 stage 3; "Speculative decoding and MTP"
+ *     §2.3 and §4.4; "MTP in TensorRT-LLM" Fig. 1):
+ *       greedy:   accept d_{j+1} iff argmax of row j equals it; the first
+ *                 mismatch is replaced by that argmax; if all D match, the
+ *                 argmax of row D is the bonus token.
+ *       sampling: accept d_{j+1} iff p_j(d) >= U_j * q_j(d) (same as accepting
+ *                 with probability min(1, p/q)); at the first rejection draw
+ *                 from normalised max(0, p_j - q_j); if all D are accepted
+ *                 draw the bonus from p_D.
+ *     Every step emits n + 1 tokens, 1 .. D+1 ("MTP principles" stage 4).
+ *  4. A categorical draw is an exponential race: argmax_v w_v / E_v with
+ *     E_v ~ Exp(1) from the counter-based generator (philox.cpp); this picks
+ *     v with probability w_v / sum(w). If every residual weight is zero the
+ *     draw falls back to p itself.
+ * The accept test and the race are evaluated in binary32, the precision the
+ * GPU decides in; decisions within 1e-5 of flipping are flagged.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <vector>
+#include "oracle.h"
+#include "oracle_internal.h"
+
+static const float kTieRel = 1e-5f;
+
+extern "C" int oracle_accept_prefix(int D, const float* p, const float* q, const float* U, uint8_t* tie) {
+  int n = 0;
+  for (int j = 0; j < D; ++j) {
+    float uq = U[j] * q[j];
+    if (q[j] > 0.0f && fabsf(p[j] - uq) < kTieRel * q[j]) *tie |= 1;
+    if (p[j] >= uq) {
+      n = j + 1;
+    } else {
+      break;
+    }
+  }
+  return n;
+}
+
+extern "C" int oracle_race(int V, const float* w, const float* E, uint8_t* near_tie) {
+  int best = -1;
+  float k1 = -1.0f, k2 = -1.0f;
+  for (int v = 0; v < V; ++v) {
+    if (!(w[v] > 0.0f)) continue;
+    float key = w[v] / E[v]; /* E == 0 gives +inf: that entry wins */
+    if (key > k1) {
+      k2 = k1;
+      k1 = key;
+      best = v;
+    } else if (key > k2) {
+      k2 = key;
+    }
+  }
+  if (best >= 0 && k2 >= 0.0f && (k1 == k2 || k1 - k2 <= kTieRel * k1)) *near_tie = 1;
+  return best;
+}
+
+extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
+                                    const void* hidden, const void* lm_head,
+                                    const int32_t* tokens, const uint8_t* mode,
+                                    const float* temperature, const float* q_draft,
+                                    uint64_t seed,
+                                    int32_t* out_tokens, int32_t* num_accepted,
+                                    uint8_t* tie_flags, float* lse_out,
+                                    int32_t* argmax_out, float* logits_out) {
+  if (B < 0 || D < 0 || H <= 0 || V <= 0 || (dtype != 0 && dtype != 1)) return ORACLE_BAD_ARG;
+  const int R = D + 1;
+  std::vector<float> logits((size_t)R * V);
+  std::vector<float> lse(R);
+  std::vector<int> amax(R);
+  std::vector<float> w(V), E(V), p(V);
+
+  for (int b = 0; b < B; ++b) {
+    for (int j = 0; j < R; ++j) {
+      int tok = tokens[(int64_t)b * R + j];
+      if (tok < 0 || tok >= V) return ORACLE_BAD_INDEX;
+    }
+    const bool sampling = mode[b] == 1 && temperature != NULL && temperature[b] > 0.0f;
+    if (sampling && q_draft == NULL) return ORACLE_BAD_ARG;
+    const float inv_t = sampling ? 1.0f / temperature[b] : 1.0f;
+
+    /* Steps 1-2 for the R rows of request b. */
+    for (int j = 0; j < R; ++j) {
+      const int64_t m = (int64_t)b * R + j;
+      float* row = &logits[(size_t)j * V];
+      for (int v = 0; v < V; ++v) {
+        double acc = 0.0;
+        for (int k = 0; k < H; ++k)
+          acc += oracle_load(hidden, dtype, m * H + k) * oracle_load(lm_head, dtype, (int64_t)v * H + k);
+        float l = (float)acc;
+        row[v] = sampling ? l * inv_t : l;
+      }
+      double mx = -INFINITY;
+      int best = 0;
+      for (int v = 0; v < V; ++v) {
+        if ((double)row[v] > mx) {
+          mx = row[v];
+          best = v;
+        }
+      }
+      double s = 0.0;
+      for (int v = 0; v < V; ++v) s += exp((double)row[v] - mx);
+      lse[j] = (float)(mx + log(s));
+      amax[j] = best;
+      if (lse_out) lse_out[m] = lse[j];
+      if (argmax_out) argmax_out[m] = best;
+      if (logits_out)
+        for (int v = 0; v < V; ++v) logits_out[m * V + v] = row[v];
+    }
+
+    /* Step 3. */
+    int32_t* out = &out_tokens[(int64_t)b * R];
+    const int32_t* tok = &tokens[(int64_t)b * R];
+    for (int j = 0; j < R; ++j) out[j] = -1;
+    uint8_t tie = 0;
+    int n;
+    if (!sampling) {
+      n = 0;
+      while (n < D && amax[n] == tok[n + 1]) ++n;
+      for (int j = 0; j < n; ++j) out[j] = tok[j + 1];
+      out[n] = amax[n];
+    } else {
+      std::vector<float> pd(D), qd(D), U(D);
+      for (int j = 0; j < D; ++j) {
+        int x = tok[j + 1];
+        pd[j] = expf(logits[(size_t)j * V + x] - lse[j]);
+        qd[j] = q_draft[((int64_t)b * D + j) * V + x];
+        U[j] = oracle_accept_uniform(seed, (uint32_t)b, (uint32_t)j);
+      }
+      n = oracle_accept_prefix(D, pd.data(), qd.data(), U.data(), &tie);
+      for (int j = 0; j < n; ++j) out[j] = tok[j + 1];
+      /* Step 4: residual draw at row n if a draft was rejected, bonus draw
+       * from row D otherwise. */
+      const uint32_t tag = n < D ? 2u : 3u;
+      const float* row = &logits[(size_t)n * V];
+      for (int v = 0; v < V; ++v) {
+        p[v] = expf(row[v] - lse[n]);
+        float qv = n < D ? q_draft[((int64_t)b * D + n) * V + v] : 0.0f;
+        float r = p[v] - qv;
+        w[v] = r > 0.0f ? r : 0.0f;
+        E[v] = oracle_race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag);
+      }
+      uint8_t race_tie = 0;
+      int winner = oracle_race(V, w.data(), E.data(), &race_tie);
+      if (winner < 0) {
+        race_tie = 0;
+        winner = oracle_race(V, p.data(), E.data(), &race_tie);
+      }
+      if (race_tie) tie |= 2;
+      out[n] = winner;
+    }
+    num_accepted[b] = n;
+    tie_flags[b] = tie;
+  }
+  return ORACLE_OK;
+}
