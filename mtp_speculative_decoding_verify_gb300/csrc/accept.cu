@@ -1,0 +1,216 @@
+// Acceptance: merge the LM head's per-slice row statistics, decide how many
+// drafts to accept, and draw the correction / bonus token of sampling
+// requests.
+//
+// "MTP principles" §三 stage 3: greedy - a draft is accepted while it equals
+// the target argmax, the first mismatch ends the scan; rejection sampling -
+// a draft is accepted when P_target/P_draft >= U, otherwise the token is
+// redrawn. Stage 4: the step emits 1 .. D+1 tokens, the first rejected
+// position replaced by the target's token. "Speculative decoding and MTP"
+// §2.3: drafts after the first rejection are dropped whatever their
+// probability; §4.4: accept with probability min(1, p/q), and at temperature
+// 0 accept only when argmax(p) is the draft, replacing it otherwise.
+// "MTP in TensorRT-LLM" Fig. 1: when every draft is accepted the target's
+// own next token is accepted too (the bonus).
+//
+// The redraw uses the residual max(0, p - q) (normalised) so that the
+// emitted tokens follow p exactly; a categorical draw is an exponential race
+// argmax_v w_v / E_v with E_v from the Philox stream, so the winner does not
+// depend on how the vocabulary is split across CTAs.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "philox.cuh"
+
+namespace mtp {
+
+namespace {
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / kWarp;
+
+struct Decision {
+  int n;         // drafts accepted
+  int sampling;  // 1: a race must fill out_tokens[b, n]
+  int tie;       // bit0 near-tie of an accept decision
+  int pad;
+};
+
+struct RacePair {
+  Race resid;  // race on max(0, p - q) (or p for the bonus row)
+  Race plain;  // race on p, the fallback when every residual weight is zero
+};
+}  // namespace
+
+// One CTA per request: reduce the R rows' partials, then warp 0 takes the
+// accept decisions in order.
+__global__ void __launch_bounds__(kThreads) accept_decide_kernel(
+    const float* __restrict__ pmax, const float* __restrict__ psum, const float* __restrict__ pbest,
+    const int* __restrict__ pidx, const float* __restrict__ ldraft, int slices, const int32_t* __restrict__ tokens,
+    const uint8_t* __restrict__ mode, const float* __restrict__ temperature, const float* __restrict__ q_draft,
+    int any_sampling, uint64_t seed, int B, int D, int V, float* __restrict__ ws_lse, int* __restrict__ ws_amax,
+    Decision* __restrict__ dec, int* __restrict__ race_count, int32_t* __restrict__ out_tokens,
+    int32_t* __restrict__ num_accepted, uint8_t* __restrict__ tie_flags, float* __restrict__ lse_out,
+    int32_t* __restrict__ argmax_out, unsigned* err) {
+  __shared__ float s_lse[kMaxRows];
+  __shared__ int s_amax[kMaxRows];
+  const int b = blockIdx.x;
+  const int R = D + 1;
+  const int M = B * R;
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+
+  for (int j = warp; j < R; j += kWarps) {
+    const int m = b * R + j;
+    RowStat st = rowstat_empty();
+    for (int sl = lane; sl < slices; sl += kWarp) {
+      const int64_t o = (int64_t)sl * M + m;
+      st = rowstat_merge(st, RowStat{pmax[o], psum[o], pbest[o], pidx[o]});
+    }
+    st = warp_merge(st);
+    if (lane == 0) {
+      const float lse = st.m + logf(st.s);
+      s_lse[j] = lse;
+      s_amax[j] = st.idx;
+      ws_lse[m] = lse;
+      ws_amax[m] = st.idx;
+      if (lse_out) lse_out[m] = lse;
+      if (argmax_out) argmax_out[m] = st.idx;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+
+  const int32_t* tok = tokens + (int64_t)b * R;
+  int32_t* out = out_tokens + (int64_t)b * R;
+  bool bad = false;
+  for (int j = 0; j < R; ++j) bad |= (tok[j] < 0 || tok[j] >= V);
+  if (bad) raise_error(err, MTP_ERR_TOKEN_ID);
+  const bool sampling = any_sampling && mode[b] == 1 && temperature[b] > 0.0f;
+  int n = 0, tie = 0;
+  if (!sampling || bad) {
+    while (!bad && n < D && s_amax[n] == tok[n + 1]) ++n;
+    for (int j = 0; j < R; ++j) out[j] = j < n ? tok[j + 1] : (j == n ? s_amax[n] : -1);
+  } else {
+    for (; n < D; ++n) {
+      const int x = tok[n + 1];
+      const float p = expf(ldraft[b * R + n] - s_lse[n]);
+      const float qx = q_draft[((int64_t)b * D + n) * V + x];
+      const float u = accept_uniform(seed, (uint32_t)b, (uint32_t)n);
+      const float uq = __fmul_rn(u, qx);
+      if (qx > 0.0f && fabsf(p - uq) < __fmul_rn(kTieRel, qx)) tie |= 1;
+      if (!(p >= uq)) break;
+    }
+    for (int j = 0; j < R; ++j) out[j] = j < n ? tok[j + 1] : -1;  // out[n] comes from the race
+  }
+  dec[b] = Decision{n, (sampling && !bad) ? 1 : 0, tie, 0};
+  race_count[b] = 0;
+  num_accepted[b] = n;
+  tie_flags[b] = (uint8_t)tie;
+}
+
+// Grid (B, race_slices): each CTA races one vocabulary slice of the row that
+// needs a draw; the last CTA of a request to finish merges the slices.
+__global__ void __launch_bounds__(kThreads) accept_race_kernel(
+    const float* __restrict__ samp_logits, const float* __restrict__ q_draft, const float* __restrict__ ws_lse,
+    const Decision* __restrict__ dec, RacePair* __restrict__ parts, int* __restrict__ race_count, uint64_t seed,
+    int D, int V, int32_t* __restrict__ out_tokens, uint8_t* __restrict__ tie_flags) {
+  __shared__ RacePair s_part[kWarps];
+  __shared__ int s_last;
+  const int b = blockIdx.x;
+  const int nsl = gridDim.y, sl_id = blockIdx.y;
+  const Decision d = dec[b];
+  if (!d.sampling) return;
+  const int R = D + 1;
+  const int n = d.n;
+  const int64_t row = (int64_t)b * R + n;
+  const float lse = ws_lse[row];
+  const uint32_t tag = n < D ? kTagResidual : kTagBonus;
+  const float* lrow = samp_logits + row * V;
+  const float* qrow = n < D ? q_draft + ((int64_t)b * D + n) * V : nullptr;
+  const int per = (V + nsl - 1) / nsl;
+  const int v0 = sl_id * per;
+  const int v1 = min(V, v0 + per);
+
+  Race resid = race_empty(), plain = race_empty();
+  for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
+    const float p = expf(lrow[v] - lse);
+    const float qv = qrow ? qrow[v] : 0.0f;
+    const float r = p - qv;
+    const float w = r > 0.0f ? r : 0.0f;
+    const float E = race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag);
+    if (w > 0.0f) race_add(resid, w / E, v);
+    if (p > 0.0f) race_add(plain, p / E, v);
+  }
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  resid = warp_race_merge(resid);
+  plain = warp_race_merge(plain);
+  if (lane == 0) s_part[warp] = RacePair{resid, plain};
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RacePair acc = s_part[0];
+    for (int w = 1; w < kWarps; ++w) {
+      acc.resid = race_merge(acc.resid, s_part[w].resid);
+      acc.plain = race_merge(acc.plain, s_part[w].plain);
+    }
+    parts[(int64_t)b * nsl + sl_id] = acc;
+    __threadfence();
+    const int done = atomicAdd(&race_count[b], 1);
+    s_last = (done == nsl - 1);
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  const volatile RacePair* vp = parts + (int64_t)b * nsl;
+  Race r1 = race_empty(), r2 = race_empty();
+  for (int sl = 0; sl < nsl; ++sl) {
+    Race a{vp[sl].resid.k1, vp[sl].resid.i1, vp[sl].resid.k2};
+    Race c{vp[sl].plain.k1, vp[sl].plain.i1, vp[sl].plain.k2};
+    r1 = race_merge(r1, a);
+    r2 = race_merge(r2, c);
+  }
+  const Race win = r1.i1 >= 0 ? r1 : r2;
+  out_tokens[row] = win.i1;
+  if (race_near_tie(win)) tie_flags[b] = (uint8_t)(tie_flags[b] | 2);
+}
+
+cudaError_t launch_accept(const mtp_lmhead_args& a, const LmPlan& p, unsigned* err, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  char* ws = (char*)a.workspace;
+  accept_decide_kernel<<<a.B, kThreads, 0, s>>>(
+      (const float*)(ws + p.off_pmax), (const float*)(ws + p.off_psum), (const float*)(ws + p.off_pbest),
+      (const int*)(ws + p.off_pidx), (const float*)(ws + p.off_ldraft), p.slices, a.tokens, a.mode, a.temperature,
+      a.q_draft, a.any_sampling, a.seed, a.B, a.D, a.V, (float*)(ws + p.off_lse), (int*)(ws + p.off_amax),
+      (Decision*)(ws + p.off_dec), (int*)(ws + p.off_count), a.out_tokens, a.num_accepted, a.tie_flags, a.lse_out,
+      a.argmax_out, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !a.any_sampling) return e;
+  dim3 grid(a.B, p.race_slices);
+  accept_race_kernel<<<grid, kThreads, 0, s>>>((const float*)(ws + p.off_logits), a.q_draft,
+                                               (const float*)(ws + p.off_lse), (const Decision*)(ws + p.off_dec),
+                                               (RacePair*)(ws + p.off_race), (int*)(ws + p.off_count), a.seed, a.D,
+                                               a.V, a.out_tokens, a.tie_flags);
+  return cudaGetLastError();
+}
+
+__global__ void rng_debug_kernel(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t v0, int n,
+                                 uint32_t* __restrict__ word0, float* __restrict__ race_e,
+                                 float* __restrict__ accept_u) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t v = v0 + (uint32_t)i;
+  if (word0) word0[i] = philox_word0(seed, b, j, v, tag);
+  if (race_e) race_e[i] = race_exponential(seed, b, j, v, tag);
+  if (accept_u) accept_u[i] = accept_uniform(seed, b, v);
+}
+
+cudaError_t launch_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t v0, int n,
+                             uint32_t* word0, float* race_e, float* accept_u, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  rng_debug_kernel<<<(n + 255) / 256, 256, 0, s>>>(seed, b, j, tag, v0, n, word0, race_e, accept_u);
+  return cudaGetLastError();
+}
+
+size_t accept_decision_bytes() { return sizeof(Decision); }
+size_t accept_race_part_bytes() { return sizeof(RacePair); }
+
+}  // namespace mtp

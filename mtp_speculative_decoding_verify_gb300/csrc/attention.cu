@@ -1,0 +1,251 @@
+// Verify attention: KV append, SIMT attention (fp32 path), split combine.
+//
+// "Multi Token Prediction" note, overall flow for K=3 draft tokens, step 2:
+// the verify tokens' queries are batched against the reused KV cache and
+// every verify token's new K/V is written to the cache for the tokens after
+// it. "MTP in TensorRT-LLM", attention for MTP: with K+1 chained input
+// tokens a causal mask is all the attention kernel needs. Row j of a request
+// with ctx cached tokens therefore attends slots 0 .. ctx+j.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtp {
+
+// ------------------------------------------------------------------- append
+// One CTA per (request, verify token): copy that token's K (and V) rows into
+// slot ctx+j of the paged cache.
+template <typename T>
+__global__ void kv_append_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new, T* __restrict__ k_cache,
+                                 T* __restrict__ v_cache, const int32_t* __restrict__ block_table,
+                                 const int32_t* __restrict__ ctx_lens, int R, int Hkv, int d_qk, int d_v,
+                                 int max_blocks, int num_blocks, unsigned* err) {
+  const int b = blockIdx.x / R, j = blockIdx.x % R;
+  const int ctx = ctx_lens[b];
+  if (ctx < 0) {
+    if (threadIdx.x == 0) raise_error(err, MTP_ERR_LENGTH);
+    return;
+  }
+  const int slot = ctx + j;
+  const int page = slot / kBlock;
+  if (page >= max_blocks) {
+    if (threadIdx.x == 0) raise_error(err, MTP_ERR_LENGTH);
+    return;
+  }
+  const int blk = block_table[(int64_t)b * max_blocks + page];
+  if (blk < 0 || blk >= num_blocks) {
+    if (threadIdx.x == 0) raise_error(err, MTP_ERR_BLOCK_ID);
+    return;
+  }
+  const int64_t cache_row = (int64_t)blk * kBlock + (slot % kBlock);
+  const int nk = Hkv * d_qk;
+  const T* ks = k_new + ((int64_t)b * R + j) * nk;
+  T* kd = k_cache + cache_row * nk;
+  for (int e = threadIdx.x; e < nk; e += blockDim.x) kd[e] = ks[e];
+  if (v_new != nullptr) {
+    const int nv = Hkv * d_v;
+    const T* vs = v_new + ((int64_t)b * R + j) * nv;
+    T* vd = v_cache + cache_row * nv;
+    for (int e = threadIdx.x; e < nv; e += blockDim.x) vd[e] = vs[e];
+  }
+}
+
+cudaError_t launch_kv_append(const mtp_attn_args& a, unsigned* err, cudaStream_t s) {
+  const int R = a.D + 1;
+  const int Hkv = a.is_mla ? 1 : a.Hkv;
+  dim3 grid(a.B * R);
+  if (a.B == 0) return cudaSuccess;
+  if (a.dtype == MTP_F32) {
+    kv_append_kernel<float><<<grid, 128, 0, s>>>((const float*)a.k_new, (const float*)a.v_new, (float*)a.k_cache,
+                                                (float*)a.v_cache, a.block_table, a.ctx_lens, R, Hkv, a.d_qk, a.d_v,
+                                                a.max_blocks, a.num_blocks, err);
+  } else {
+    using bf = __nv_bfloat16;
+    kv_append_kernel<bf><<<grid, 128, 0, s>>>((const bf*)a.k_new, (const bf*)a.v_new, (bf*)a.k_cache,
+                                             (bf*)a.v_cache, a.block_table, a.ctx_lens, R, Hkv, a.d_qk, a.d_v,
+                                             a.max_blocks, a.num_blocks, err);
+  }
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------- plan
+static int rows_per_cta(const mtp_attn_args& a) {
+  if (a.dtype == MTP_F32) return 8;     // SIMT: one warp per row, 8 warps
+  if (a.is_mla) return 64;              // MLA tensor-core tile
+  return 16;                            // GQA tensor-core tile
+}
+
+AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
+  AttnPlan p{};
+  const int R = a.D + 1;
+  const int group = a.Hq / a.Hkv;
+  p.rows_per_kv = group * R;
+  const int row_tiles = (p.rows_per_kv + rows_per_cta(a) - 1) / rows_per_cta(a);
+  const int max_len = a.max_blocks * kBlock;
+  const long long base = (long long)a.B * (a.is_mla ? 1 : a.Hkv) * row_tiles;
+  const int kMaxSplitLen = 4096, kMinSplitLen = 256;
+  int n = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));
+  n = std::max(n, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
+  n = std::min(n, std::max(1, (max_len + kMinSplitLen - 1) / kMinSplitLen));
+  int split_len = (max_len + n - 1) / n;
+  split_len = (split_len + kBlock - 1) / kBlock * kBlock;
+  p.split_len = split_len;
+  p.n_splits = (max_len + split_len - 1) / split_len;
+  p.ws_bytes = 0;
+  if (p.n_splits > 1) {
+    const size_t rows = (size_t)a.B * R * a.Hq;
+    p.ws_partial_o = 0;
+    p.ws_partial_lse = rows * p.n_splits * a.d_v * sizeof(float);
+    p.ws_bytes = p.ws_partial_lse + rows * p.n_splits * sizeof(float);
+    p.ws_bytes = (p.ws_bytes + 255) / 256 * 256;
+  }
+  return p;
+}
+
+// -------------------------------------------------------------------- SIMT
+// One warp per query row; lane l holds elements l, l+32, ... of q and of the
+// running output. Online softmax over the keys of this CTA's split.
+template <typename T, int EQ, int EV>
+__global__ void __launch_bounds__(256) attention_simt_kernel(
+    const T* __restrict__ q, const T* __restrict__ k_cache, const T* __restrict__ v_cache,
+    const int32_t* __restrict__ block_table, const int32_t* __restrict__ ctx_lens, T* __restrict__ out,
+    float* __restrict__ part_o, float* __restrict__ part_lse, int R, int Hq, int Hkv, int group, int max_blocks,
+    int num_blocks, int split_len, int n_splits, int is_mla, float sm_scale, unsigned* err) {
+  constexpr int DQ = EQ * kWarp, DV = EV * kWarp;
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  const int split = blockIdx.x;
+  const int b = blockIdx.y / Hkv, kvh = blockIdx.y % Hkv;
+  const int r = blockIdx.z * (blockDim.x / kWarp) + warp;
+  if (r >= group * R) return;
+  const int j = r / group, h = kvh * group + r % group;
+  const int ctx = ctx_lens[b];
+  const int L = ctx + j + 1;
+  if (ctx < 0 || ctx + R > max_blocks * kBlock) {
+    if (lane == 0 && split == 0) raise_error(err, MTP_ERR_LENGTH);
+    return;
+  }
+  const int t0 = split * split_len;
+  if (t0 >= L) return;
+  const int t1 = min(L, t0 + split_len);
+
+  const int64_t row = ((int64_t)b * R + j) * Hq + h;
+  float qv[EQ];
+#pragma unroll
+  for (int i = 0; i < EQ; ++i) qv[i] = Num<T>::to_f(q[row * DQ + i * kWarp + lane]) * sm_scale;
+  float acc[EV];
+#pragma unroll
+  for (int i = 0; i < EV; ++i) acc[i] = 0.0f;
+  float m = -INFINITY, l = 0.0f;
+  const int kv_heads = is_mla ? 1 : Hkv;
+  const int32_t* tbl = block_table + (int64_t)b * max_blocks;
+  for (int t = t0; t < t1; ++t) {
+    const int blk = tbl[t / kBlock];
+    if (blk < 0 || blk >= num_blocks) {
+      if (lane == 0) raise_error(err, MTP_ERR_BLOCK_ID);
+      continue;
+    }
+    const int64_t slot = (int64_t)blk * kBlock + (t % kBlock);
+    const T* kp = k_cache + (slot * kv_heads + (is_mla ? 0 : kvh)) * DQ;
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EQ; ++i) dot += qv[i] * Num<T>::to_f(kp[i * kWarp + lane]);
+    const float sc = warp_sum(dot);
+    const float m_new = fmaxf(m, sc);
+    const float corr = expf(m - m_new);
+    const float pr = expf(sc - m_new);
+    l = l * corr + pr;
+    const T* vp = is_mla ? kp : v_cache + (slot * kv_heads + kvh) * DV;
+#pragma unroll
+    for (int i = 0; i < EV; ++i) acc[i] = acc[i] * corr + pr * Num<T>::to_f(vp[i * kWarp + lane]);
+    m = m_new;
+  }
+  const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+  if (n_splits == 1) {
+#pragma unroll
+    for (int i = 0; i < EV; ++i) out[row * DV + i * kWarp + lane] = Num<T>::from_f(acc[i] * inv_l);
+  } else {
+    float* po = part_o + (row * n_splits + split) * DV;
+#pragma unroll
+    for (int i = 0; i < EV; ++i) po[i * kWarp + lane] = acc[i] * inv_l;
+    if (lane == 0) part_lse[row * n_splits + split] = m + logf(l);
+  }
+}
+
+template <typename T, int EQ, int EV>
+static void run_simt(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s) {
+  const int R = a.D + 1, group = a.Hq / a.Hkv;
+  const int kv_heads = a.is_mla ? 1 : a.Hkv;
+  dim3 grid(p.n_splits, a.B * kv_heads, (group * R + 7) / 8);
+  float* po = p.n_splits > 1 ? (float*)((char*)a.workspace + p.ws_partial_o) : nullptr;
+  float* pl = p.n_splits > 1 ? (float*)((char*)a.workspace + p.ws_partial_lse) : nullptr;
+  attention_simt_kernel<T, EQ, EV><<<grid, 256, 0, s>>>(
+      (const T*)a.q, (const T*)a.k_cache, (const T*)a.v_cache, a.block_table, a.ctx_lens, (T*)a.out, po, pl, R,
+      a.Hq, kv_heads, group, a.max_blocks, a.num_blocks, p.split_len, p.n_splits, a.is_mla, a.sm_scale, err);
+}
+
+cudaError_t launch_attention_simt(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  using bf = __nv_bfloat16;
+  if (a.dtype == MTP_F32) {
+    if (a.d_qk == 64 && a.d_v == 64) run_simt<float, 2, 2>(a, p, err, s);
+    else if (a.d_qk == 128 && a.d_v == 128) run_simt<float, 4, 4>(a, p, err, s);
+    else return cudaErrorInvalidValue;
+  } else {
+    if (a.is_mla && a.d_qk == 576 && a.d_v == 512) run_simt<bf, 18, 16>(a, p, err, s);
+    else if (a.d_qk == 64 && a.d_v == 64) run_simt<bf, 2, 2>(a, p, err, s);
+    else if (a.d_qk == 128 && a.d_v == 128) run_simt<bf, 4, 4>(a, p, err, s);
+    else return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per (request, row, head): merge the non-empty splits with
+// weights exp(lse_s - LSE).
+template <typename T>
+__global__ void attention_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                         const int32_t* __restrict__ ctx_lens, T* __restrict__ out, int B, int R,
+                                         int Hq, int d_v, int split_len, int n_splits, int max_len) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp, lane = threadIdx.x % kWarp;
+  const int rows = B * R * Hq;
+  if (warp >= rows) return;
+  const int b = warp / (R * Hq), j = (warp / Hq) % R;
+  const int ctx = ctx_lens[b];
+  if (ctx < 0 || ctx + R > max_len) return;
+  const int L = ctx + j + 1;
+  const int ns = min(n_splits, (L + split_len - 1) / split_len);
+  const float* lse = part_lse + (int64_t)warp * n_splits;
+  float mx = -INFINITY;
+  for (int sp = 0; sp < ns; ++sp) mx = fmaxf(mx, lse[sp]);
+  float denom = 0.0f;
+  for (int sp = 0; sp < ns; ++sp) denom += expf(lse[sp] - mx);
+  const float inv = 1.0f / denom;
+  for (int e = lane; e < d_v; e += kWarp) {
+    float acc = 0.0f;
+    for (int sp = 0; sp < ns; ++sp) acc += expf(lse[sp] - mx) * part_o[((int64_t)warp * n_splits + sp) * d_v + e];
+    out[(int64_t)warp * d_v + e] = Num<T>::from_f(acc * inv);
+  }
+}
+
+cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s) {
+  if (p.n_splits == 1 || a.B == 0) return cudaSuccess;
+  const int R = a.D + 1;
+  const int rows = a.B * R * a.Hq;
+  const int threads = 256;
+  const int blocks = (rows * kWarp + threads - 1) / threads;
+  const float* po = (const float*)((const char*)a.workspace + p.ws_partial_o);
+  const float* pl = (const float*)((const char*)a.workspace + p.ws_partial_lse);
+  if (a.dtype == MTP_F32)
+    attention_combine_kernel<float><<<blocks, threads, 0, s>>>(po, pl, a.ctx_lens, (float*)a.out, a.B, R, a.Hq,
+                                                               a.d_v, p.split_len, p.n_splits, a.max_blocks * kBlock);
+  else
+    attention_combine_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(po, pl, a.ctx_lens, (__nv_bfloat16*)a.out,
+                                                                       a.B, R, a.Hq, a.d_v, p.split_len, p.n_splits,
+                                                                       a.max_blocks * kBlock);
+  return cudaGetLastError();
+}
+
+}  // namespace mtp

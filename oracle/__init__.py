@@ -27,7 +27,7 @@ def lib():
         L.oracle_philox4x32_10.restype = None
         L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 8
         L.oracle_verify_attention.restype = i32
-        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 6
+        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7
         L.oracle_lmhead_accept.restype = i32
         L.oracle_kv_rollback.argtypes = [i32] * 4 + [P] * 5
         L.oracle_kv_rollback.restype = i32
@@ -112,7 +112,8 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *
     return out
 
 
-def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, want_logits=False):
+def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, want_logits=False,
+                  request_index=None):
     """LM head + row statistics + acceptance. Returns a dict of numpy arrays."""
     hidden, dt = _storage(hidden)
     lm_head, dt2 = _storage(lm_head)
@@ -130,8 +131,9 @@ def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, 
     lse = np.zeros((B, R), np.float32)
     amax = np.zeros((B, R), np.int32)
     logits = np.zeros((B * R, V), np.float32) if want_logits else None
+    rid = None if request_index is None else _c(request_index, np.int32)
     rc = lib().oracle_lmhead_accept(B, D, H, V, dt, _ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode),
-                                    _ptr(temperature), _ptr(q_draft), ctypes.c_uint64(seed), _ptr(out_tokens),
+                                    _ptr(temperature), _ptr(q_draft), ctypes.c_uint64(seed), _ptr(rid), _ptr(out_tokens),
                                     _ptr(num_acc), _ptr(ties), _ptr(lse), _ptr(amax), _ptr(logits))
     if rc != 0:
         raise ValueError("oracle_lmhead_accept returned %d" % rc)

@@ -71,7 +71,7 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                                     const void* hidden, const void* lm_head,
                                     const int32_t* tokens, const uint8_t* mode,
                                     const float* temperature, const float* q_draft,
-                                    uint64_t seed,
+                                    uint64_t seed, const int32_t* request_index,
                                     int32_t* out_tokens, int32_t* num_accepted,
                                     uint8_t* tie_flags, float* lse_out,
                                     int32_t* argmax_out, float* logits_out) {
@@ -87,6 +87,7 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
       int tok = tokens[(int64_t)b * R + j];
       if (tok < 0 || tok >= V) return ORACLE_BAD_INDEX;
     }
+    const uint32_t rid = request_index ? (uint32_t)request_index[b] : (uint32_t)b;
     const bool sampling = mode[b] == 1 && temperature != NULL && temperature[b] > 0.0f;
     if (sampling && q_draft == NULL) return ORACLE_BAD_ARG;
     const float inv_t = sampling ? 1.0f / temperature[b] : 1.0f;
@@ -137,7 +138,7 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
         int x = tok[j + 1];
         pd[j] = expf(logits[(size_t)j * V + x] - lse[j]);
         qd[j] = q_draft[((int64_t)b * D + j) * V + x];
-        U[j] = oracle_accept_uniform(seed, (uint32_t)b, (uint32_t)j);
+        U[j] = oracle_accept_uniform(seed, rid, (uint32_t)j);
       }
       n = oracle_accept_prefix(D, pd.data(), qd.data(), U.data(), &tie);
       for (int j = 0; j < n; ++j) out[j] = tok[j + 1];
@@ -150,7 +151,7 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
         float qv = n < D ? q_draft[((int64_t)b * D + n) * V + v] : 0.0f;
         float r = p[v] - qv;
         w[v] = r > 0.0f ? r : 0.0f;
-        E[v] = oracle_race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag);
+        E[v] = oracle_race_exponential(seed, rid, (uint32_t)n, (uint32_t)v, tag);
       }
       uint8_t race_tie = 0;
       int winner = oracle_race(V, w.data(), E.data(), &race_tie);

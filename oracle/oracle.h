@@ -74,6 +74,9 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
  *   temperature <= 0 is decided greedily: the T -> 0 limit)
  *   temperature [B] (may be NULL when every request is greedy)
  *   q_draft [B, D, V] fp32 (may be NULL when every request is greedy)
+ *   request_index [B]: the request number used as counter word 0 of the
+ *   random stream (NULL: 0 .. B-1), so that a subset of a batch draws the
+ *   same numbers as the full batch
  * Outputs: out_tokens [B, R] (-1 padded), num_accepted [B] (drafts accepted,
  * 0..D; emitted = num_accepted + 1), tie_flags [B] (bit0: |p - U q| < 1e-5 q
  * at a decision; bit1: top-2 race keys within 1e-5 relative), and optional
@@ -82,7 +85,7 @@ int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                          const void* hidden, const void* lm_head,
                          const int32_t* tokens, const uint8_t* mode,
                          const float* temperature, const float* q_draft,
-                         uint64_t seed,
+                         uint64_t seed, const int32_t* request_index,
                          int32_t* out_tokens, int32_t* num_accepted,
                          uint8_t* tie_flags, float* lse_out,
                          int32_t* argmax_out, float* logits_out);

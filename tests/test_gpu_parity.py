@@ -1,0 +1,295 @@
+"""GPU parity: the library's CUDA path against the CPU oracle, element by
+element, on the same seeded inputs.
+
+  * reduced workloads (every request compared): several vocab tiles with a
+    ragged tail, contexts that straddle block boundaries, both dtypes;
+  * the standard workloads at full size, in the benchmark's launch
+    configuration: a sample of requests compared with the oracle one by one,
+    and properties checked on every request;
+  * edge cases: D = 0, D = 15, empty context, tiny vocabularies, a single
+    request, device-side range checks.
+"""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU hosts too; the marker keeps them out of -m "not gpu"
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import oracle  # noqa: E402
+import mtp_speculative_decoding_verify_gb300 as mv  # noqa: E402
+from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
+from gpu_util import (A, TOL_ATTN, TOL_LOGITS, TOL_LSE_REL, check_invariants, compare_accept,  # noqa: E402
+                      gpu_attention, gpu_lmhead, gpu_rollback, oracle_attention, oracle_lmhead)
+from philox_py import philox_vec, race_exponential_vec  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+SMALL = {
+    "cfg0": synth.CFG0,
+    "cfg1_small_mla": synth.CFG1.with_(name="MLA bf16 small", B=4, Hq=16, ctx=(60, 300), H=512, V=3037),
+    "cfg2_small_gqa_sampling": synth.CFG2.with_(name="GQA bf16 sampling small", B=6, Hq=16, Hkv=2, ctx=(300, 300),
+                                                H=256, V=5003),
+    "cfg3_small_mixed": synth.CFG3.with_(name="GQA bf16 mixed small", B=8, Hq=8, Hkv=2, ctx=(64, 700), H=256,
+                                         V=7001),
+    "mha_bf16_d64": synth.CFG0.with_(name="MHA bf16 d64", dtype="bf16", ctx=(0, 200), B=5, H=128, V=999),
+}
+
+
+def _par(fn, items, workers=8):
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, items))
+
+
+def _stack(results):
+    keys = results[0].keys()
+    return {k: np.concatenate([r[k] for r in results]) for k in keys}
+
+
+def _oracle_lm_parallel(w, lm, reqs, want_logits=False):
+    W = A(lm["lm_head"])
+    return _stack(_par(lambda b: oracle_lmhead(w, lm, [b], W, want_logits), list(reqs)))
+
+
+def _oracle_attn_parallel(w, att, reqs):
+    return np.concatenate(_par(lambda b: oracle_attention(w, att, [b]), list(reqs)))
+
+
+def _check_attention(w, att, out, reqs):
+    ref = _oracle_attn_parallel(w, att, reqs)
+    got = out.index_select(0, torch.tensor(list(reqs), device=DEV)).float().cpu().numpy()
+    ref = ref.astype(np.float32) if ref.dtype == np.float32 else \
+        torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy()
+    err = float(np.abs(got - ref).max())
+    assert err < TOL_ATTN[w.dtype], err
+    return err
+
+
+def _check_append(w, att, att_before_knew):
+    """The verify slots of the cache hold exactly the verify tokens' K (and V)."""
+    table = A(att["block_table"])
+    ctx = A(att["ctx_lens"])
+    for b in range(min(w.B, 8)):
+        for j in range(w.R):
+            s = int(ctx[b]) + j
+            blk = int(table[b, s // 64])
+            got = att["k_cache"][blk, s % 64]
+            exp = att_before_knew[b, j].reshape(got.shape)
+            assert torch.equal(got, exp)
+
+
+def _full_check_lm(w, lm, gpu, reqs, logits=False):
+    ref = _oracle_lm_parallel(w, lm, reqs, want_logits=logits)
+    flagged = compare_accept(gpu, ref, reqs)
+    idx = torch.tensor(list(reqs), device=DEV)
+    lse = gpu["lse"].index_select(0, idx).cpu().numpy()
+    np.testing.assert_allclose(lse, ref["lse"], rtol=TOL_LSE_REL, atol=1e-6)
+    assert (gpu["argmax"].index_select(0, idx).cpu().numpy() == ref["argmax"]).all()
+    if logits:
+        rows = torch.tensor([b * w.R + j for b in reqs for j in range(w.R)], device=DEV)
+        gl = gpu["logits"].index_select(0, rows).cpu().numpy()
+        err = float(np.abs(gl - ref["logits"]).max())
+        assert err < TOL_LOGITS[w.dtype], err
+    return flagged
+
+
+def _check_rollback(w, att, gpu_n):
+    table, seq, fl, fc = gpu_rollback(w, att["block_table"], att["ctx_lens"], gpu_n)
+    t_h = A(att["block_table"]).copy()
+    s_h = A(att["ctx_lens"]).copy()
+    fl_h = np.full(fl.numel(), -1, np.int32)
+    fc_h = np.zeros(1, np.int32)
+    oracle.kv_rollback(t_h, s_h, gpu_n.cpu().numpy(), fl_h, fc_h, D=w.D, block_size=64)
+    assert (seq.cpu().numpy() == s_h).all()
+    assert (table.cpu().numpy() == t_h).all()
+    assert int(fc.item()) == int(fc_h[0])
+    assert (fl.cpu().numpy() == fl_h).all()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workload_all_requests(name):
+    w = SMALL[name]
+    att = synth.make_attention_inputs(w, DEV)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    k_new = att["k_new"].clone()
+    out = gpu_attention(w, att)
+    gpu = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    _check_append(w, att, k_new)
+    _check_attention(w, att, out, range(w.B))
+    flagged = _full_check_lm(w, lm, gpu, range(w.B), logits=True)
+    assert flagged <= max(1, w.B // 20)
+    check_invariants(w, lm, gpu)
+    _check_rollback(w, att, gpu["num_accepted"])
+    mv.sync_status()
+
+
+FULL = {
+    "cfg1_D3": (synth.CFG1, [0, 31]),
+    "cfg1_D1": (synth.CFG1.with_(D=1), [5]),
+    "cfg2": (synth.CFG2, [0, 63]),
+    "cfg3": (synth.CFG3, [0, 127, 128, 255]),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled_requests(name):
+    w, reqs = FULL[name]
+    torch.cuda.empty_cache()
+    att = synth.make_attention_inputs(w, DEV)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    k_new = att["k_new"].clone()
+    out = gpu_attention(w, att)
+    gpu = gpu_lmhead(w, lm)
+    mv.sync_status()
+    _check_append(w, att, k_new)
+    _check_attention(w, att, out, reqs)
+    flagged = _full_check_lm(w, lm, gpu, reqs)
+    assert flagged <= 1
+    check_invariants(w, lm, gpu)
+    if w.sampling == "none" or w.sampling == "half":
+        # Planted targets: greedy rows' argmax is the planted token.
+        greedy = [b for b in range(w.B) if int(lm["mode"][b]) == 0]
+        amax = gpu["argmax"].cpu().numpy()
+        assert (amax[greedy] == lm["planted"].numpy()[greedy]).all()
+    _check_rollback(w, att, gpu["num_accepted"])
+    del att, lm, out, gpu
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B,D", [(1, 7), (8, 1)])
+def test_sweep_points_sampled(B, D):
+    w = synth.sweep_point(B, D)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    gpu = gpu_lmhead(w, lm)
+    mv.sync_status()
+    reqs = [0] if B == 1 else [0, B - 1]
+    assert _full_check_lm(w, lm, gpu, reqs) <= 1
+    check_invariants(w, lm, gpu)
+
+
+EDGE = {
+    "D0": synth.CFG0.with_(name="D=0", D=0, dtype="bf16", H=64, V=300),
+    "D15": synth.CFG0.with_(name="D=15", D=15, dtype="bf16", H=64, V=300, ctx=(50, 130), sampling="half"),
+    "ctx0_fp32": synth.CFG0.with_(name="empty context", ctx=(0, 0), V=50, H=16),
+    "tiny_vocab_sampling": synth.CFG0.with_(name="V=7 sampling", V=7, H=8, sampling="all", B=16),
+    "single_request": synth.CFG1.with_(name="B=1 MLA", B=1, Hq=8, ctx=(63, 63), H=64, V=130),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases(name):
+    w = EDGE[name]
+    att = synth.make_attention_inputs(w, DEV)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    out = gpu_attention(w, att)
+    gpu = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    _check_attention(w, att, out, range(w.B))
+    _full_check_lm(w, lm, gpu, range(w.B), logits=True)
+    check_invariants(w, lm, gpu)
+    _check_rollback(w, att, gpu["num_accepted"])
+
+
+def test_rng_streams_bit_exact():
+    n = 1 << 20
+    for seed, b, j, tag in ((0, 0, 0, 2), (0x1234_5678_9ABC, 77, 5, 3)):
+        word0, E, U = mv._binding.rng_debug(seed, b, j, tag, 0, n)
+        ref = philox_vec(np.full(n, b), np.full(n, j), np.arange(n), np.full(n, tag), seed & 0xFFFFFFFF, seed >> 32)[0]
+        assert (word0 == ref).all()
+        refE = race_exponential_vec(seed, b, j, np.arange(n), tag)
+        np.testing.assert_array_max_ulp(E, refE, maxulp=2)
+        for v in (0, 1, 12345, n - 1):
+            assert U[v] == oracle.accept_uniform(seed, b, v)
+            assert abs(E[v] - oracle.race_exponential(seed, b, j, v, tag)) <= 2 * np.spacing(E[v])
+
+
+def test_lossless_sampling_on_gpu_chi2():
+    """Through the GPU path: the first emitted token follows p_target exactly."""
+    from scipy import special, stats
+    rng = np.random.default_rng(5)
+    trials, D, V = 200_000, 2, 8
+    logits = (rng.standard_normal((D + 1, V)) * 1.2).astype(np.float32)
+    q = special.softmax(rng.standard_normal((D, V)) * 1.2, axis=1).astype(np.float32)
+    hidden = torch.tensor(np.tile(logits, (trials, 1)), device=DEV)
+    W = torch.eye(V, dtype=torch.float32, device=DEV)
+    tokens = np.zeros((trials, D + 1), np.int32)
+    for j in range(D):
+        tokens[:, j + 1] = rng.choice(V, size=trials, p=q[j] / q[j].sum())
+    lm = dict(hidden=hidden, lm_head=W, tokens=torch.tensor(tokens, device=DEV),
+              mode=torch.ones(trials, dtype=torch.uint8, device=DEV),
+              temperature=torch.ones(trials, dtype=torch.float32, device=DEV),
+              q_draft=torch.tensor(np.broadcast_to(q, (trials, D, V)).copy(), device=DEV), seed=99)
+    w = synth.CFG0.with_(B=trials, D=D, V=V, H=V)
+    gpu = gpu_lmhead(w, lm)
+    first = gpu["out_tokens"][:, 0].cpu().numpy()
+    p = special.softmax(logits.astype(np.float64), axis=1)
+    assert stats.chisquare(np.bincount(first, minlength=V), p[0] * trials).pvalue > 1e-3
+    # Acceptance rate of draft 1 equals sum_v min(p, q).
+    alpha = np.minimum(p[0], q[0]).sum()
+    rate = (gpu["num_accepted"].cpu().numpy() >= 1).mean()
+    assert abs(rate - alpha) < 4 * np.sqrt(alpha * (1 - alpha) / trials)
+    # And the GPU agrees with the oracle request by request on a sample.
+    sample = list(range(0, trials, 4001))
+    ref = oracle.lmhead_accept(np.tile(logits, (len(sample), 1)), np.eye(V, dtype=np.float32), tokens[sample],
+                               np.ones(len(sample), np.uint8), np.ones(len(sample), np.float32),
+                               np.broadcast_to(q, (len(sample), D, V)).copy(), 99,
+                               request_index=np.array(sample, np.int32))
+    assert compare_accept(gpu, ref, sample) <= 1
+
+
+def test_rollback_many_requests_and_capacity():
+    rng = np.random.default_rng(11)
+    w = synth.CFG3.with_(B=3000, D=5)
+    ctx = rng.integers(0, 500, w.B).astype(np.int32)
+    need = (ctx + w.R + 63) // 64
+    max_blocks = int(need.max()) + 1
+    table = np.full((w.B, max_blocks), -1, np.int32)
+    perm = rng.permutation(int(need.sum())).astype(np.int32)
+    pos = 0
+    for b in range(w.B):
+        table[b, :need[b]] = perm[pos:pos + need[b]]
+        pos += need[b]
+    n = rng.integers(0, w.D + 1, w.B).astype(np.int32)
+    t_d = torch.tensor(table, device=DEV)
+    c_d = torch.tensor(ctx, device=DEV)
+    n_d = torch.tensor(n, device=DEV)
+    cap = 4 * w.B
+    g_table, g_seq, g_fl, g_fc = gpu_rollback(w, t_d, c_d, n_d, capacity=cap)
+    mv.sync_status()
+    fl = np.full(cap, -1, np.int32)
+    fc = np.zeros(1, np.int32)
+    t_h, s_h = table.copy(), ctx.copy()
+    oracle.kv_rollback(t_h, s_h, n, fl, fc, D=w.D, block_size=64)
+    assert (g_seq.cpu().numpy() == s_h).all() and (g_table.cpu().numpy() == t_h).all()
+    assert int(g_fc.item()) == int(fc[0]) and (g_fl.cpu().numpy() == fl).all()
+    # A free list that is too short is reported, not overrun.
+    g_table, g_seq, g_fl, g_fc = gpu_rollback(w, t_d, c_d, n_d, capacity=10)
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert ei.value.code == 4
+    assert int(g_fc.item()) == 10
+
+
+def test_device_range_checks_report_and_recover():
+    w = SMALL["cfg3_small_mixed"]
+    att = synth.make_attention_inputs(w, DEV)
+    att["block_table"][1, 0] = 10 ** 6          # block id beyond the cache: skipped and reported
+    gpu_attention(w, att)
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert ei.value.code == 4 and "block-id" in str(ei.value)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    lm["tokens"][2, 1] = w.V + 5                # draft id beyond the vocabulary
+    gpu_lmhead(w, lm)
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert "token-id" in str(ei.value)
+    # The context stays usable: a clean call afterwards succeeds.
+    w0 = SMALL["cfg0"]
+    gpu_lmhead(w0, synth.make_lmhead_inputs(w0, DEV))
+    mv.sync_status()
