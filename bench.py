@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Benchmark of one MTP verify step on GB300.
+
+A step is the whole verify path for one batch: mtp_verify_attention (KV
+append + multi-query verify attention), mtp_verify_logits_accept (LM head
+with streaming softmax statistics + acceptance) and kv_rollback, on seeded
+synthetic inputs already resident in HBM. The default workload is the
+DeepSeek-V3-shaped greedy MTP batch (B=32 requests, D=3 drafts, absorbed MLA
+128 heads x 576/512, contexts 512-4096, hidden 7168, vocab 129280, bf16).
+
+Output: one JSON line on rank 0 with requests/s (value), accepted tokens/s,
+the roofline of the dominant kernel, an end-to-end number through the C ABI
+with host buffers, and a CPU baseline (the oracle on a bounded sample).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch
+(requests are independent, so the step shards by request with no
+collective); value = total requests of all ranks / max-over-ranks time.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
+
+METRIC = "verify-step requests/s and accepted tokens/s on 1 GB300; % of HBM/TC roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workloads():
+    return {
+        "cfg1_D3": synth.CFG1,
+        "cfg1_D1": synth.CFG1.with_(D=1),
+        "cfg0": synth.CFG0,
+        "cfg2": synth.CFG2,
+        "cfg3": synth.CFG3,
+        **{"sweep_B%d_D%d" % (B, D): synth.sweep_point(B, D) for B in (1, 8, 64, 256, 512) for D in (1, 3, 5, 7)},
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def elem_bytes(w):
+    return 4 if w.dtype == "f32" else 2
+
+
+def algorithmic(w, ctx):
+    """Algorithmic bytes and flops of one step: KV read once (ctx + R keys per
+    request and KV head), W read once; flops of the LM head and attention."""
+    eb = elem_bytes(w)
+    R = w.R
+    keys = float(np.sum(ctx + R))
+    if w.is_mla:
+        kv_bytes = keys * w.d_qk * eb
+        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * float(np.sum([sum(c + j + 1 for j in range(R)) for c in ctx]))
+    else:
+        kv_bytes = keys * w.Hkv * (w.d_qk + w.d_v) * eb
+        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * float(np.sum([sum(c + j + 1 for j in range(R)) for c in ctx]))
+    w_bytes = float(w.V) * w.H * eb
+    lm_flops = 2.0 * w.M * w.H * w.V
+    return dict(kv_bytes=kv_bytes, w_bytes=w_bytes, attn_flops=attn_flops, lm_flops=lm_flops)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+class Step:
+    """The three C-ABI calls of one verify step, with argument structs built once."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        from mtp_speculative_decoding_verify_gb300 import _binding as B
+        self.B = B
+        self.L = B.lib()
+        self.w = w.with_(seed=w.seed + seed_offset)
+        w = self.w
+        self.att = synth.make_attention_inputs(w, dev)
+        self.lm = synth.make_lmhead_inputs(w, dev)
+        att, lm = self.att, self.lm
+        self.out = torch.empty((w.B, w.R, w.Hq, w.d_v), dtype=w.torch_dtype, device=dev)
+        self.out_tokens = torch.empty((w.B, w.R), dtype=torch.int32, device=dev)
+        self.num_acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+        self.ties = torch.empty(w.B, dtype=torch.uint8, device=dev)
+        self.table_work = att["block_table"].clone()
+        self.seq = att["ctx_lens"].clone()
+        self.free_list = torch.full((w.B * 2 + 8,), -1, dtype=torch.int32, device=dev)
+        self.free_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.a_attn = B.attn_args(att["q"], att["k_new"], att["v_new"], att["k_cache"], att["v_cache"],
+                                  att["block_table"], att["ctx_lens"], self.out, sm_scale=w.sm_scale)
+        self.a_lm = B.lm_args(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
+                              lm["q_draft"], lm["seed"], self.out_tokens, self.num_acc, self.ties)
+        self.a_rb = B.rollback_args(self.table_work, self.seq, self.num_acc, self.free_list, self.free_count, D=w.D)
+        self.launches = 0
+
+    def set_events(self, attn_pair, lm_pair):
+        for args, pair in ((self.a_attn, attn_pair), (self.a_lm, lm_pair)):
+            args.timing_events[0] = pair[0].cuda_event if pair else None
+            args.timing_events[1] = pair[1].cuda_event if pair else None
+
+    def run(self, stream):
+        h = ctypes.c_void_p(stream.cuda_stream)
+        # Reset the rollback's bookkeeping so every step starts from the same state.
+        self.table_work.copy_(self.att["block_table"])
+        self.seq.copy_(self.att["ctx_lens"])
+        self.free_count.zero_()
+        L, chk = self.L, self.B._check
+        chk(L.mtp_verify_attention(ctypes.byref(self.a_attn), h))
+        n = L.mtp_last_launch_count()
+        chk(L.mtp_verify_logits_accept(ctypes.byref(self.a_lm), h))
+        n += L.mtp_last_launch_count()
+        chk(L.kv_rollback(ctypes.byref(self.a_rb), h))
+        n += L.mtp_last_launch_count()
+        self.launches = n
+
+
+def combine_ranks(ms, e2e_ms, emitted, world, device):
+    """Whole-job figures: the slowest rank's times and the total tokens emitted."""
+    if world == 1:
+        return ms, e2e_ms, emitted
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    e = torch.tensor([emitted], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(e, op=torch.distributed.ReduceOp.SUM)
+    return float(t[0]), float(t[1]), float(e[0])
+
+
+def event_pairs(n):
+    """Timing event pairs; each is recorded once so its CUDA event exists before
+    its handle goes into an argument struct."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in pairs:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    return pairs
+
+
+def run_gpu(args, w, rank, world, dev):
+    stream = torch.cuda.current_stream()
+    step = Step(w, dev, seed_offset=rank)
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    step.B.sync_status()
+
+    K = args.steps
+    ev_attn, ev_lm = event_pairs(K), event_pairs(K)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    launches = 0
+    for k in range(K):
+        step.set_events(ev_attn[k], ev_lm[k])
+        step.run(stream)
+        launches += step.launches
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    step.set_events(None, None)
+    step.B.sync_status()
+    ms = t0.elapsed_time(t1) / K
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
+    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_lm)
+    n_acc = step.num_acc.cpu().numpy()
+    ctx = step.att["ctx_lens"].cpu().numpy().astype(np.int64)
+
+    # End to end through the public API with host buffers: each step copies its
+    # inputs from pinned host memory, runs the three calls and reads the
+    # accept result back.
+    host = {k: step.att[k].cpu().pin_memory() for k in ("q", "k_new", "ctx_lens")}
+    host.update({k: step.lm[k].cpu().pin_memory() for k in ("hidden", "tokens")})
+    dev_t = {"q": step.att["q"], "k_new": step.att["k_new"], "ctx_lens": step.att["ctx_lens"],
+             "hidden": step.lm["hidden"], "tokens": step.lm["tokens"]}
+    res_tok = torch.empty_like(step.out_tokens, device="cpu").pin_memory()
+    res_n = torch.empty_like(step.num_acc, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = res_tok.numel() * 4 + res_n.numel() * 4
+    for _ in range(max(1, args.warmup // 2)):
+        step.run(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e2e_t0 = time.perf_counter()
+    for _ in range(K):
+        for k, t in host.items():
+            dev_t[k].copy_(t, non_blocking=True)
+        step.run(stream)
+        res_tok.copy_(step.out_tokens, non_blocking=True)
+        res_n.copy_(step.num_acc, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - e2e_t0) * 1e3 / K
+
+    ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, float(n_acc.sum() + w.B), world, dev)
+    return dict(ms=ms, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
+                clocks=clocks, launches=launches, h2d=h2d, d2h=d2h)
+
+
+def cpu_baseline(w, seconds, dev=None):
+    """The oracle, as it stands, on a bounded sample of the same workload:
+    whole requests (attention + LM head + acceptance + rollback), one thread."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
+    gen_dev = dev if dev is not None else torch.device("cpu")
+    att = synth.make_attention_inputs(w, gen_dev)
+    lm = synth.make_lmhead_inputs(w, gen_dev)
+    W = synth.as_oracle_array(lm["lm_head"])
+    table = synth.as_oracle_array(att["block_table"])
+    ctx = synth.as_oracle_array(att["ctx_lens"])
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b = done % w.B
+        oracle_attention(w, att, [b])
+        r = oracle_lmhead(w, lm, [b], W)
+        t = table[b:b + 1].copy()
+        s = ctx[b:b + 1].copy()
+        fl = np.zeros(w.D // 64 + 4, np.int32)
+        fc = np.zeros(1, np.int32)
+        oracle.kv_rollback(t, s, r["num_accepted"], fl, fc, D=w.D, block_size=64)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 4 * w.B:
+            break
+    return dict(value=done / el, unit="requests/s", cores=1, kind="oracle",
+                sample="%d request(s) of the %d-request batch (attention + LM head + acceptance + rollback), "
+                       "single-threaded oracle, %.1f s" % (done, w.B, el))
+
+
+def json_line(**kw):
+    print(json.dumps(kw), flush=True)
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the CPU oracle on the host cores, timed per step on a
+    bounded sample (one request per step) of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
+    gen_dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if torch.cuda.is_available() else "cpu"
+    att = synth.make_attention_inputs(w, gen_dev)
+    lm = synth.make_lmhead_inputs(w, gen_dev)
+    W = synth.as_oracle_array(lm["lm_head"])
+    table = synth.as_oracle_array(att["block_table"])
+    ctx = synth.as_oracle_array(att["ctx_lens"])
+
+    def one(b):
+        oracle_attention(w, att, [b])
+        r = oracle_lmhead(w, lm, [b], W)
+        fl = np.zeros(8, np.int32)
+        fc = np.zeros(1, np.int32)
+        oracle.kv_rollback(table[b:b + 1].copy(), ctx[b:b + 1].copy(), r["num_accepted"], fl, fc, D=w.D,
+                           block_size=64)
+    for i in range(args.warmup):
+        one(i % w.B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one((args.warmup + i) % w.B)
+    el = time.perf_counter() - t0
+    rps = args.steps / el
+    sample = "1 request per step of the %d-request batch (attention + LM head + acceptance + rollback), " \
+             "single-threaded oracle" % w.B
+    json_line(impl="reference", metric=METRIC, value=rps, unit="requests/s", n_gpus=world, steps=args.steps,
+              warmup=args.warmup, ms_per_step=el * 1e3 / args.steps, higher_is_better=True, scaling="weak",
+              vs_baseline=None, dtype=w.dtype, data="synthetic", config=config_of(w, args),
+              cpu_baseline=dict(value=rps, unit="requests/s", cores=1, kind="oracle", sample=sample),
+              e2e=dict(value=rps, unit="requests/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "D": w.D, "parallelism": "request-sharded replicas",
+            "l2": "inputs larger than L2 (LM-head weights %.2f GB streamed every step)" % (w.V * w.H * elem_bytes(w) / 1e9)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg1_D3", choices=sorted(workloads()))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workloads()[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+
+    r = run_gpu(args, w, rank, world, dev)
+    if rank != 0:
+        torch.distributed.destroy_process_group() if world > 1 else None
+        return
+    peaks, src = load_peaks()
+    alg = algorithmic(w, r["ctx"])
+    hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])
+    # Dominant kernel: the LM head (HBM-bound on W below M ~ 290 rows, tensor-bound above).
+    ridge = tc_peak * 1e12 / (hbm * 1e9)
+    lm_intensity = alg["lm_flops"] / alg["w_bytes"]
+    if lm_intensity < ridge or w.dtype == "f32":
+        roof = dict(kernel="lm_head", bound="hbm", achieved=alg["w_bytes"] / (r["lm_ms"] * 1e-3) / 1e9, peak=hbm,
+                    unit="GB/s", peak_source=src + " (hbm_gbs)")
+    else:
+        roof = dict(kernel="lm_head", bound="tensor", achieved=alg["lm_flops"] / (r["lm_ms"] * 1e-3) / 1e12,
+                    peak=tc_peak, unit="TFLOP/s", peak_source=src + " (bf16_tflops burst)")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["avg_launch_ms"] = r["lm_ms"]
+    step_bound_s = max((alg["kv_bytes"] + alg["w_bytes"]) / (hbm * 1e9),
+                       (alg["lm_flops"] + alg["attn_flops"]) / (tc_peak * 1e12))
+    value = world * w.B / (r["ms"] * 1e-3)
+    line = dict(metric=METRIC, value=value, unit="requests/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=r["ms"], higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype,
+                data="synthetic (seeded; random-init weights of the named shapes)", config=config_of(w, args),
+                accepted_tokens_per_s=r["emitted"] / (r["ms"] * 1e-3),
+                mean_drafts_accepted=float(np.mean(r["n_acc"])),
+                roofline=roof,
+                step_roofline=dict(bound_ms=step_bound_s * 1e3, frac=step_bound_s * 1e3 / r["ms"],
+                                   kv_gb=alg["kv_bytes"] / 1e9, w_gb=alg["w_bytes"] / 1e9,
+                                   gflop=(alg["lm_flops"] + alg["attn_flops"]) / 1e9),
+                kernels=dict(attention_ms=r["attn_ms"],
+                             attention_gbs=alg["kv_bytes"] / (r["attn_ms"] * 1e-3) / 1e9,
+                             attention_tflops=alg["attn_flops"] / (r["attn_ms"] * 1e-3) / 1e12,
+                             lm_head_ms=r["lm_ms"]),
+                e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
+                         d2h_bytes_per_step=r["d2h"]),
+                gpu_launches=r["launches"], clocks=r["clocks"])
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, dev)
+    json_line(**line)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

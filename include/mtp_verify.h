@@ -125,6 +125,8 @@ typedef struct {
   int32_t dtype;             /* mtp_dtype */
   void* workspace;           /* device, >= mtp_attention_workspace_size() bytes */
   size_t workspace_bytes;
+  void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just
+                                after the attention kernel proper (append and combine excluded) */
 } mtp_attn_args;
 
 size_t mtp_attention_workspace_size(const mtp_attn_args* args);
@@ -197,6 +199,8 @@ typedef struct {
   int32_t any_sampling;      /* 0: every request is greedy (q_draft/temperature unused) */
   void* workspace;           /* device, >= mtp_lmhead_workspace_size() bytes */
   size_t workspace_bytes;
+  void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just
+                                after the LM-head GEMM kernel (acceptance kernels excluded) */
 } mtp_lmhead_args;
 
 size_t mtp_lmhead_workspace_size(const mtp_lmhead_args* args);
@@ -253,6 +257,10 @@ const char* mtp_last_error(void);
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns MTP_DEVICE_ERROR (message lists the bits) if any bit was set. */
 int mtp_sync_status(void* stream);
+
+/* Number of kernels the last successful call on this thread launched (for
+ * launch accounting in benchmarks and tests). */
+int mtp_last_launch_count(void);
 
 /* ABI version (MTP_ABI_VERSION) and sizeof of the argument structs
  * (0 = mtp_attn_args, 1 = mtp_lmhead_args, 2 = mtp_rollback_args), for

@@ -27,7 +27,8 @@ class AttnArgs(ctypes.Structure):
                 ("block_table", _P), ("ctx_lens", _P), ("out", _P),
                 ("B", _I), ("D", _I), ("Hq", _I), ("Hkv", _I), ("d_qk", _I), ("d_v", _I),
                 ("block_size", _I), ("max_blocks", _I), ("num_blocks", _I), ("is_mla", _I),
-                ("sm_scale", ctypes.c_float), ("dtype", _I), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+                ("sm_scale", ctypes.c_float), ("dtype", _I), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
+                ("timing_events", _P * 2)]
 
 
 class LmArgs(ctypes.Structure):
@@ -35,7 +36,7 @@ class LmArgs(ctypes.Structure):
                 ("q_draft", _P), ("seed", ctypes.c_uint64), ("out_tokens", _P), ("num_accepted", _P),
                 ("tie_flags", _P), ("lse_out", _P), ("argmax_out", _P), ("logits_debug", _P),
                 ("B", _I), ("D", _I), ("H", _I), ("V", _I), ("dtype", _I), ("any_sampling", _I),
-                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
 
 
 class RollbackArgs(ctypes.Structure):
@@ -78,6 +79,8 @@ def lib():
         L.mtp_rng_debug.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     ctypes.c_uint32, ctypes.c_int32, _P, _P, _P, _P]
         L.mtp_rng_debug.restype = ctypes.c_int
+        L.mtp_last_launch_count.argtypes = []
+        L.mtp_last_launch_count.restype = ctypes.c_int
         L.mtp_abi_version.argtypes = []
         L.mtp_abi_version.restype = ctypes.c_int
         L.mtp_abi_struct_size.argtypes = [ctypes.c_int]

@@ -26,6 +26,11 @@ cudaError_t launch_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag
 namespace {
 
 thread_local std::string g_last_error;
+thread_local int g_launches = 0;
+
+cudaError_t record(void* ev, cudaStream_t s) {
+  return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
+}
 
 // One 4-byte error word per device: kernels OR their range-check failures
 // into it; mtp_sync_status() reads and clears it.
@@ -167,6 +172,8 @@ const char* mtp_last_error(void) { return g_last_error.c_str(); }
 
 int mtp_abi_version(void) { return MTP_ABI_VERSION; }
 
+int mtp_last_launch_count(void) { return g_launches; }
+
 size_t mtp_abi_struct_size(int which) {
   switch (which) {
     case 0: return sizeof(mtp_attn_args);
@@ -186,6 +193,7 @@ size_t mtp_attention_workspace_size(const mtp_attn_args* a) {
 int mtp_verify_attention(const mtp_attn_args* a, void* stream) {
   int rc = check_attn(a);
   if (rc != MTP_OK) return rc;
+  g_launches = 0;
   if (a->B == 0) return MTP_OK;
   DeviceCtx* c = nullptr;
   if ((rc = device_ctx(&c)) != MTP_OK) return rc;
@@ -195,12 +203,15 @@ int mtp_verify_attention(const mtp_attn_args* a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = mtp::launch_kv_append(*a, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "kv append launch");
+  if ((e = record(a->timing_events[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if (a->dtype == MTP_BF16 && a->is_mla && mtp::attention_mma_supported(*a)) e = mtp::launch_attention_mla(*a, p, c->err, s);
   else if (a->dtype == MTP_BF16 && mtp::attention_mma_supported(*a)) e = mtp::launch_attention_mma(*a, p, c->err, s);
   else e = mtp::launch_attention_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_attention_combine(*a, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention combine launch");
+  g_launches = 2 + (p.n_splits > 1 ? 1 : 0);
   return MTP_OK;
 }
 
@@ -214,6 +225,7 @@ size_t mtp_lmhead_workspace_size(const mtp_lmhead_args* a) {
 int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
   int rc = check_lm(a);
   if (rc != MTP_OK) return rc;
+  g_launches = 0;
   if (a->B == 0) return MTP_OK;
   DeviceCtx* c = nullptr;
   if ((rc = device_ctx(&c)) != MTP_OK) return rc;
@@ -222,21 +234,27 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
     return fail(MTP_INVALID_ARG, "workspace of %zu bytes needed, %zu given", p.ws_bytes, a->workspace_bytes);
   if (((uintptr_t)a->workspace) % 256) return fail(MTP_INVALID_ARG, "workspace must be 256-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = p.tc ? mtp::launch_lmhead_tc(*a, p, c->err, s) : mtp::launch_lmhead_simt(*a, p, c->err, s);
+  cudaError_t e = record(a->timing_events[0], s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  e = p.tc ? mtp::launch_lmhead_tc(*a, p, c->err, s) : mtp::launch_lmhead_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM head launch");
+  if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_accept(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  g_launches = 2 + (a->any_sampling ? 1 : 0);
   return MTP_OK;
 }
 
 int kv_rollback(const mtp_rollback_args* a, void* stream) {
   int rc = check_rb(a);
   if (rc != MTP_OK) return rc;
+  g_launches = 0;
   if (a->B == 0) return MTP_OK;
   DeviceCtx* c = nullptr;
   if ((rc = device_ctx(&c)) != MTP_OK) return rc;
   cudaError_t e = mtp::launch_rollback(*a, c->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rollback launch");
+  g_launches = 1;
   return MTP_OK;
 }
 
