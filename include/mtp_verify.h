@@ -206,6 +206,32 @@ typedef struct {
 size_t mtp_lmhead_workspace_size(const mtp_lmhead_args* args);
 int mtp_verify_logits_accept(const mtp_lmhead_args* args, void* stream);
 
+/* 2b. The same call for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that have no way to provide a workspace: for example a plugin inside an
+ * inference engine that owns all device memory and gives plugins none, or a
+ * latency-critical loop where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable.
+ *
+ * Arguments, results and errors are those of mtp_verify_logits_accept, except
+ * that `workspace` and `workspace_bytes` are ignored. Scratch comes from one
+ * array of MTP_NOALLOC_SCRATCH_BYTES (8 MiB) in device memory owned by the
+ * library: every GPU that loads the library holds it until the process exits.
+ * A batch whose scratch would not fit (mtp_lmhead_workspace_size() larger
+ * than the array, e.g. sampling requests with a large M * V) is rejected with
+ * MTP_INVALID_ARG and a message. Nothing here allocates: no cudaMalloc,
+ * cudaFree or allocating library routine.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current). Every call on a device shares the one
+ * array and leaves its contents behind; each call writes all the scratch it
+ * reads before reading it, so nothing needs clearing in between. Calls whose
+ * kernels overlap on the GPU (e.g. on two streams) race on the array: issue
+ * them in order on one stream. */
+#define MTP_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int mtp_verify_logits_accept_noalloc(const mtp_lmhead_args* args, void* stream);
+size_t mtp_noalloc_scratch_bytes(void);
+
 /* ------------------------------------------------------------------------ */
 /* 3. KV-cache rollback.
  *

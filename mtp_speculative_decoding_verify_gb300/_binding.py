@@ -79,6 +79,10 @@ def lib():
         L.mtp_rng_debug.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     ctypes.c_uint32, ctypes.c_int32, _P, _P, _P, _P]
         L.mtp_rng_debug.restype = ctypes.c_int
+        L.mtp_verify_logits_accept_noalloc.argtypes = [ctypes.POINTER(LmArgs), _P]
+        L.mtp_verify_logits_accept_noalloc.restype = ctypes.c_int
+        L.mtp_noalloc_scratch_bytes.argtypes = []
+        L.mtp_noalloc_scratch_bytes.restype = ctypes.c_size_t
         L.mtp_last_launch_count.argtypes = []
         L.mtp_last_launch_count.restype = ctypes.c_int
         L.mtp_abi_version.argtypes = []
@@ -236,6 +240,25 @@ def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft
     a = lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
                 lse_out, argmax_out, logits_debug, workspace)
     _check(lib().mtp_verify_logits_accept(ctypes.byref(a), _stream_handle(stream)))
+
+
+def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens,
+                                     num_accepted, tie_flags, lse_out=None, argmax_out=None, logits_debug=None,
+                                     stream=None):
+    """mtp_verify_logits_accept for callers that cannot allocate device memory:
+    the scratch lives in a fixed array owned by the library (no workspace is
+    allocated or passed). Raises MtpError if the batch needs more scratch
+    than that array holds. Calls must not overlap on the GPU."""
+    a = LmArgs(_ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode), _ptr(temperature), _ptr(q_draft),
+               int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_tokens), _ptr(num_accepted), _ptr(tie_flags), _ptr(lse_out),
+               _ptr(argmax_out), _ptr(logits_debug), tokens.shape[0], tokens.shape[1] - 1, lm_head.shape[1],
+               lm_head.shape[0], _dtype_code(lm_head), int(q_draft is not None), None, 0)
+    for t, n in ((hidden, "hidden"), (lm_head, "lm_head"), (tokens, "tokens"), (mode, "mode"),
+                 (temperature, "temperature"), (q_draft, "q_draft"), (out_tokens, "out_tokens"),
+                 (num_accepted, "num_accepted"), (tie_flags, "tie_flags"), (lse_out, "lse_out"),
+                 (argmax_out, "argmax_out"), (logits_debug, "logits_debug")):
+        _dev(t, n)
+    _check(lib().mtp_verify_logits_accept_noalloc(ctypes.byref(a), _stream_handle(stream)))
 
 
 def rollback_args(block_table, seq_lens, num_accepted, free_list, free_count, *, D):

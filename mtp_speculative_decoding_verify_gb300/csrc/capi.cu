@@ -137,8 +137,10 @@ int check_rb(const mtp_rollback_args* a) {
   return MTP_OK;
 }
 
+}  // namespace
+
 // --------------------------------------------------------------- planning
-mtp::LmPlan plan_lm(const mtp_lmhead_args& a, int sm_count) {
+mtp::LmPlan mtp::plan_lmhead(const mtp_lmhead_args& a, int sm_count) {
   mtp::LmPlan p{};
   const int R = a.D + 1;
   p.M = a.B * R;
@@ -164,7 +166,21 @@ mtp::LmPlan plan_lm(const mtp_lmhead_args& a, int sm_count) {
   return p;
 }
 
-}  // namespace
+namespace mtp {
+// Host-side validation and per-device context shared with the other entry points.
+int check_lmhead_args(const mtp_lmhead_args* a) { return check_lm(a); }
+int device_context(unsigned** err, int* sm_count) {
+  DeviceCtx* c = nullptr;
+  const int rc = device_ctx(&c);
+  if (rc != MTP_OK) return rc;
+  *err = c->err;
+  *sm_count = c->sm_count;
+  return MTP_OK;
+}
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+int set_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+void set_launch_count(int n) { g_launches = n; }
+}  // namespace mtp
 
 extern "C" {
 
@@ -219,7 +235,7 @@ size_t mtp_lmhead_workspace_size(const mtp_lmhead_args* a) {
   if (check_lm(a) != MTP_OK) return 0;
   DeviceCtx* c = nullptr;
   if (device_ctx(&c) != MTP_OK) return 0;
-  return std::max<size_t>(256, plan_lm(*a, c->sm_count).ws_bytes);
+  return std::max<size_t>(256, mtp::plan_lmhead(*a, c->sm_count).ws_bytes);
 }
 
 int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
@@ -229,7 +245,7 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
   if (a->B == 0) return MTP_OK;
   DeviceCtx* c = nullptr;
   if ((rc = device_ctx(&c)) != MTP_OK) return rc;
-  const mtp::LmPlan p = plan_lm(*a, c->sm_count);
+  const mtp::LmPlan p = mtp::plan_lmhead(*a, c->sm_count);
   if (!a->workspace || a->workspace_bytes < p.ws_bytes)
     return fail(MTP_INVALID_ARG, "workspace of %zu bytes needed, %zu given", p.ws_bytes, a->workspace_bytes);
   if (((uintptr_t)a->workspace) % 256) return fail(MTP_INVALID_ARG, "workspace must be 256-byte aligned");
