@@ -1,14 +1,457 @@
-// LM head on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// LM head on the 5th-generation tensor cores (tcgen05 MMA into TMEM, TMA
+// loads, mbarrier pipeline) with the softmax statistics fused into the
+// epilogue, for bf16 weights.
+//
+// "Multi Token Prediction" note, K=3 flow step 4: Logits_i = H_i x W_o for
+// all verify rows in one product; step 5: softmax over the vocabulary. The
+// full logits are never stored for greedy rows: the epilogue keeps, per row,
+// a running max, sum of exp(l - max) and argmax over the vocabulary this CTA
+// sees; rejection-sampling rows also get their fp32 logit rows written once
+// (their residual draw needs the whole row after the log-sum-exp is known).
+//
+// Mapping (swap-AB): the MMA's M dimension is 128 vocabulary rows of W (the
+// big streamed operand), its N dimension is a group of N verify rows of
+// hidden (N = 32..256), K runs over the hidden size in 64-element steps, so
+// one accumulator tile is 128 (vocab, TMEM lanes) x N (rows, TMEM columns)
+// fp32. Persistent CTAs: row group g of the hidden rows is served by
+// `cpg` CTAs that walk the vocabulary tiles t = s, s + cpg, ...
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
+// and issues the MMAs, warps 2..5 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. +31). Two TMEM accumulators let the epilogue of tile i overlap
+// the MMAs of tile i+1.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace mtp {
 
-bool lmhead_tc_supported(const mtp_lmhead_args& a) { (void)a; return false; }
-int lmhead_tc_slices(int V, int M, int sm_count) { (void)V; (void)M; return sm_count; }
-cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& p, unsigned* err, cudaStream_t s) {
-  (void)a; (void)p; (void)err; (void)s;
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kThreadsTc = 192;
+constexpr int kTileV = 128;          // vocab rows per MMA tile (MMA M)
+constexpr int kTileK = 64;           // hidden elements per pipeline stage (128 B rows, 128-B swizzle)
+constexpr int kMaxN = 256;           // rows per row group (MMA N)
+constexpr int kSmemLimit = 232448;   // 227 KB opt-in per CTA
+constexpr int kMaxStages = 8;
+
+struct TcParams {
+  const int32_t* tokens;
+  const uint8_t* mode;
+  const float* temperature;
+  float* pmax;
+  float* psum;
+  float* pbest;
+  int* pidx;
+  float* ldraft;
+  float* samp_logits;   // [M, V], rows of sampling requests only (nullptr: none)
+  float* logits_debug;  // [M, V] optional
+  unsigned* err;
+  int any_sampling;
+  int M, R, H, V;
+  int N;                // rows per group (multiple of 32)
+  int cpg;              // CTAs per row group
+  int n_tiles;          // vocab tiles
+  int stages;
+  uint32_t tmem_cols;   // allocated TMEM columns (power of 2 >= 2N); accumulator b at b * tmem_cols / 2
+};
+
+struct SmemLayout {
+  int a_off, b_off, stage_bytes, bar_off, misc_off, epi_off, rows_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
+  SmemLayout L;
+  const int a_bytes = kTileV * kTileK * 2;       // 16 KB
+  const int b_bytes = N * kTileK * 2;            // N x 128 B
+  L.stage_bytes = a_bytes + b_bytes;
+  L.a_off = 0;                                   // stage s: A at s*stage_bytes, B right after A
+  L.b_off = a_bytes;
+  int off = stages * L.stage_bytes;              // multiple of 1024 (a_bytes and b_bytes are)
+  L.bar_off = off;
+  off += (2 * stages + 5) * 8;                   // full[], empty[], acc_full[2], acc_empty[2], final
+  L.misc_off = off;
+  off += 16;                                     // TMEM base, abort flag
+  off = (off + 15) / 16 * 16;
+  L.epi_off = off;
+  off += 4 * 32 * 33 * 4;                        // per-epilogue-warp 32x33 transpose buffers
+  L.rows_off = off;
+  off += N * 12;                                 // per-row draft id, 1/T, sampling flag
+  L.total = off + 1024;                          // + alignment slack for the 1024-B aligned base
+  return L;
+}
+
+__device__ __forceinline__ void abort_all(volatile int* abort, unsigned* err) {
+  *abort = 1;
+  raise_error(err, MTP_ERR_TIMEOUT);
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                     const TcParams p) {
+  constexpr int N = NCH * 32;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemLayout L = smem_layout(N, p.stages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + p.stages;
+  uint64_t* acc_full = empty + p.stages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* final_bar = acc_empty + 2;
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+  float* epi_buf = reinterpret_cast<float*>(smem + L.epi_off);
+  int* row_draft = reinterpret_cast<int*>(smem + L.rows_off);
+  float* row_inv_t = reinterpret_cast<float*>(smem + L.rows_off + N * 4);
+  int* row_samp = reinterpret_cast<int*>(smem + L.rows_off + N * 8);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int group = blockIdx.x / p.cpg;
+  const int cta_in_group = blockIdx.x % p.cpg;
+  const int row0 = group * N;
+  const int k_steps = p.H / kTileK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      sm100::mbar_init(&full[s], 1);
+      sm100::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      sm100::mbar_init(&acc_full[b], 1);
+      sm100::mbar_init(&acc_empty[b], 4);
+    }
+    sm100::mbar_init(final_bar, 1);
+    *abort = 0;
+    sm100::fence_barrier_init();
+    sm100::tma_prefetch_desc(&tm_w);
+    sm100::tma_prefetch_desc(&tm_h);
+  }
+  if (warp == 1) {
+    sm100::tmem_alloc(tmem_base_slot, p.tmem_cols);
+    sm100::tmem_relinquish();
+  }
+  // Per-row information of this CTA's row group.
+  for (int r = threadIdx.x; r < N; r += kThreadsTc) {
+    const int m = row0 + r;
+    int draft = -1, samp = 0;
+    float inv_t = 1.0f;
+    if (m < p.M) {
+      const int b = m / p.R, j = m % p.R;
+      if (p.any_sampling && p.mode[b] == 1 && p.temperature[b] > 0.0f) {
+        samp = 1;
+        inv_t = 1.0f / p.temperature[b];
+      }
+      if (j < p.R - 1) draft = p.tokens[m + 1];
+    }
+    row_draft[r] = draft;
+    row_inv_t[r] = inv_t;
+    row_samp[r] = samp;
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  // Tiles of this CTA: t = cta_in_group + i * cpg.
+  const int my_tiles = cta_in_group < p.n_tiles ? (p.n_tiles - 1 - cta_in_group) / p.cpg + 1 : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = sm100::l2_policy_evict_first();
+      const uint64_t pol_h = sm100::l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int v0 = (cta_in_group + i * p.cpg) * kTileV;
+        for (int k = 0; k < k_steps; ++k) {
+          if (!sm100::mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+            abort_all(abort, p.err);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * L.stage_bytes;
+          sm100::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+          sm100::tma_load_2d(st + L.a_off, &tm_w, &full[stage], k * kTileK, v0, pol_w);
+          sm100::tma_load_2d(st + L.b_off, &tm_h, &full[stage], k * kTileK, row0, pol_h);
+          ++issued;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued load must have landed before the CTA exits: wait (time
+      // limited) for the completion of the most recent fill of each stage.
+      for (int j = 0; j < min(issued, p.stages); ++j) {
+        const int idx = issued - 1 - j;
+        sm100::mbar_wait_timeout(&full[idx % p.stages], (uint32_t)((idx / p.stages) & 1), sm100::kWaitTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = sm100::idesc_bf16_f32(kTileV, N);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int buf = i & 1;
+        const uint32_t acc_phase = (i >> 1) & 1;
+        if (!sm100::mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort)) {
+          abort_all(abort, p.err);
+          break;
+        }
+        sm100::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * (p.tmem_cols / 2);
+        for (int k = 0; k < k_steps; ++k) {
+          if (!sm100::mbar_wait(&full[stage], phase, abort)) {
+            abort_all(abort, p.err);
+            ok = false;
+            break;
+          }
+          sm100::tc_fence_after();
+          const uint32_t a_addr = sm100::smem_u32(smem + stage * L.stage_bytes + L.a_off);
+          const uint32_t b_addr = sm100::smem_u32(smem + stage * L.stage_bytes + L.b_off);
+          const uint64_t adesc = sm100::smem_desc_sw128_kmajor(a_addr);
+          const uint64_t bdesc = sm100::smem_desc_sw128_kmajor(b_addr);
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            // Advance 16 elements (32 B) along K inside the 128-B swizzled row.
+            sm100::tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                               (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          sm100::tc_commit(&empty[stage]);  // stage free once these MMAs have read it
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) sm100::tc_commit(&acc_full[buf]);
+      }
+      // Every MMA issued so far has completed before TMEM is released.
+      sm100::tc_commit(final_bar);
+      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp % 4;                       // TMEM lane quarter
+    float* tb = epi_buf + (warp - 2) * 32 * 33;   // this warp's transpose buffer
+    RowStat st[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) st[c] = rowstat_empty();
+    for (int i = 0; i < my_tiles; ++i) {
+      const int buf = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      const bool ok = __all_sync(0xffffffffu, sm100::mbar_wait(&acc_full[buf], acc_phase, abort) ? 1 : 0) != 0;
+      if (!ok) {
+        if (lane == 0) abort_all(abort, p.err);
+        break;
+      }
+      sm100::tc_fence_after();
+      const int vbase = (cta_in_group + i * p.cpg) * kTileV + 32 * q;   // vocab of lane 0 of this warp
+      const int nvalid = min(32, p.V - vbase);                          // may be <= 0 in the tail tile
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint32_t r[32];
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + buf * (p.tmem_cols / 2) + c * 32;
+        sm100::tmem_ld_32x32b_x32(taddr, r);
+        sm100::tmem_ld_wait();
+        // r[x] = logit(vocab vbase + lane, row c*32 + x): transpose so that
+        // this thread then owns row c*32 + lane across the warp's 32 vocab.
+#pragma unroll
+        for (int x = 0; x < 32; ++x) tb[x * 33 + lane] = __uint_as_float(r[x]);
+        __syncwarp();
+        const int rr = c * 32 + lane;
+        const int m = row0 + rr;
+        if (m < p.M && nvalid > 0) {
+          const bool samp = row_samp[rr] != 0;
+          const float inv_t = row_inv_t[rr];
+          float* rowv = tb + lane * 33;
+          float cmax = -INFINITY;
+          int cidx = 0;
+          for (int x = 0; x < nvalid; ++x) {
+            float l = rowv[x];
+            if (samp) l = __fmul_rn(l, inv_t);
+            rowv[x] = l;
+            if (l > cmax) {
+              cmax = l;
+              cidx = x;
+            }
+          }
+          float csum = 0.0f;
+          for (int x = 0; x < nvalid; ++x) csum += expf(rowv[x] - cmax);
+          st[c] = rowstat_merge(st[c], RowStat{cmax, csum, cmax, vbase + cidx});
+          const int d = row_draft[rr];
+          if (d >= vbase && d < vbase + nvalid) p.ldraft[m] = rowv[d - vbase];
+          float* dst_s = (samp && p.samp_logits) ? p.samp_logits + (int64_t)m * p.V + vbase : nullptr;
+          float* dst_d = p.logits_debug ? p.logits_debug + (int64_t)m * p.V + vbase : nullptr;
+          if (dst_s || dst_d) {
+            if (nvalid == 32 && (p.V & 3) == 0) {
+#pragma unroll
+              for (int x = 0; x < 32; x += 4) {
+                const float4 v4 = make_float4(rowv[x], rowv[x + 1], rowv[x + 2], rowv[x + 3]);
+                if (dst_s) *reinterpret_cast<float4*>(dst_s + x) = v4;
+                if (dst_d) *reinterpret_cast<float4*>(dst_d + x) = v4;
+              }
+            } else {
+              for (int x = 0; x < nvalid; ++x) {
+                if (dst_s) dst_s[x] = rowv[x];
+                if (dst_d) dst_d[x] = rowv[x];
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+      sm100::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(&acc_empty[buf]);
+    }
+    // Partials of this (CTA, lane quarter): slice = cta_in_group * 4 + q.
+    const int slice = cta_in_group * 4 + q;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int m = row0 + c * 32 + lane;
+      if (m < p.M) {
+        const int64_t o = (int64_t)slice * p.M + m;
+        p.pmax[o] = st[c].m;
+        p.psum[o] = st[c].s;
+        p.pbest[o] = st[c].best;
+        p.pidx[o] = st[c].idx;
+      }
+    }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 row-major [rows, cols] tensor, box {64 columns, box_rows rows},
+// 128-byte swizzle, out-of-bounds rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct TcShape {
+  int N, groups, cpg, stages;
+  uint32_t tmem_cols;
+};
+
+TcShape tc_shape(int M, int sm_count) {
+  TcShape s;
+  s.groups = (M + kMaxN - 1) / kMaxN;
+  const int per = (M + s.groups - 1) / s.groups;
+  s.N = std::max(32, (per + 31) / 32 * 32);
+  s.cpg = std::max(1, sm_count / s.groups);
+  s.stages = kMaxStages;
+  while (s.stages > 2 && smem_layout(s.N, s.stages).total > kSmemLimit) --s.stages;
+  s.tmem_cols = 64;
+  while (s.tmem_cols < (uint32_t)(2 * s.N)) s.tmem_cols *= 2;
+  return s;
+}
+
+template <int NCH>
+cudaError_t launch_nch(const TcShape& sh, const CUtensorMap& tw, const CUtensorMap& th, const TcParams& p,
+                       cudaStream_t s) {
+  const int smem = smem_layout(NCH * 32, sh.stages).total;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  lmhead_tc_kernel<NCH><<<sh.groups * sh.cpg, kThreadsTc, smem, s>>>(tw, th, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool lmhead_tc_supported(const mtp_lmhead_args& a) {
+  return a.dtype == MTP_BF16 && a.H % kTileK == 0 && encode_fn() != nullptr;
+}
+
+int lmhead_tc_slices(int V, int M, int sm_count) {
+  (void)V;
+  return tc_shape(M, sm_count).cpg * 4;
+}
+
+cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& pl, unsigned* err, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const TcShape sh = tc_shape(pl.M, sms);
+  if (sh.cpg * 4 != pl.slices) return cudaErrorInvalidValue;
+  CUtensorMap tw, th;
+  if (!make_map(&tw, a.lm_head, (uint64_t)a.V, (uint64_t)a.H, kTileV)) return cudaErrorInvalidValue;
+  if (!make_map(&th, a.hidden, (uint64_t)pl.M, (uint64_t)a.H, (uint32_t)sh.N)) return cudaErrorInvalidValue;
+  char* ws = (char*)a.workspace;
+  TcParams p;
+  p.tokens = a.tokens;
+  p.mode = a.mode;
+  p.temperature = a.temperature;
+  p.pmax = (float*)(ws + pl.off_pmax);
+  p.psum = (float*)(ws + pl.off_psum);
+  p.pbest = (float*)(ws + pl.off_pbest);
+  p.pidx = (int*)(ws + pl.off_pidx);
+  p.ldraft = (float*)(ws + pl.off_ldraft);
+  p.samp_logits = a.any_sampling ? (float*)(ws + pl.off_logits) : nullptr;
+  p.logits_debug = a.logits_debug;
+  p.err = err;
+  p.any_sampling = a.any_sampling;
+  p.M = pl.M;
+  p.R = a.D + 1;
+  p.H = a.H;
+  p.V = a.V;
+  p.N = sh.N;
+  p.cpg = sh.cpg;
+  p.n_tiles = (a.V + kTileV - 1) / kTileV;
+  p.stages = sh.stages;
+  p.tmem_cols = sh.tmem_cols;
+  switch (sh.N / 32) {
+    case 1: return launch_nch<1>(sh, tw, th, p, s);
+    case 2: return launch_nch<2>(sh, tw, th, p, s);
+    case 3: return launch_nch<3>(sh, tw, th, p, s);
+    case 4: return launch_nch<4>(sh, tw, th, p, s);
+    case 5: return launch_nch<5>(sh, tw, th, p, s);
+    case 6: return launch_nch<6>(sh, tw, th, p, s);
+    case 7: return launch_nch<7>(sh, tw, th, p, s);
+    case 8: return launch_nch<8>(sh, tw, th, p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace mtp
