@@ -75,7 +75,7 @@ cudaError_t launch_kv_append(const mtp_attn_args& a, unsigned* err, cudaStream_t
 static int rows_per_cta(const mtp_attn_args& a) {
   if (a.dtype == MTP_F32) return 8;     // SIMT: one warp per row, 8 warps
   if (a.is_mla) return 64;              // MLA tensor-core tile
-  return 16;                            // GQA tensor-core tile
+  return 128;                           // GQA tensor-core CTA: all rows of a KV head (up to 128)
 }
 
 AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {

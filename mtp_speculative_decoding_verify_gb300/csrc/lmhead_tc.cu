@@ -33,6 +33,10 @@
 
 namespace mtp {
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box);
+
 namespace {
 
 constexpr int kThreadsTc = 192;
@@ -341,32 +345,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 }
 
 // ------------------------------------------------------------------- host
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2D bf16 row-major [rows, cols] tensor, box {64 columns, box_rows rows},
 // 128-byte swizzle, out-of-bounds rows read as zero.
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kTileK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_bf16_map(map, base, 2, dims, strides, box);
 }
 
 struct TcShape {
@@ -400,7 +385,7 @@ cudaError_t launch_nch(const TcShape& sh, const CUtensorMap& tw, const CUtensorM
 }  // namespace
 
 bool lmhead_tc_supported(const mtp_lmhead_args& a) {
-  return a.dtype == MTP_BF16 && a.H % kTileK == 0 && encode_fn() != nullptr;
+  return a.dtype == MTP_BF16 && a.H % kTileK == 0 && tensor_map_encoder() != nullptr;
 }
 
 int lmhead_tc_slices(int V, int M, int sm_count) {
