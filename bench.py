@@ -49,6 +49,10 @@ def workloads():
         "cfg2": synth.CFG2,
         "cfg3": synth.CFG3,
         **{"sweep_B%d_D%d" % (B, D): synth.sweep_point(B, D) for B in (1, 8, 64, 256, 512) for D in (1, 3, 5, 7)},
+        # Reduced cases for profiler captures (inputs still larger than L2).
+        "profile_mla_V32k": synth.CFG1.with_(name="profiling case: DeepSeek-V3-shaped MLA B=32 D=3, vocab 32768",
+                                             V=32768),
+        "profile_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, B=16", B=16),
     }
 
 
@@ -230,7 +234,43 @@ def run_gpu(args, w, rank, world, dev):
     clocks = sampler.stop() if sampler else None
     step.set_events(None, None)
     step.B.sync_status()
-    ms = t0.elapsed_time(t1) / K
+    ms_eager = t0.elapsed_time(t1) / K
+
+    # The same step captured once in a CUDA graph and replayed K times (the
+    # library's calls are capture-safe once each has run on the device).
+    graph_ms = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                step.run(side)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        sampler2 = ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) if rank == 0 else None
+        if sampler2:
+            sampler2.start()
+            time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(K):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks_g = sampler2.stop() if sampler2 else None
+        step.B.sync_status()
+        graph_ms = g0.elapsed_time(g1) / K
+        if clocks_g:
+            clocks = clocks_g
+    ms = graph_ms if graph_ms is not None else ms_eager
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_lm)
     n_acc = step.num_acc.cpu().numpy()
@@ -263,7 +303,8 @@ def run_gpu(args, w, rank, world, dev):
     e2e_ms = (time.perf_counter() - e2e_t0) * 1e3 / K
 
     ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, float(n_acc.sum() + w.B), world, dev)
-    return dict(ms=ms, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
+    ms_eager, _, _ = combine_ranks(ms_eager, 0.0, 0.0, world, dev)
+    return dict(ms=ms, ms_eager=ms_eager, graph=graph_ms is not None, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
                 clocks=clocks, launches=launches, h2d=h2d, d2h=d2h)
 
 
@@ -342,6 +383,7 @@ def run_reference(args, w, rank, world):
 
 def config_of(w, args):
     return {"workload": w.name, "B": w.B, "D": w.D, "parallelism": "request-sharded replicas",
+            "cuda_graph": not getattr(args, "no_graph", False) and getattr(args, "impl", "gb300") == "gb300",
             "l2": "inputs larger than L2 (LM-head weights %.2f GB streamed every step)" % (w.V * w.H * elem_bytes(w) / 1e9)}
 
 
@@ -354,6 +396,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches only (no CUDA-graph replay)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -394,7 +437,7 @@ def main():
                        (alg["lm_flops"] + alg["attn_flops"]) / (tc_peak * 1e12))
     value = world * w.B / (r["ms"] * 1e-3)
     line = dict(metric=METRIC, value=value, unit="requests/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
-                ms_per_step=r["ms"], higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype,
+                ms_per_step=r["ms"], ms_per_step_eager=r["ms_eager"], higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype,
                 data="synthetic (seeded; random-init weights of the named shapes)", config=config_of(w, args),
                 accepted_tokens_per_s=r["emitted"] / (r["ms"] * 1e-3),
                 mean_drafts_accepted=float(np.mean(r["n_acc"])),

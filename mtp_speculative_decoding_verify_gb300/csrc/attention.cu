@@ -91,7 +91,8 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
   n = std::max(n, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
   n = std::min(n, std::max(1, (max_len + kMinSplitLen - 1) / kMinSplitLen));
   int split_len = (max_len + n - 1) / n;
-  split_len = (split_len + kBlock - 1) / kBlock * kBlock;
+  const int gran = (a.is_mla && a.dtype == MTP_BF16) ? 128 : kBlock;   // MLA tensor-core tiles are 128 keys
+  split_len = (split_len + gran - 1) / gran * gran;
   p.split_len = split_len;
   p.n_splits = (max_len + split_len - 1) / split_len;
   p.ws_bytes = 0;

@@ -1,0 +1,611 @@
+// Absorbed-MLA verify attention on the 5th-generation tensor cores.
+//
+// "Multi Token Prediction" note, K=3 flow step 2 (stacked queries against the
+// reused cache, causal within the verify chain) in the absorbed MLA form: one
+// latent vector of 576 per token is the key, its first 512 entries the value;
+// every query head attends it. Row of verify token j (request context ctx)
+// attends slots 0..ctx+j.
+//
+// Transposed formulation so that every operand fits the tensor memory:
+//   S^T [128 keys x 64 rows]  = K_tile [128 x 576] . Q^T        (M = keys)
+//   O^T [512 dv   x 64 rows] += V^T [dv x 128 keys] . P^T         (M = 128 dv, 4 chunks)
+// TMEM: O^T in columns 0..255 (4 chunks x 64), three S^T buffers in 256..447
+// so that two QK tiles run ahead of the softmax. The Q tile (64 rows x 576,
+// 72 KB) stays in shared memory; K chunks [128 keys x 64 dims] and V chunks
+// [64 keys x 128 dv] stream through two separate 16 KB-stage TMA rings (V is
+// read a second time, from L2, after the softmax), so K of later tiles keeps
+// flowing while V waits for P. V^T is consumed MN-major straight from the
+// cache layout (dv contiguous).
+//
+// The row blocks of one request form a thread-block cluster (up to
+// MTP_MLA_MAX_CLUSTER CTAs): every K / V stage is fetched from L2 once per
+// cluster with a TMA multicast (the fills are spread round-robin over the
+// CTAs) and released by a multicast tcgen05.commit from each CTA's MMA
+// thread, so L2 requests drop by the cluster size.
+//
+// Warps (4 warpgroups): 0 MMA issuer, 1-2 K-ring producers, 3 and 12 V-ring
+// producers, 4..11 softmax / epilogue (warp w owns TMEM lanes 32*(w%4)..+31 =
+// keys of S^T, dv of O^T, and one half of the 64 row columns), 13-15 idle.
+// A single thread serialises its TMA issues, so each ring has two producer
+// warps and each stage's two boxes go out from two lanes; setmaxnreg moves
+// registers from the producer warpgroups to the softmax warpgroups. Row max / sum across keys use a
+// butterfly transpose-reduce over the warp plus a 4-way merge in shared
+// memory. Online softmax with a lazy rescale: the running row max only moves
+// when a tile's max exceeds it by more than 8 (log2 units), then O^T columns
+// and the row sum are rescaled; results are exact either way since P and l use
+// the same reference max.
+#include <cuda.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+#ifndef MTP_MLA_MAX_CLUSTER
+#define MTP_MLA_MAX_CLUSTER 2
+#endif
+
+namespace mtp {
+
+bool make_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box);
+
+namespace {
+
+constexpr int kRows = 64;             // query rows per CTA (MMA N)
+constexpr int kKeys = 128;            // keys per tile (MMA M of S^T)
+constexpr int kDQ = 576, kDV = 512;
+constexpr int kQChunks = kDQ / 64;    // 9
+constexpr int kStageBytes = 16384;
+constexpr int kKStages = 4;           // ring of K chunks [128 keys x 64 dims]
+constexpr int kVStages = 3;           // ring of V chunks [64 keys x 128 dv]
+constexpr int kSBufs = 3;             // S^T buffers: two QK tiles run ahead of the softmax
+constexpr int kSoftWarps = 8;         // 2 per TMEM lane quarter (row halves)
+constexpr int kThreads = 512;         // 4 warpgroups: [MMA, K, K, V], softmax x 2, [V, idle x 3]
+constexpr int kRegsLight = 64;        // producer / MMA warpgroups after setmaxnreg
+constexpr int kRegsSoftmax = 192;     // softmax warpgroups: 128 * (64 + 192 + 192 + 64) = 65536
+static_assert(128 * (2 * kRegsLight + 2 * kRegsSoftmax) <= 65536, "register split exceeds the launch's file");
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazyRescale = 8.0f;  // log2 units
+constexpr int kMaxCluster = MTP_MLA_MAX_CLUSTER;   // CTAs (row blocks) sharing each KV tile by TMA multicast
+
+constexpr int kQOff = 0;                                    // 9 x 8 KB
+constexpr int kKOff = kQOff + kQChunks * 8192;              // 73728
+constexpr int kVOff = kKOff + kKStages * kStageBytes;
+constexpr int kPOff = kVOff + kVStages * kStageBytes;       // 2 buffers x (2 x 8 KB)
+constexpr int kPBytes = 16384;
+constexpr int kRedOff = kPOff + 2 * kPBytes;                // red_max[4][64], red_sum[4][64]
+constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;           // m_run, l_run, m_ref, scale [64] floats, lim [64] int
+constexpr int kBarOff = kRowOff + 5 * 64 * 4;
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 1 + 2 * kSBufs + 2 + 2 + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;            // tmem base, abort, rescale flag
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;       // O^T chunk c at c * 64
+constexpr uint32_t kColS = 256;     // S^T buffer b at 256 + b * 64
+
+struct Params {
+  __nv_bfloat16* out;
+  float* part_o;
+  float* part_lse;
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  unsigned* err;
+  int R, Hq, max_blocks, num_blocks, split_len, n_splits;
+  int cluster;          // CTAs per cluster (row blocks of one request sharing each KV tile by multicast)
+  float scale_log2;
+};
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return sm100::smem_desc_sw128_kmajor(saddr); }
+
+// MN-major operand with 128-B swizzling: 64-element MN blocks `lbo` bytes
+// apart, 8-row K groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(lbo >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Lane l ends up with op-reduction over the 32 lanes of element l of v[]
+// (a butterfly transpose-reduce: 31 shuffles for 32 values).
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = upper ? v[k] : v[k + w];
+      const float keep = upper ? v[k + w] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+// One ring of TMA stages consumed in order by the MMA thread.
+struct Ring {
+  uint64_t* full;
+  uint64_t* empty;
+  int n, stage;
+  uint32_t phase;
+  __device__ __forceinline__ void advance() {
+    if (++stage == n) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                  const __grid_constant__ CUtensorMap tm_kv,
+                                                                  const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* red_max = reinterpret_cast<float*>(smem + kRedOff);
+  float* red_sum = red_max + 4 * 64;
+  float* m_run = reinterpret_cast<float*>(smem + kRowOff);
+  float* l_run = m_run + 64;
+  float* m_ref = m_run + 128;
+  float* rscale = m_run + 192;
+  int* lim = reinterpret_cast<int*>(m_run + 256);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* kempty = kfull + kKStages;
+  uint64_t* vfull = kempty + kKStages;
+  uint64_t* vempty = vfull + kVStages;
+  uint64_t* qbar = vempty + kVStages;
+  uint64_t* s_full = qbar + 1;
+  uint64_t* s_empty = s_full + kSBufs;
+  uint64_t* p_full = s_empty + kSBufs;    // [2]: P buffer b written
+  uint64_t* o_done = p_full + 2;          // [2]: PV of the tile using P buffer b done
+  uint64_t* final_bar = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+  volatile int* need_rescale = reinterpret_cast<volatile int*>(smem + kMiscOff + 8);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int split = blockIdx.x, b = blockIdx.y;
+  const int rows = p.R * p.Hq;
+  const int row_base = blockIdx.z * kRows;
+  const int C = p.cluster;
+  const uint32_t rank = C > 1 ? sm100::cluster_ctarank() : 0u;
+  const uint16_t peers = (uint16_t)((1u << C) - 1u);
+  const int ctx = p.ctx_lens[b];
+  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {   // uniform over the cluster (same request)
+    if (threadIdx.x == 0 && split == 0 && blockIdx.z == 0) raise_error(p.err, MTP_ERR_LENGTH);
+    return;
+  }
+  // Every CTA of a cluster walks the same keys (those visible to the cluster's
+  // last row); rows that see fewer keys mask the rest.
+  const int cluster_rows_end = min((int)(blockIdx.z / C + 1) * C * kRows, rows);
+  const int j_max = min(p.R - 1, (cluster_rows_end - 1) / p.Hq);
+  const int t0 = split * p.split_len;
+  const int t_end = min(t0 + p.split_len, ctx + j_max + 1);
+  if (t0 >= t_end) return;  // no key of this split is visible to these rows: the combine skips it
+  const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kKStages; ++s) {
+      sm100::mbar_init(&kfull[s], 1);
+      sm100::mbar_init(&kempty[s], C);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      sm100::mbar_init(&vfull[s], 1);
+      sm100::mbar_init(&vempty[s], C);
+    }
+    sm100::mbar_init(qbar, 1);
+    for (int i = 0; i < kSBufs; ++i) {
+      sm100::mbar_init(&s_full[i], 1);
+      sm100::mbar_init(&s_empty[i], kSoftWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      sm100::mbar_init(&p_full[i], kSoftWarps);
+      sm100::mbar_init(&o_done[i], 1);
+    }
+    sm100::mbar_init(final_bar, 1);
+    *abort = 0;
+    *need_rescale = 0;
+    sm100::fence_barrier_init();
+  }
+  if (warp == 0) {
+    sm100::tmem_alloc(tmem_slot, kTmemCols);
+    sm100::tmem_relinquish();
+  }
+  if (threadIdx.x < kRows) {
+    const int rr = min(row_base + (int)threadIdx.x, rows - 1);
+    lim[threadIdx.x] = ctx + rr / p.Hq;
+    m_run[threadIdx.x] = -INFINITY;
+    l_run[threadIdx.x] = 0.0f;
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (C > 1) sm100::cluster_sync();   // peers' barriers exist before any multicast lands
+  sm100::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem_base = sm100::smem_u32(smem);
+
+  auto softmax_role = [&]() {
+    // ------------------------------------------------------- softmax warps
+    const int sw = warp - 4;                 // 0..7
+    const int qq = warp % 4;                 // TMEM lane quarter: keys / dv 32*qq + lane
+    const int ch = sw >> 2;                  // row half: rows 32*ch .. 32*ch+31
+    const int st = sw * 32 + lane;           // 0..255
+    const uint32_t lane_addr = (uint32_t)(32 * qq) << 16;
+    // Every softmax warp runs the same sequence of named barriers for every
+    // tile; after an abort the tensor-memory work is skipped but the barrier
+    // sequence is kept, so no warp is left waiting on the others.
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int buf = i % kSBufs;
+      ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&s_full[buf], (i / kSBufs) & 1, abort) ? 1 : 0);
+      float s[32];
+      if (ok) {
+        sm100::tc_fence_after();
+        uint32_t r[32];
+        sm100::tmem_ld_32x32b_x32(tmem + lane_addr + kColS + buf * 64 + ch * 32, r);
+        sm100::tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) s[x] = __uint_as_float(r[x]);
+        sm100::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(&s_empty[buf]);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) s[x] = -INFINITY;
+      }
+      const int key = t0 + i * kKeys + 32 * qq + lane;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const float v = s[x] * p.scale_log2;
+        s[x] = (key > lim[ch * 32 + x] || key >= t_end) ? -INFINITY : v;
+      }
+      {
+        float t[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) t[x] = s[x];
+        red_max[qq * 64 + ch * 32 + lane] = transpose_reduce<true>(t, lane);
+      }
+      softmax_barrier();
+      if (st < kRows) {
+        const float mt = fmaxf(fmaxf(red_max[st], red_max[64 + st]), fmaxf(red_max[128 + st], red_max[192 + st]));
+        const float mo = m_run[st];
+        float mn = mo, sc = 1.0f;
+        if (mt > mo + kLazyRescale) {
+          mn = mt;
+          sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+          if (i > 0 && sc != 1.0f) *need_rescale = 1;
+        }
+        m_run[st] = mn;
+        m_ref[st] = mn == -INFINITY ? 0.0f : mn;
+        rscale[st] = sc;
+        l_run[st] *= sc;
+      }
+      softmax_barrier();
+#pragma unroll
+      for (int x = 0; x < 32; ++x) s[x] = exp2f(s[x] - m_ref[ch * 32 + x]);   // s now holds p
+      // P buffer i%2 is free once PV(i-2) is done; rescaling O^T needs every
+      // earlier PV done (completions are in issue order, so PV(i-1) suffices).
+      if (i >= 2 && !*need_rescale)
+        ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&o_done[i & 1], ((i >> 1) - 1) & 1, abort) ? 1 : 0);
+      if (i >= 1 && *need_rescale) {
+        ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort) ? 1 : 0);
+        if (ok) {
+          sm100::tc_fence_after();
+#pragma unroll 1
+          for (int dc = 0; dc < 4; ++dc) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_addr + kColO + dc * 64 + ch * 32;
+            sm100::tmem_ld_32x32b_x32(ta, r);
+            sm100::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * rscale[ch * 32 + x]);
+            tmem_st_32x32b_x32(ta, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P^T (bf16) into the K-major B tile: block of 64 keys, row, key.
+      {
+        const int k = 32 * qq + lane;
+        uint8_t* pb = smem + kPOff + (i & 1) * kPBytes + (k >> 6) * 8192;
+        const int kin = k & 63;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int r = ch * 32 + x;
+          *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kin >> 3) ^ (r & 7))) << 4) + (kin & 7) * 2) =
+              __float2bfloat16_rn(s[x]);
+        }
+      }
+      red_sum[qq * 64 + ch * 32 + lane] = transpose_reduce<false>(s, lane);
+      fence_async_smem();
+      sm100::tc_fence_before();
+      softmax_barrier();
+      if (st < kRows) l_run[st] += red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
+      if (st == 0) *need_rescale = 0;
+      __syncwarp();
+      if (lane == 0 && ok) sm100::mbar_arrive(&p_full[i & 1]);
+    }
+    if (!ok && lane == 0) {
+      *abort = 1;
+      raise_error(p.err, MTP_ERR_TIMEOUT);
+    }
+    // -------------------------------------------------------- epilogue
+    const bool done =
+        ok && __all_sync(0xffffffffu,
+                         sm100::mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort) ? 1 : 0);
+    softmax_barrier();
+    if (done) {
+      sm100::tc_fence_after();
+      const int dvl = 32 * qq + lane;
+#pragma unroll 1
+      for (int dc = 0; dc < 4; ++dc) {
+        const int dv = dc * 128 + dvl;
+        uint32_t r[32];
+        sm100::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + dc * 64 + ch * 32, r);
+        sm100::tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int rloc = ch * 32 + x;
+          const int rr = row_base + rloc;
+          if (rr >= rows) continue;
+          const float l = l_run[rloc];
+          const float o = l > 0.0f ? __uint_as_float(r[x]) / l : 0.0f;
+          const int64_t orow = (int64_t)b * rows + rr;
+          if (p.n_splits == 1) p.out[orow * kDV + dv] = __float2bfloat16_rn(o);
+          else p.part_o[(orow * p.n_splits + split) * kDV + dv] = o;
+        }
+      }
+      if (p.n_splits > 1 && st < kRows && row_base + st < rows) {
+        const float l = l_run[st];
+        const int64_t orow = (int64_t)b * rows + row_base + st;
+        p.part_lse[orow * p.n_splits + split] = l > 0.0f ? (m_run[st] + log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+    };
+
+  // Warp roles. Warpgroups 0 and 3 hand registers to the softmax warpgroups
+  // (every warp of a warpgroup runs the same setmaxnreg).
+  const int wg = warp / 4;
+  const int k_prod = (warp == 1 || warp == 2) ? warp - 1 : -1;    // two K-ring producers
+  const int v_prod = warp == 3 ? 0 : (warp == 12 ? 1 : -1);       // two V-ring producers
+  if (wg == 1 || wg == 2) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    softmax_role();
+  } else {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
+  if (k_prod >= 0 || v_prod >= 0) {
+    // ------------------------------------------- TMA producers (K ring / V ring)
+    // Fills alternate between the two producers of a ring; lanes 0 and 1 of a
+    // producer issue the stage's two boxes together.
+    if (lane < 2) {
+      const bool is_k = k_prod >= 0;
+      const int pidx = is_k ? k_prod : v_prod;
+      const uint64_t pol_kv = sm100::l2_policy_evict_last();   // the V pass and the other row blocks re-read it
+      if (is_k && pidx == 0 && lane == 0) {
+        sm100::tma_prefetch_desc(&tm_q);
+        sm100::tma_prefetch_desc(&tm_kv);
+        sm100::mbar_arrive_expect_tx(qbar, kQChunks * 8192);
+        const uint64_t pol_q = sm100::l2_policy_evict_first();
+        for (int c = 0; c < kQChunks; ++c)
+          sm100::tma_load_2d(smem + kQOff + c * 8192, &tm_q, qbar, c * 64, b * rows + row_base, pol_q);
+      }
+      const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
+      auto block_of = [&](int key0) -> int {   // cache block holding keys key0..key0+63, or -1 (zero fill)
+        if (key0 >= t_end) return -1;
+        const int blk = tbl[key0 / kBlock];
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (is_k) raise_error(p.err, MTP_ERR_BLOCK_ID);
+          return -1;
+        }
+        return blk;
+      };
+      uint64_t* fullb = is_k ? kfull : vfull;
+      uint64_t* emptyb = is_k ? kempty : vempty;
+      const int nst = is_k ? kKStages : kVStages;
+      uint8_t* base = smem + (is_k ? kKOff : kVOff);
+      const int nchunks = is_k ? kQChunks : 8;
+      bool ok = true;
+      for (int seq = pidx; seq < n_tiles * nchunks && ok; seq += 2) {
+        const int i = seq / nchunks, c = seq % nchunks;
+        const int stage = seq % nst;
+        const uint32_t phase = (uint32_t)((seq / nst) & 1);
+        const int key0 = t0 + i * kKeys;
+        // Empty once every CTA of the cluster consumed the previous fill.
+        if (lane == 0) ok = sm100::mbar_wait(&emptyb[stage], phase ^ 1u, abort);
+        ok = __shfl_sync(0x3u, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        uint8_t* dst = base + stage * kStageBytes;
+        uint64_t* bar = &fullb[stage];
+        if (lane == 0) sm100::mbar_arrive_expect_tx(bar, kStageBytes);
+        __syncwarp(0x3u);
+        if (seq % C == (int)rank) {
+          int x, z;
+          if (is_k) {          // [128 keys x 64 dims]: lane 0 keys 0..63, lane 1 keys 64..127
+            x = c * 64;
+            z = block_of(key0 + lane * 64);
+          } else {             // [64 keys x 128 dv] for key half c / 4, dv chunk c % 4
+            x = (c & 3) * 128 + lane * 64;
+            z = block_of(key0 + (c >> 2) * 64);
+          }
+          if (C > 1) sm100::tma_load_3d_mc(dst + lane * 8192, &tm_kv, bar, x, 0, z, peers, pol_kv);
+          else sm100::tma_load_3d(dst + lane * 8192, &tm_kv, bar, x, 0, z, pol_kv);
+        }
+      }
+      if (!ok && lane == 0) {
+        *abort = 1;
+        raise_error(p.err, MTP_ERR_TIMEOUT);
+      }
+      // Every copy must land before the CTA may exit: wait (time-limited) for
+      // the latest fill of each stage (it completes after all earlier ones);
+      // the producer that made that fill waits for it.
+      if (lane == 0) {
+        if (is_k && pidx == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
+        const int total = n_tiles * nchunks;
+        for (int st2 = 0; st2 < nst && st2 < total; ++st2) {
+          const int last = st2 + ((total - 1 - st2) / nst) * nst;
+          if (last % 2 != pidx) continue;
+          sm100::mbar_wait_timeout(&fullb[st2], (uint32_t)((last / nst) & 1), sm100::kWaitTimeoutNs);
+        }
+      }
+    }
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- MMA
+    // Order: QK of two tiles ahead, then PV of the oldest tile. A consumed
+    // ring stage is released to every CTA of the cluster (multicast commit).
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, kRows);
+      constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, kRows) | (1u << 15);   // A (V^T) MN-major
+      Ring kr{kfull, kempty, kKStages, 0, 0u};
+      Ring vr{vfull, vempty, kVStages, 0, 0u};
+      auto release = [&](Ring& r) {
+        if (C > 1) sm100::tc_commit_mc(&r.empty[r.stage], peers);
+        else sm100::tc_commit(&r.empty[r.stage]);
+        r.advance();
+      };
+      bool ok = sm100::mbar_wait(qbar, 0, abort);
+      auto issue_qk = [&](int i) -> bool {
+        const int buf = i % kSBufs;
+        if (!sm100::mbar_wait(&s_empty[buf], ((i / kSBufs) & 1) ^ 1u, abort)) return false;
+        sm100::tc_fence_after();
+        const uint32_t d = tmem + kColS + buf * 64;
+        for (int c = 0; c < kQChunks; ++c) {
+          if (!sm100::mbar_wait(&kr.full[kr.stage], kr.phase, abort)) return false;
+          sm100::tc_fence_after();
+          const uint32_t a = smem_base + kKOff + kr.stage * kStageBytes;
+          const uint32_t qa = smem_base + kQOff + c * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            sm100::tc_mma_bf16(d, desc_kmajor(a + kk * 32), desc_kmajor(qa + kk * 32), idesc_qk,
+                               (c > 0 || kk > 0) ? 1u : 0u);
+          release(kr);
+        }
+        sm100::tc_commit(&s_full[buf]);
+        return true;
+      };
+      auto issue_pv = [&](int i) -> bool {
+        if (!sm100::mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort)) return false;
+        sm100::tc_fence_after();
+        for (int c = 0; c < 8; ++c) {
+          const int kh = c >> 2, dc = c & 3;
+          if (!sm100::mbar_wait(&vr.full[vr.stage], vr.phase, abort)) return false;
+          sm100::tc_fence_after();
+          const uint32_t a = smem_base + kVOff + vr.stage * kStageBytes;
+          const uint32_t pb = smem_base + kPOff + (i & 1) * kPBytes + kh * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            sm100::tc_mma_bf16(tmem + kColO + dc * 64, desc_mnmajor(a + kk * 2048, 8192), desc_kmajor(pb + kk * 32),
+                               idesc_pv, (i > 0 || kh > 0 || kk > 0) ? 1u : 0u);
+          release(vr);
+        }
+        sm100::tc_commit(&o_done[i & 1]);
+        return true;
+      };
+      for (int i = 0; i < kSBufs - 1 && i < n_tiles && ok; ++i) ok = issue_qk(i);
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        if (i + kSBufs - 1 < n_tiles) ok = issue_qk(i + kSBufs - 1);
+        if (ok) ok = issue_pv(i);
+      }
+      if (!ok) {
+        *abort = 1;
+        raise_error(p.err, MTP_ERR_TIMEOUT);
+      }
+      sm100::tc_commit(final_bar);
+      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
+    }
+  }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (C > 1) sm100::cluster_sync();   // no peer may still multicast into, or arrive on, this CTA
+}
+
+}  // namespace
+
+int mla_tc_split_granularity() { return kKeys; }
+
+cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, cudaStream_t s) {
+  if (a.B == 0) return cudaSuccess;
+  if (pl.split_len % kKeys) return cudaErrorInvalidValue;
+  const int R = a.D + 1, rows = R * a.Hq;
+  CUtensorMap tq, tkv;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kDQ, (cuuint64_t)a.B * rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kDQ * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+    if (!make_bf16_map(&tq, a.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kDQ, (cuuint64_t)kBlock, (cuuint64_t)a.num_blocks};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDQ * 2, (cuuint64_t)kBlock * kDQ * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBlock, 1};
+    if (!make_bf16_map(&tkv, a.k_cache, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Params p;
+  p.out = (__nv_bfloat16*)a.out;
+  p.part_o = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_o) : nullptr;
+  p.part_lse = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_lse) : nullptr;
+  p.block_table = a.block_table;
+  p.ctx_lens = a.ctx_lens;
+  p.err = err;
+  p.R = R;
+  p.Hq = a.Hq;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.split_len = pl.split_len;
+  p.n_splits = pl.n_splits;
+  p.scale_log2 = a.sm_scale * kLog2e;
+  const int row_blocks = (rows + kRows - 1) / kRows;
+  int C = kMaxCluster;
+  while (row_blocks % C) --C;   // cluster = row blocks of one request, at most kMaxCluster
+  p.cluster = C;
+  cudaError_t e = cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.n_splits, a.B, row_blocks);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = C;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tq, tkv, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace mtp

@@ -9,15 +9,10 @@
 // TensorRT-LLM", attention for MTP: K+1 chained queries need only a causal
 // mask. Row of verify token j (request context ctx) attends slots 0..ctx+j.
 //
-// Two kernels:
-//   attn_gqa_kernel<D>  GQA/MHA, d_qk = d_v = D (64 or 128). CTA = (split,
-//                       request x KV head, row block): the g*R query rows
-//                       that share one KV head (up to 128: one consumer warp
-//                       per 16 rows), 64-key tiles = one cache block.
-//   attn_mla_kernel     absorbed MLA: one latent KV head of 576 (value = its
-//                       first 512). CTA = (split, request, 64 query rows);
-//                       the Q tile stays in shared memory; 8 consumer warps
-//                       = 4 groups of 16 rows x 2 halves of the value width.
+// attn_gqa_kernel<D>: GQA/MHA, d_qk = d_v = D (64 or 128). CTA = (split,
+// request x KV head, row block): the g*R query rows that share one KV head
+// (up to 112: one consumer warp per 16 rows), 64-key tiles = one cache
+// block. (Absorbed MLA runs on tcgen05: attention_mla_tc.cu.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -311,269 +306,6 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
 }
 
 
-// ------------------------------------------------------------------ MLA
-struct MlaCfg {
-  static constexpr int kDQ = 576, kDV = 512;
-  static constexpr int kTileKeys = 32;                       // half a cache block per stage
-  static constexpr int kRows = 64;                           // query rows per CTA
-  static constexpr int kKBox = kTileKeys * 128;              // [32 keys][64 dims] box, 4 KB
-  static constexpr int kStageBytes = (kDQ / 64) * kKBox;     // 36 KB
-  static constexpr int kQBox = kRows * 128;                  // [64 rows][64 dims] box, 8 KB
-  static constexpr int kQBytes = (kDQ / 64) * kQBox;         // 72 KB
-};
-
-struct MlaParams {
-  __nv_bfloat16* out;
-  float* part_o;
-  float* part_lse;
-  const int32_t* block_table;
-  const int32_t* ctx_lens;
-  unsigned* err;
-  int R, Hq;
-  int max_blocks, num_blocks, split_len, n_splits, stages;
-  float scale_log2;
-};
-
-__global__ void __launch_bounds__(256, 1) attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                          const __grid_constant__ CUtensorMap tm_kv,
-                                                          const MlaParams p) {
-  using C = MlaCfg;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem;
-  uint8_t* kv = smem + C::kQBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(kv + p.stages * C::kStageBytes);
-  uint64_t* empty = full + p.stages;
-  uint64_t* qbar = empty + p.stages;
-  int* stage_valid = reinterpret_cast<int*>(qbar + 1);
-  volatile int* abort = stage_valid + p.stages;
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int split = blockIdx.x, b = blockIdx.y;
-  const int rows = p.R * p.Hq;
-  const int row_base = blockIdx.z * C::kRows;   // first request-local row of this CTA
-  const int ctx = p.ctx_lens[b];
-  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.z == 0) raise_error(p.err, MTP_ERR_LENGTH);
-    return;
-  }
-  // Rows of this CTA see at most ctx + j_max + 1 keys.
-  const int j_max = min(p.R - 1, (min(row_base + C::kRows, rows) - 1) / p.Hq);
-  const int t0 = split * p.split_len;
-  const int t_end = min(t0 + p.split_len, ctx + j_max + 1);
-  if (t0 >= t_end) return;   // nothing visible to these rows in this split: the combine skips it
-  const int n_tiles = (t_end - t0 + C::kTileKeys - 1) / C::kTileKeys;
-  const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
-
-  // Producer duties run on thread 0 between its own tiles: it fills stage
-  // (i % stages) with tile i once all 8 warps have released that stage.
-  int last_parity[8];
-  uint64_t pol_kv = 0;
-  auto issue = [&](int i, int stage, uint32_t phase) {
-    const int key0 = t0 + i * C::kTileKeys;
-    const int blk = tbl[key0 / kBlock];
-    const bool valid = blk >= 0 && blk < p.num_blocks;
-    stage_valid[stage] = valid ? 1 : 0;
-    if (valid) {
-      sm100::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-      uint8_t* dst = kv + stage * C::kStageBytes;
-#pragma unroll 1
-      for (int c = 0; c < C::kDQ / 64; ++c)
-        sm100::tma_load_3d(dst + c * C::kKBox, &tm_kv, &full[stage], c * 64, key0 % kBlock, blk, pol_kv);
-      last_parity[stage] = (int)phase;
-    } else {
-      raise_error(p.err, MTP_ERR_BLOCK_ID);
-      sm100::mbar_arrive(&full[stage]);
-    }
-  };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      sm100::mbar_init(&full[s], 1);
-      sm100::mbar_init(&empty[s], 8);
-    }
-    sm100::mbar_init(qbar, 1);
-    *abort = 0;
-    sm100::fence_barrier_init();
-    sm100::tma_prefetch_desc(&tm_q);
-    sm100::tma_prefetch_desc(&tm_kv);
-    pol_kv = sm100::l2_policy_evict_last();   // re-read by the request's other row blocks
-    for (int s2 = 0; s2 < 8; ++s2) last_parity[s2] = -1;
-    sm100::mbar_arrive_expect_tx(qbar, C::kQBytes);
-    const int qrow0 = b * rows + row_base;
-    const uint64_t pol_q = sm100::l2_policy_evict_first();
-#pragma unroll 1
-    for (int c = 0; c < C::kDQ / 64; ++c) sm100::tma_load_2d(qs + c * C::kQBox, &tm_q, qbar, c * 64, qrow0, pol_q);
-    for (int i = 0; i < min(p.stages, n_tiles); ++i) issue(i, i, 0);
-  }
-  __syncthreads();
-
-  // ---------------------------------------------------------- consumers
-  const int cw = warp;
-  const int rg = cw & 3, vh = cw >> 2;            // 16-row group, value half
-  const int g = lane >> 2, t = lane & 3, mi = lane >> 3;
-  const int r_lo = row_base + rg * 16 + g, r_hi = r_lo + 8;
-  const int j_lo = min(r_lo, rows - 1) / p.Hq, j_hi = min(r_hi, rows - 1) / p.Hq;
-  const int lim_lo = ctx + j_lo, lim_hi = ctx + j_hi;
-  const uint32_t q_base = sm100::smem_u32(qs);
-
-  float o[32][4];
-#pragma unroll
-  for (int n = 0; n < 32; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.0f, l_hi = 0.0f;
-
-  bool ok = __all_sync(0xffffffffu, sm100::mbar_wait(qbar, 0, abort) ? 1 : 0) != 0;
-  int stage = 0;
-  uint32_t phase = 0;
-  for (int i = 0; i < n_tiles && ok; ++i) {
-    if (!__all_sync(0xffffffffu, sm100::mbar_wait(&full[stage], phase, abort) ? 1 : 0)) {
-      ok = false;
-      break;
-    }
-    if (stage_valid[stage]) {
-      const uint32_t kb = sm100::smem_u32(kv + stage * C::kStageBytes);
-      float s[4][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
-#pragma unroll 4
-      for (int kk = 0; kk < C::kDQ / 16; ++kk) {
-        uint32_t a[4];
-        mma::ldsm_x4(q_base + mma::sw128_boxed(C::kRows, rg * 16 + (lane & 15), kk * 16 + (lane >> 4) * 8), a[0],
-                     a[1], a[2], a[3]);
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t b0, b1, b2, b3;
-          mma::ldsm_x4(kb + mma::sw128_boxed(C::kTileKeys, np * 16 + (mi >> 1) * 8 + (lane & 7), kk * 16 + (mi & 1) * 8),
-                       b0, b1, b2, b3);
-          mma::mma_bf16_16816(s[2 * np], a, b0, b1);
-          mma::mma_bf16_16816(s[2 * np + 1], a, b2, b3);
-        }
-      }
-      const int tk = t0 + i * C::kTileKeys;
-      const bool need_mask = tk + C::kTileKeys - 1 > min(lim_lo, lim_hi);
-      float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = s[n][e] * p.scale_log2;
-          if (need_mask) {
-            const int key = tk + n * 8 + 2 * t + (e & 1);
-            if (key > ((e < 2) ? lim_lo : lim_hi)) v = -INFINITY;
-          }
-          s[n][e] = v;
-        }
-        mx_lo = fmaxf(mx_lo, fmaxf(s[n][0], s[n][1]));
-        mx_hi = fmaxf(mx_hi, fmaxf(s[n][2], s[n][3]));
-      }
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-      const float base_lo = mn_lo == -INFINITY ? 0.0f : mn_lo;
-      const float base_hi = mn_hi == -INFINITY ? 0.0f : mn_hi;
-      const float c_lo = exp2f(m_lo - base_lo), c_hi = exp2f(m_hi - base_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-      l_lo *= c_lo;
-      l_hi *= c_hi;
-#pragma unroll
-      for (int n = 0; n < 32; ++n) {
-        o[n][0] *= c_lo;
-        o[n][1] *= c_lo;
-        o[n][2] *= c_hi;
-        o[n][3] *= c_hi;
-      }
-      uint32_t pa[2][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const float p0 = exp2f(s[n][0] - base_lo), p1 = exp2f(s[n][1] - base_lo);
-        const float p2 = exp2f(s[n][2] - base_hi), p3 = exp2f(s[n][3] - base_hi);
-        l_lo += p0 + p1;
-        l_hi += p2 + p3;
-        pa[n >> 1][(n & 1) * 2 + 0] = mma::pack_bf16(p0, p1);
-        pa[n >> 1][(n & 1) * 2 + 1] = mma::pack_bf16(p2, p3);
-      }
-      // O[:, half] += P V[:, half]; V = first 512 latent dims.
-#pragma unroll
-      for (int kp = 0; kp < 2; ++kp) {
-#pragma unroll
-        for (int dp = 0; dp < 16; ++dp) {
-          uint32_t b0, b1, b2, b3;
-          mma::ldsm_x4_trans(kb + mma::sw128_boxed(C::kTileKeys, kp * 16 + (mi & 1) * 8 + (lane & 7),
-                                                   vh * 256 + dp * 16 + (mi >> 1) * 8),
-                             b0, b1, b2, b3);
-          mma::mma_bf16_16816(o[2 * dp], pa[kp], b0, b1);
-          mma::mma_bf16_16816(o[2 * dp + 1], pa[kp], b2, b3);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) sm100::mbar_arrive(&empty[stage]);
-    if (threadIdx.x == 0 && i + p.stages < n_tiles) {
-      // Refill this stage with tile i + stages once every warp released it.
-      if (sm100::mbar_wait(&empty[stage], phase, abort)) {
-        issue(i + p.stages, stage, phase ^ 1u);
-      } else {
-        *abort = 1;
-        raise_error(p.err, MTP_ERR_TIMEOUT);
-      }
-    }
-    __syncwarp();
-    if (++stage == p.stages) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  }
-  if (!ok) {
-    if (lane == 0) {
-      *abort = 1;
-      raise_error(p.err, MTP_ERR_TIMEOUT);
-    }
-  }
-  if (threadIdx.x == 0) {
-    // Every copy issued must land before the CTA may exit.
-    sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
-    for (int s2 = 0; s2 < p.stages; ++s2)
-      if (last_parity[s2] >= 0)
-        sm100::mbar_wait_timeout(&full[s2], (uint32_t)last_parity[s2], sm100::kWaitTimeoutNs);
-  }
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = l_lo > 0.0f ? 1.0f / l_lo : 0.0f;
-  const float inv_hi = l_hi > 0.0f ? 1.0f / l_hi : 0.0f;
-  const bool st_lo = r_lo < rows, st_hi = r_hi < rows;
-  const int64_t orow_lo = (int64_t)b * rows + r_lo, orow_hi = (int64_t)b * rows + r_hi;
-  if (p.n_splits == 1) {
-#pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      const int dim = vh * 256 + n * 8 + 2 * t;
-      if (st_lo)
-        *reinterpret_cast<uint32_t*>(p.out + orow_lo * C::kDV + dim) = mma::pack_bf16(o[n][0] * inv_lo, o[n][1] * inv_lo);
-      if (st_hi)
-        *reinterpret_cast<uint32_t*>(p.out + orow_hi * C::kDV + dim) = mma::pack_bf16(o[n][2] * inv_hi, o[n][3] * inv_hi);
-    }
-  } else {
-#pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      const int dim = vh * 256 + n * 8 + 2 * t;
-      if (st_lo)
-        *reinterpret_cast<float2*>(p.part_o + (orow_lo * p.n_splits + split) * C::kDV + dim) =
-            make_float2(o[n][0] * inv_lo, o[n][1] * inv_lo);
-      if (st_hi)
-        *reinterpret_cast<float2*>(p.part_o + (orow_hi * p.n_splits + split) * C::kDV + dim) =
-            make_float2(o[n][2] * inv_hi, o[n][3] * inv_hi);
-    }
-    if (t == 0 && vh == 0) {
-      if (st_lo) p.part_lse[orow_lo * p.n_splits + split] = l_lo > 0.0f ? m_lo * kLn2 + logf(l_lo) : -INFINITY;
-      if (st_hi) p.part_lse[orow_hi * p.n_splits + split] = l_hi > 0.0f ? m_hi * kLn2 + logf(l_hi) : -INFINITY;
-    }
-  }
-}
-
 // --------------------------------------------------------------- launchers
 template <int D>
 int gqa_smem_bytes(int stages) {
@@ -618,46 +350,6 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
   return cudaGetLastError();
 }
 
-cudaError_t run_mla(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, cudaStream_t s) {
-  using C = MlaCfg;
-  const int stages = 3;
-  const int R = a.D + 1, rows = R * a.Hq;
-  CUtensorMap tq, tkv;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)C::kDQ, (cuuint64_t)a.B * rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)C::kDQ * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)C::kRows};
-    if (!make_bf16_map(&tq, a.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)C::kDQ, (cuuint64_t)kBlock, (cuuint64_t)a.num_blocks};
-    const cuuint64_t strides[2] = {(cuuint64_t)C::kDQ * 2, (cuuint64_t)kBlock * C::kDQ * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)C::kTileKeys, 1};
-    if (!make_bf16_map(&tkv, a.k_cache, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  MlaParams p;
-  p.out = (__nv_bfloat16*)a.out;
-  p.part_o = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_o) : nullptr;
-  p.part_lse = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_lse) : nullptr;
-  p.block_table = a.block_table;
-  p.ctx_lens = a.ctx_lens;
-  p.err = err;
-  p.R = R;
-  p.Hq = a.Hq;
-  p.max_blocks = a.max_blocks;
-  p.num_blocks = a.num_blocks;
-  p.split_len = pl.split_len;
-  p.n_splits = pl.n_splits;
-  p.stages = stages;
-  p.scale_log2 = a.sm_scale * kLog2e;
-  const int smem = C::kQBytes + stages * C::kStageBytes + stages * 20 + 64 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(pl.n_splits, a.B, (rows + C::kRows - 1) / C::kRows);
-  attn_mla_kernel<<<grid, 256, smem, s>>>(tq, tkv, p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 bool attention_mma_supported(const mtp_attn_args& a) {
@@ -672,8 +364,7 @@ cudaError_t launch_attention_mma(const mtp_attn_args& a, const AttnPlan& p, unsi
 }
 
 cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s) {
-  if (a.B == 0) return cudaSuccess;
-  return run_mla(a, p, err, s);
+  return launch_attention_mla_tc(a, p, err, s);
 }
 
 }  // namespace mtp

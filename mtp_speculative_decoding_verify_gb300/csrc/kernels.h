@@ -25,6 +25,7 @@ cudaError_t launch_kv_append(const mtp_attn_args& a, unsigned* err, cudaStream_t
 cudaError_t launch_attention_simt(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_mma(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ LM head

@@ -85,7 +85,7 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   off += 16;                                     // TMEM base, abort flag
   off = (off + 15) / 16 * 16;
   L.epi_off = off;
-  off += 4 * 32 * 33 * 4;                        // per-epilogue-warp 32x33 transpose buffers
+  off += 4 * 32 * 33 * 4;                        // per-epilogue-warp 32x33 transpose buffers (later: 4 x N row stats)
   L.rows_off = off;
   off += N * 12;                                 // per-row draft id, 1/T, sampling flag
   L.total = off + 1024;                          // + alignment slack for the 1024-B aligned base
@@ -322,18 +322,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       __syncwarp();
       if (lane == 0) sm100::mbar_arrive(&acc_empty[buf]);
     }
-    // Partials of this (CTA, lane quarter): slice = cta_in_group * 4 + q.
-    const int slice = cta_in_group * 4 + q;
+    // Merge the four lane quarters' statistics through shared memory, then
+    // write one partial per (CTA, row): slice = cta_in_group.
+    asm volatile("bar.sync 1, 128;" ::: "memory");            // every epilogue warp is done with its buffer
+    RowStat* ex = reinterpret_cast<RowStat*>(epi_buf);         // [4][N]
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int m = row0 + c * 32 + lane;
-      if (m < p.M) {
-        const int64_t o = (int64_t)slice * p.M + m;
-        p.pmax[o] = st[c].m;
-        p.psum[o] = st[c].s;
-        p.pbest[o] = st[c].best;
-        p.pidx[o] = st[c].idx;
-      }
+    for (int c = 0; c < NCH; ++c) ex[q * N + c * 32 + lane] = st[c];
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int r = (warp - 2) * 32 + lane; r < N; r += 128) {
+      const int m = row0 + r;
+      if (m >= p.M) continue;
+      RowStat a = rowstat_merge(rowstat_merge(ex[r], ex[N + r]), rowstat_merge(ex[2 * N + r], ex[3 * N + r]));
+      const int64_t o = (int64_t)cta_in_group * p.M + m;
+      p.pmax[o] = a.m;
+      p.psum[o] = a.s;
+      p.pbest[o] = a.best;
+      p.pidx[o] = a.idx;
     }
   }
   sm100::tc_fence_before();
@@ -390,7 +394,7 @@ bool lmhead_tc_supported(const mtp_lmhead_args& a) {
 
 int lmhead_tc_slices(int V, int M, int sm_count) {
   (void)V;
-  return tc_shape(M, sm_count).cpg * 4;
+  return tc_shape(M, sm_count).cpg;
 }
 
 cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& pl, unsigned* err, cudaStream_t s) {
@@ -399,7 +403,7 @@ cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& pl, unsigne
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const TcShape sh = tc_shape(pl.M, sms);
-  if (sh.cpg * 4 != pl.slices) return cudaErrorInvalidValue;
+  if (sh.cpg != pl.slices) return cudaErrorInvalidValue;
   CUtensorMap tw, th;
   if (!make_map(&tw, a.lm_head, (uint64_t)a.V, (uint64_t)a.H, kTileV)) return cudaErrorInvalidValue;
   if (!make_map(&th, a.hidden, (uint64_t)pl.M, (uint64_t)a.H, (uint32_t)sh.N)) return cudaErrorInvalidValue;

@@ -37,6 +37,9 @@ SMALL = {
     "cfg3_small_mixed": synth.CFG3.with_(name="GQA bf16 mixed small", B=8, Hq=8, Hkv=2, ctx=(64, 700), H=256,
                                          V=7001),
     "mha_bf16_d64": synth.CFG0.with_(name="MHA bf16 d64", dtype="bf16", ctx=(0, 200), B=5, H=128, V=999),
+    # MLA with 4 and 3 row blocks per request: clusters sharing KV tiles by multicast
+    "mla_cluster4": synth.CFG1.with_(name="MLA 4 row blocks", B=3, Hq=64, ctx=(60, 700), H=256, V=2000),
+    "mla_cluster3": synth.CFG1.with_(name="MLA 3 row blocks", B=2, Hq=48, ctx=(130, 400), H=128, V=777),
 }
 
 
