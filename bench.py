@@ -65,6 +65,14 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
+# DRAM bytes per launch of the LM-head kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), by workload. The capture ran
+# a reduced vocabulary (32768) of the same kernel and shapes; traffic grows in
+# proportion to the vocabulary, so it is scaled to the full one. Only valid
+# while the kernel is unchanged since the capture (profiles/ names the file).
+LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.688704e6 + 3.054592e6) / 32768}
+
+
 def elem_bytes(w):
     return 4 if w.dtype == "f32" else 2
 
@@ -431,7 +439,10 @@ def main():
         roof = dict(kernel="lm_head", bound="tensor", achieved=alg["lm_flops"] / (r["lm_ms"] * 1e-3) / 1e12,
                     peak=tc_peak, unit="TFLOP/s", peak_source=src + " (bf16_tflops burst)")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    per_row = LMHEAD_TRAFFIC_PER_VOCAB_ROW.get(args.workload)
+    roof["traffic"] = per_row * w.V if per_row else None
+    roof["traffic_note"] = ("ncu capture of the same kernel at vocab 32768, scaled to the full vocabulary"
+                            if per_row else "no capture for this workload")
     roof["avg_launch_ms"] = r["lm_ms"]
     step_bound_s = max((alg["kv_bytes"] + alg["w_bytes"]) / (hbm * 1e9),
                        (alg["lm_flops"] + alg["attn_flops"]) / (tc_peak * 1e12))
