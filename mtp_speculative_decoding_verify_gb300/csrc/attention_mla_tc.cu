@@ -9,31 +9,33 @@
 // Transposed formulation so that every operand fits the tensor memory:
 //   S^T [128 keys x 64 rows]  = K_tile [128 x 576] . Q^T        (M = keys)
 //   O^T [512 dv   x 64 rows] += V^T [dv x 128 keys] . P^T         (M = 128 dv, 4 chunks)
-// TMEM: O^T in columns 0..255 (4 chunks x 64), three S^T buffers in 256..447
-// so that two QK tiles run ahead of the softmax. The Q tile (64 rows x 576,
-// 72 KB) stays in shared memory; K chunks [128 keys x 64 dims] and V chunks
-// [64 keys x 128 dv] stream through two separate 16 KB-stage TMA rings (V is
-// read a second time, from L2, after the softmax), so K of later tiles keeps
-// flowing while V waits for P. V^T is consumed MN-major straight from the
-// cache layout (dv contiguous).
+// TMEM: O^T in columns 0..255 (4 chunks x 64), two S^T buffers in 256..383.
+// Shared memory holds the Q tile (64 rows x 576, 72 KB) and the whole key
+// tile: nine 16 KB slots, slot c = [128 keys x 64 dims] for dims 64c..64c+63.
+// QK reads them K-major; PV reads V^T MN-major straight from slots 2dc and
+// 2dc+1 (the value is the first 512 latent dims), so the cache is read once.
+// P^T (bf16) is written into the rope slot (dims 512..575) once QK is done.
+// Slots are released as PV stops needing them and refilled with the next
+// tile (prefetched into L2 one tile ahead), so loads overlap PV.
 //
-// The row blocks of one request form a thread-block cluster (up to
-// MTP_MLA_MAX_CLUSTER CTAs): every K / V stage is fetched from L2 once per
-// cluster with a TMA multicast (the fills are spread round-robin over the
-// CTAs) and released by a multicast tcgen05.commit from each CTA's MMA
-// thread, so L2 requests drop by the cluster size.
+// The row blocks of one request may form a thread-block cluster (up to
+// MTP_MLA_MAX_CLUSTER CTAs): every slot fill is fetched from L2 once per
+// cluster with a TMA multicast (fills spread round-robin over the CTAs) and
+// released by a multicast tcgen05.commit from each CTA's MMA thread.
 //
-// Warps (4 warpgroups): 0 MMA issuer, 1-2 K-ring producers, 3 and 12 V-ring
-// producers, 4..11 softmax / epilogue (warp w owns TMEM lanes 32*(w%4)..+31 =
-// keys of S^T, dv of O^T, and one half of the 64 row columns), 13-15 idle.
-// A single thread serialises its TMA issues, so each ring has two producer
-// warps and each stage's two boxes go out from two lanes; setmaxnreg moves
-// registers from the producer warpgroups to the softmax warpgroups. Row max / sum across keys use a
-// butterfly transpose-reduce over the warp plus a 4-way merge in shared
-// memory. Online softmax with a lazy rescale: the running row max only moves
-// when a tile's max exceeds it by more than 8 (log2 units), then O^T columns
-// and the row sum are rescaled; results are exact either way since P and l use
-// the same reference max.
+// Warps (4 warpgroups): 0 MMA issuer, 1-3 and 13-15 TMA producers (one 8 KB
+// box per issue, so six warps keep many copies in flight), 4..11 softmax /
+// epilogue (warp w owns TMEM lanes 32*(w%4)..+31 = keys of S^T, dv of O^T,
+// and one half of the 64 row columns), 12 idle. setmaxnreg moves registers
+// from warpgroups 0 and 3 to the softmax warpgroups.
+//
+// Online softmax with a lazy rescale: the reference row max only moves when
+// a score exceeds it by more than 8 (log2 units); one barrier reduction tells
+// all softmax warps whether any did, and only then are the tile's row maxima
+// taken (butterfly transpose-reduce over the warp plus a 4-way merge in shared
+// memory) and the O^T columns rescaled. Results are exact either way since P
+// and l use the same reference. Each thread keeps partial row sums over its
+// keys; they are reduced once, after the last tile.
 #include <cuda.h>
 #include <math.h>
 
@@ -58,13 +60,14 @@ constexpr int kRows = 64;             // query rows per CTA (MMA N)
 constexpr int kKeys = 128;            // keys per tile (MMA M of S^T)
 constexpr int kDQ = 576, kDV = 512;
 constexpr int kQChunks = kDQ / 64;    // 9
-constexpr int kStageBytes = 16384;
-constexpr int kKStages = 4;           // ring of K chunks [128 keys x 64 dims]
-constexpr int kVStages = 3;           // ring of V chunks [64 keys x 128 dv]
-constexpr int kSBufs = 3;             // S^T buffers: two QK tiles run ahead of the softmax
-constexpr int kSoftWarps = 8;         // 2 per TMEM lane quarter (row halves)
-constexpr int kThreads = 512;         // 4 warpgroups: [MMA, K, K, V], softmax x 2, [V, idle x 3]
-constexpr int kRegsLight = 64;        // producer / MMA warpgroups after setmaxnreg
+constexpr int kSlotBytes = 16384;     // one [128 keys x 64 dims] chunk of the tile
+constexpr int kSlots = kQChunks;      // the whole tile is resident: slot c = dims 64c .. 64c+63
+constexpr int kPSlot = 8;             // the rope chunk's slot receives P^T once QK is done
+constexpr int kSBufs = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kProducers = 6;         // TMA issuing warps (warps 1-3 and 13-15)         // 2 per TMEM lane quarter (row halves)
+constexpr int kThreads = 512;         // 4 warpgroups: [MMA, producer x 3], softmax x 2, idle
+constexpr int kRegsLight = 64;        // producer / MMA / idle warpgroups after setmaxnreg
 constexpr int kRegsSoftmax = 192;     // softmax warpgroups: 128 * (64 + 192 + 192 + 64) = 65536
 static_assert(128 * (2 * kRegsLight + 2 * kRegsSoftmax) <= 65536, "register split exceeds the launch's file");
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,14 +76,11 @@ constexpr float kLazyRescale = 8.0f;  // log2 units
 constexpr int kMaxCluster = MTP_MLA_MAX_CLUSTER;   // CTAs (row blocks) sharing each KV tile by TMA multicast
 
 constexpr int kQOff = 0;                                    // 9 x 8 KB
-constexpr int kKOff = kQOff + kQChunks * 8192;              // 73728
-constexpr int kVOff = kKOff + kKStages * kStageBytes;
-constexpr int kPOff = kVOff + kVStages * kStageBytes;       // 2 buffers x (2 x 8 KB)
-constexpr int kPBytes = 16384;
-constexpr int kRedOff = kPOff + 2 * kPBytes;                // red_max[4][64], red_sum[4][64]
-constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;           // m_run, l_run, m_ref, scale [64] floats, lim [64] int
-constexpr int kBarOff = kRowOff + 5 * 64 * 4;
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 1 + 2 * kSBufs + 2 + 2 + 1;
+constexpr int kSlotOff = kQOff + kQChunks * 8192;           // 73728
+constexpr int kRedOff = kSlotOff + kSlots * kSlotBytes;     // red_max[4][64], red_sum[4][64]
+constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;           // m_run, l_run, m_ref, scale [64] floats, lim [64] int, shift [64]
+constexpr int kBarOff = kRowOff + 6 * 64 * 4;
+constexpr int kNumBars = 2 * kSlots + 1 + 2 * kSBufs + 1 + 1 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;            // tmem base, abort, rescale flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 
@@ -130,6 +130,27 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 __device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// Named barrier 1 over the 256 softmax threads that also returns whether any
+// of them passed true.
+__device__ __forceinline__ bool softmax_barrier_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 256, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22, far below the
+// bf16 rounding P goes through); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Lane l ends up with op-reduction over the 32 lanes of element l of v[]
@@ -150,20 +171,6 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
   return v[0];
 }
 
-// One ring of TMA stages consumed in order by the MMA thread.
-struct Ring {
-  uint64_t* full;
-  uint64_t* empty;
-  int n, stage;
-  uint32_t phase;
-  __device__ __forceinline__ void advance() {
-    if (++stage == n) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
 __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                   const __grid_constant__ CUtensorMap tm_kv,
                                                                   const Params p) {
@@ -176,19 +183,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   float* m_ref = m_run + 128;
   float* rscale = m_run + 192;
   int* lim = reinterpret_cast<int*>(m_run + 256);
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* kempty = kfull + kKStages;
-  uint64_t* vfull = kempty + kKStages;
-  uint64_t* vempty = vfull + kVStages;
-  uint64_t* qbar = vempty + kVStages;
+  float* m_shift = m_run + 320;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kSlots]: slot c holds this tile's chunk c
+  uint64_t* empty = full + kSlots;                                  // [kSlots]: every cluster CTA is done with it
+  uint64_t* qbar = empty + kSlots;
   uint64_t* s_full = qbar + 1;
   uint64_t* s_empty = s_full + kSBufs;
-  uint64_t* p_full = s_empty + kSBufs;    // [2]: P buffer b written
-  uint64_t* o_done = p_full + 2;          // [2]: PV of the tile using P buffer b done
-  uint64_t* final_bar = o_done + 2;
+  uint64_t* p_full = s_empty + kSBufs;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* final_bar = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
-  volatile int* need_rescale = reinterpret_cast<volatile int*>(smem + kMiscOff + 8);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int split = blockIdx.x, b = blockIdx.y;
@@ -212,26 +217,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      sm100::mbar_init(&kfull[s], 1);
-      sm100::mbar_init(&kempty[s], C);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      sm100::mbar_init(&vfull[s], 1);
-      sm100::mbar_init(&vempty[s], C);
+    for (int c = 0; c < kSlots; ++c) {
+      sm100::mbar_init(&full[c], 2);   // one arrival per box
+      sm100::mbar_init(&empty[c], C);
     }
     sm100::mbar_init(qbar, 1);
     for (int i = 0; i < kSBufs; ++i) {
       sm100::mbar_init(&s_full[i], 1);
       sm100::mbar_init(&s_empty[i], kSoftWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      sm100::mbar_init(&p_full[i], kSoftWarps);
-      sm100::mbar_init(&o_done[i], 1);
-    }
+    sm100::mbar_init(p_full, kSoftWarps);
+    sm100::mbar_init(o_done, 1);
     sm100::mbar_init(final_bar, 1);
     *abort = 0;
-    *need_rescale = 0;
     sm100::fence_barrier_init();
   }
   if (warp == 0) {
@@ -242,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
     const int rr = min(row_base + (int)threadIdx.x, rows - 1);
     lim[threadIdx.x] = ctx + rr / p.Hq;
     m_run[threadIdx.x] = -INFINITY;
+    m_ref[threadIdx.x] = 0.0f;   // reference max the softmax warps start from
     l_run[threadIdx.x] = 0.0f;
   }
   sm100::tc_fence_before();
@@ -250,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   sm100::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = sm100::smem_u32(smem);
+  const uint32_t p_base = smem_base + kSlotOff + kPSlot * kSlotBytes;
 
   auto softmax_role = [&]() {
     // ------------------------------------------------------- softmax warps
@@ -258,66 +258,85 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
     const int ch = sw >> 2;                  // row half: rows 32*ch .. 32*ch+31
     const int st = sw * 32 + lane;           // 0..255
     const uint32_t lane_addr = (uint32_t)(32 * qq) << 16;
+    // Thread (qq, lane) sees key 32*qq + lane of every tile for the 32 rows of
+    // its half. It keeps each row's reference max (the same in every thread
+    // of the half) and its own partial row sums; the sums are reduced over
+    // the keys once, after the last tile.
+    float acc[32];
+#pragma unroll
+    for (int x = 0; x < 32; ++x) acc[x] = 0.0f;
+    const int lim_min = ctx + row_base / p.Hq;   // smallest key limit of the block's rows
     // Every softmax warp runs the same sequence of named barriers for every
     // tile; after an abort the tensor-memory work is skipped but the barrier
     // sequence is kept, so no warp is left waiting on the others.
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int buf = i % kSBufs;
+      // S^T(i) is complete; so is every earlier MMA, PV(i-1) included (the
+      // tile's rope chunk was refilled only after PV(i-1) released its slot).
       ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&s_full[buf], (i / kSBufs) & 1, abort) ? 1 : 0);
-      float s[32];
+      // d = score (log2 units) - reference max of the row.
+      float d[32];
       if (ok) {
         sm100::tc_fence_after();
         uint32_t r[32];
         sm100::tmem_ld_32x32b_x32(tmem + lane_addr + kColS + buf * 64 + ch * 32, r);
         sm100::tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) s[x] = __uint_as_float(r[x]);
+        for (int x = 0; x < 32; ++x) d[x] = fmaf(__uint_as_float(r[x]), p.scale_log2, -m_ref[ch * 32 + x]);
         sm100::tc_fence_before();
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(&s_empty[buf]);
       } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) s[x] = -INFINITY;
+        for (int x = 0; x < 32; ++x) d[x] = -INFINITY;
       }
-      const int key = t0 + i * kKeys + 32 * qq + lane;
+      const int tile0 = t0 + i * kKeys;
+      if (tile0 + kKeys - 1 > lim_min || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
+        const int key = tile0 + 32 * qq + lane;
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const float v = s[x] * p.scale_log2;
-        s[x] = (key > lim[ch * 32 + x] || key >= t_end) ? -INFINITY : v;
+        for (int x = 0; x < 32; ++x) d[x] = (key > lim[ch * 32 + x] || key >= t_end) ? -INFINITY : d[x];
       }
-      {
-        float t[32];
+      // The reference only moves when a score exceeds it by more than
+      // kLazyRescale: then (and on the first tile) the tile's row maxima are
+      // taken and the references updated.
+      bool exceed = (i == 0);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) t[x] = s[x];
-        red_max[qq * 64 + ch * 32 + lane] = transpose_reduce<true>(t, lane);
-      }
-      softmax_barrier();
-      if (st < kRows) {
-        const float mt = fmaxf(fmaxf(red_max[st], red_max[64 + st]), fmaxf(red_max[128 + st], red_max[192 + st]));
-        const float mo = m_run[st];
-        float mn = mo, sc = 1.0f;
-        if (mt > mo + kLazyRescale) {
-          mn = mt;
-          sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
-          if (i > 0 && sc != 1.0f) *need_rescale = 1;
+      for (int x = 0; x < 32; ++x) exceed |= d[x] > kLazyRescale;
+      if (softmax_barrier_any(exceed)) {
+        {
+          float t[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) t[x] = d[x];
+          // max of d over the warp's keys; the reference is the same for all of them
+          red_max[qq * 64 + ch * 32 + lane] = transpose_reduce<true>(t, lane) + m_ref[ch * 32 + lane];
         }
-        m_run[st] = mn;
-        m_ref[st] = mn == -INFINITY ? 0.0f : mn;
-        rscale[st] = sc;
-        l_run[st] *= sc;
-      }
-      softmax_barrier();
+        softmax_barrier();
+        if (st < kRows) {
+          const float mt = fmaxf(fmaxf(red_max[st], red_max[64 + st]), fmaxf(red_max[128 + st], red_max[192 + st]));
+          const float mo = m_run[st];
+          float mn = mo, sc = 1.0f;
+          if (mt > mo + kLazyRescale) {
+            mn = mt;
+            sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+          }
+          m_run[st] = mn;
+          const float ref = mn == -INFINITY ? 0.0f : mn;   // rows with no visible key yet: p = 2^-inf = 0
+          m_shift[st] = m_ref[st] - ref;
+          m_ref[st] = ref;
+          rscale[st] = sc;
+        }
+        softmax_barrier();
+        bool rescale = false;
 #pragma unroll
-      for (int x = 0; x < 32; ++x) s[x] = exp2f(s[x] - m_ref[ch * 32 + x]);   // s now holds p
-      // P buffer i%2 is free once PV(i-2) is done; rescaling O^T needs every
-      // earlier PV done (completions are in issue order, so PV(i-1) suffices).
-      if (i >= 2 && !*need_rescale)
-        ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&o_done[i & 1], ((i >> 1) - 1) & 1, abort) ? 1 : 0);
-      if (i >= 1 && *need_rescale) {
-        ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&o_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort) ? 1 : 0);
-        if (ok) {
-          sm100::tc_fence_after();
+        for (int x = 0; x < 32; ++x) {
+          const float sc = rscale[ch * 32 + x];
+          rescale |= sc != 1.0f;
+          acc[x] *= sc;
+          d[x] += m_shift[ch * 32 + x];
+        }
+        // O^T columns of these rows hold PV up to tile i-1 (complete): rescale them.
+        if (ok && i > 0 && rescale) {
 #pragma unroll 1
           for (int dc = 0; dc < 4; ++dc) {
             uint32_t r[32];
@@ -331,35 +350,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
           tmem_st_wait();
         }
       }
-      // P^T (bf16) into the K-major B tile: block of 64 keys, row, key.
+      // p = 2^d: P^T (bf16) into the rope slot as a K-major B tile (block of
+      // 64 keys, row, key), and into this thread's partial row sums.
       {
         const int k = 32 * qq + lane;
-        uint8_t* pb = smem + kPOff + (i & 1) * kPBytes + (k >> 6) * 8192;
+        uint8_t* pb = smem + kSlotOff + kPSlot * kSlotBytes + (k >> 6) * 8192;
         const int kin = k & 63;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
+          const float pv = fast_exp2(d[x]);
+          acc[x] += pv;
           const int r = ch * 32 + x;
           *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kin >> 3) ^ (r & 7))) << 4) + (kin & 7) * 2) =
-              __float2bfloat16_rn(s[x]);
+              __float2bfloat16_rn(pv);
         }
       }
-      red_sum[qq * 64 + ch * 32 + lane] = transpose_reduce<false>(s, lane);
       fence_async_smem();
       sm100::tc_fence_before();
-      softmax_barrier();
-      if (st < kRows) l_run[st] += red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
-      if (st == 0) *need_rescale = 0;
       __syncwarp();
-      if (lane == 0 && ok) sm100::mbar_arrive(&p_full[i & 1]);
+      if (lane == 0 && ok) sm100::mbar_arrive(p_full);
     }
     if (!ok && lane == 0) {
       *abort = 1;
       raise_error(p.err, MTP_ERR_TIMEOUT);
     }
+    // Row sums: over the warp's 32 keys, then over the 4 lane quarters.
+    red_sum[qq * 64 + ch * 32 + lane] = transpose_reduce<false>(acc, lane);
+    softmax_barrier();
+    if (st < kRows) l_run[st] = red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
     // -------------------------------------------------------- epilogue
-    const bool done =
-        ok && __all_sync(0xffffffffu,
-                         sm100::mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort) ? 1 : 0);
+    const bool done = ok && __all_sync(0xffffffffu, sm100::mbar_wait(o_done, (n_tiles - 1) & 1, abort) ? 1 : 0);
     softmax_barrier();
     if (done) {
       sm100::tc_fence_after();
@@ -388,27 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         p.part_lse[orow * p.n_splits + split] = l > 0.0f ? (m_run[st] + log2f(l)) * kLn2 : -INFINITY;
       }
     }
-    };
+  };
 
   // Warp roles. Warpgroups 0 and 3 hand registers to the softmax warpgroups
   // (every warp of a warpgroup runs the same setmaxnreg).
   const int wg = warp / 4;
-  const int k_prod = (warp == 1 || warp == 2) ? warp - 1 : -1;    // two K-ring producers
-  const int v_prod = warp == 3 ? 0 : (warp == 12 ? 1 : -1);       // two V-ring producers
   if (wg == 1 || wg == 2) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     softmax_role();
   } else {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
-  if (k_prod >= 0 || v_prod >= 0) {
-    // ------------------------------------------- TMA producers (K ring / V ring)
-    // Fills alternate between the two producers of a ring; lanes 0 and 1 of a
-    // producer issue the stage's two boxes together.
-    if (lane < 2) {
-      const bool is_k = k_prod >= 0;
-      const int pidx = is_k ? k_prod : v_prod;
-      const uint64_t pol_kv = sm100::l2_policy_evict_last();   // the V pass and the other row blocks re-read it
-      if (is_k && pidx == 0 && lane == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
+    const int pw = warp <= 3 ? warp - 1 : (warp >= 13 ? warp - 10 : -1);   // producer 0..5, or -1
+    if (pw >= 0 && lane == 0) {
+      // ------------------------------------------------------ TMA producers
+      // A tile is 18 boxes of [64 keys x 64 dims] (8 KB): box x = slot x/2,
+      // keys 64*(x%2).. of the tile. Producer pw owns boxes pw, pw+6, pw+12
+      // (slots in the order the MMA consumes them) and refills a box as soon
+      // as every cluster CTA released its slot from the previous tile. Each
+      // box issue is followed by an L2 prefetch of the same box of the next
+      // tile, so that the refill after the release hits L2.
+      const uint64_t pol_kv = sm100::l2_policy_evict_last();   // the cluster's other row blocks re-read it
+      if (pw == 0) {
         sm100::tma_prefetch_desc(&tm_q);
         sm100::tma_prefetch_desc(&tm_kv);
         sm100::mbar_arrive_expect_tx(qbar, kQChunks * 8192);
@@ -421,73 +441,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         if (key0 >= t_end) return -1;
         const int blk = tbl[key0 / kBlock];
         if (blk < 0 || blk >= p.num_blocks) {
-          if (is_k) raise_error(p.err, MTP_ERR_BLOCK_ID);
+          raise_error(p.err, MTP_ERR_BLOCK_ID);
           return -1;
         }
         return blk;
       };
-      uint64_t* fullb = is_k ? kfull : vfull;
-      uint64_t* emptyb = is_k ? kempty : vempty;
-      const int nst = is_k ? kKStages : kVStages;
-      uint8_t* base = smem + (is_k ? kKOff : kVOff);
-      const int nchunks = is_k ? kQChunks : 8;
       bool ok = true;
-      for (int seq = pidx; seq < n_tiles * nchunks && ok; seq += 2) {
-        const int i = seq / nchunks, c = seq % nchunks;
-        const int stage = seq % nst;
-        const uint32_t phase = (uint32_t)((seq / nst) & 1);
-        const int key0 = t0 + i * kKeys;
-        // Empty once every CTA of the cluster consumed the previous fill.
-        if (lane == 0) ok = sm100::mbar_wait(&emptyb[stage], phase ^ 1u, abort);
-        ok = __shfl_sync(0x3u, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        uint8_t* dst = base + stage * kStageBytes;
-        uint64_t* bar = &fullb[stage];
-        if (lane == 0) sm100::mbar_arrive_expect_tx(bar, kStageBytes);
-        __syncwarp(0x3u);
-        if (seq % C == (int)rank) {
-          int x, z;
-          if (is_k) {          // [128 keys x 64 dims]: lane 0 keys 0..63, lane 1 keys 64..127
-            x = c * 64;
-            z = block_of(key0 + lane * 64);
-          } else {             // [64 keys x 128 dv] for key half c / 4, dv chunk c % 4
-            x = (c & 3) * 128 + lane * 64;
-            z = block_of(key0 + (c >> 2) * 64);
+      for (int i = 0; i < n_tiles && ok; ++i) {
+#pragma unroll 1
+        for (int x = pw; x < 2 * kSlots; x += kProducers) {
+          const int c = x >> 1, half = x & 1;
+          ok = sm100::mbar_wait(&empty[c], (uint32_t)((i & 1) ^ 1), abort);
+          if (!ok) break;
+          sm100::mbar_arrive_expect_tx(&full[c], kSlotBytes / 2);
+          if ((i * 2 * kSlots + x) % C == (int)rank) {
+            const int blk = block_of(t0 + i * kKeys + half * 64);
+            uint8_t* dst = smem + kSlotOff + c * kSlotBytes + half * (kSlotBytes / 2);
+            if (C > 1) sm100::tma_load_3d_mc(dst, &tm_kv, &full[c], c * 64, 0, blk, peers, pol_kv);
+            else sm100::tma_load_3d(dst, &tm_kv, &full[c], c * 64, 0, blk, pol_kv);
+            if (i + 1 < n_tiles) {
+              const int nblk = block_of(t0 + (i + 1) * kKeys + half * 64);
+              if (nblk >= 0) sm100::tma_prefetch_3d(&tm_kv, c * 64, 0, nblk);
+            }
           }
-          if (C > 1) sm100::tma_load_3d_mc(dst + lane * 8192, &tm_kv, bar, x, 0, z, peers, pol_kv);
-          else sm100::tma_load_3d(dst + lane * 8192, &tm_kv, bar, x, 0, z, pol_kv);
         }
       }
-      if (!ok && lane == 0) {
+      if (!ok) {
         *abort = 1;
         raise_error(p.err, MTP_ERR_TIMEOUT);
       }
-      // Every copy must land before the CTA may exit: wait (time-limited) for
-      // the latest fill of each stage (it completes after all earlier ones);
-      // the producer that made that fill waits for it.
-      if (lane == 0) {
-        if (is_k && pidx == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
-        const int total = n_tiles * nchunks;
-        for (int st2 = 0; st2 < nst && st2 < total; ++st2) {
-          const int last = st2 + ((total - 1 - st2) / nst) * nst;
-          if (last % 2 != pidx) continue;
-          sm100::mbar_wait_timeout(&fullb[st2], (uint32_t)((last / nst) & 1), sm100::kWaitTimeoutNs);
-        }
-      }
-    }
-  } else if (warp == 0) {
-    // ---------------------------------------------------------------- MMA
-    // Order: QK of two tiles ahead, then PV of the oldest tile. A consumed
-    // ring stage is released to every CTA of the cluster (multicast commit).
-    if (lane == 0) {
+      // Every copy must land before the CTA may exit: wait (time-limited)
+      // for the last fill of each slot this producer fed.
+      if (pw == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
+      for (int x = pw; x < 2 * kSlots; x += kProducers)
+        sm100::mbar_wait_timeout(&full[x >> 1], (uint32_t)((n_tiles - 1) & 1), sm100::kWaitTimeoutNs);
+    } else if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      // QK(i) over the 9 resident chunks, then (once P(i) is published) PV(i)
+      // reading V^T MN-major from chunk slots 2dc, 2dc+1 and P^T from the rope
+      // slot; each slot is released to every cluster CTA as soon as PV(i) no
+      // longer needs it, so tile i+1 loads overlap PV(i). Descriptors are
+      // formed once and advanced by constants (16-byte units in the start
+      // address field): the issue loop must stay far below one MMA's time.
       constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, kRows);
       constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, kRows) | (1u << 15);   // A (V^T) MN-major
-      Ring kr{kfull, kempty, kKStages, 0, 0u};
-      Ring vr{vfull, vempty, kVStages, 0, 0u};
-      auto release = [&](Ring& r) {
-        if (C > 1) sm100::tc_commit_mc(&r.empty[r.stage], peers);
-        else sm100::tc_commit(&r.empty[r.stage]);
-        r.advance();
+      const uint64_t d_slot = desc_kmajor(smem_base + kSlotOff);
+      const uint64_t d_q = desc_kmajor(smem_base + kQOff);
+      const uint64_t d_vt = desc_mnmajor(smem_base + kSlotOff, kSlotBytes);
+      const uint64_t d_p = desc_kmajor(p_base);
+      auto release = [&](int c) {
+        if (C > 1) sm100::tc_commit_mc(&empty[c], peers);
+        else sm100::tc_commit(&empty[c]);
       };
       bool ok = sm100::mbar_wait(qbar, 0, abort);
       auto issue_qk = [&](int i) -> bool {
@@ -495,42 +499,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         if (!sm100::mbar_wait(&s_empty[buf], ((i / kSBufs) & 1) ^ 1u, abort)) return false;
         sm100::tc_fence_after();
         const uint32_t d = tmem + kColS + buf * 64;
-        for (int c = 0; c < kQChunks; ++c) {
-          if (!sm100::mbar_wait(&kr.full[kr.stage], kr.phase, abort)) return false;
+#pragma unroll 1
+        for (int c = 0; c < kSlots; ++c) {
+          if (!sm100::mbar_wait(&full[c], (uint32_t)(i & 1), abort)) return false;
           sm100::tc_fence_after();
-          const uint32_t a = smem_base + kKOff + kr.stage * kStageBytes;
-          const uint32_t qa = smem_base + kQOff + c * 8192;
+          const uint64_t a = d_slot + (uint64_t)(c * (kSlotBytes >> 4));
+          const uint64_t q = d_q + (uint64_t)(c * (8192 >> 4));
+          sm100::tc_mma_bf16(d, a, q, idesc_qk, c > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            sm100::tc_mma_bf16(d, desc_kmajor(a + kk * 32), desc_kmajor(qa + kk * 32), idesc_qk,
-                               (c > 0 || kk > 0) ? 1u : 0u);
-          release(kr);
+          for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16(d, a + 2 * kk, q + 2 * kk, idesc_qk, 1u);
         }
         sm100::tc_commit(&s_full[buf]);
         return true;
       };
       auto issue_pv = [&](int i) -> bool {
-        if (!sm100::mbar_wait(&p_full[i & 1], (i >> 1) & 1, abort)) return false;
+        if (!sm100::mbar_wait(p_full, (uint32_t)(i & 1), abort)) return false;
         sm100::tc_fence_after();
-        for (int c = 0; c < 8; ++c) {
-          const int kh = c >> 2, dc = c & 3;
-          if (!sm100::mbar_wait(&vr.full[vr.stage], vr.phase, abort)) return false;
-          sm100::tc_fence_after();
-          const uint32_t a = smem_base + kVOff + vr.stage * kStageBytes;
-          const uint32_t pb = smem_base + kPOff + (i & 1) * kPBytes + kh * 8192;
+        const uint32_t first = i > 0 ? 1u : 0u;
+#pragma unroll 1
+        for (int dc = 0; dc < 4; ++dc) {
+          const uint64_t a = d_vt + (uint64_t)(2 * dc * (kSlotBytes >> 4));
+          const uint32_t d = tmem + kColO + dc * 64;
+          sm100::tc_mma_bf16(d, a, d_p, idesc_pv, first);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            sm100::tc_mma_bf16(tmem + kColO + dc * 64, desc_mnmajor(a + kk * 2048, 8192), desc_kmajor(pb + kk * 32),
-                               idesc_pv, (i > 0 || kh > 0 || kk > 0) ? 1u : 0u);
-          release(vr);
+          for (int kk = 1; kk < 8; ++kk)
+            sm100::tc_mma_bf16(d, a + (uint64_t)(kk * (2048 >> 4)),
+                               d_p + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_pv, 1u);
+          release(2 * dc);
+          release(2 * dc + 1);
         }
-        sm100::tc_commit(&o_done[i & 1]);
+        release(kPSlot);
+        sm100::tc_commit(o_done);
         return true;
       };
-      for (int i = 0; i < kSBufs - 1 && i < n_tiles && ok; ++i) ok = issue_qk(i);
+      if (ok) ok = issue_qk(0);
       for (int i = 0; i < n_tiles && ok; ++i) {
-        if (i + kSBufs - 1 < n_tiles) ok = issue_qk(i + kSBufs - 1);
-        if (ok) ok = issue_pv(i);
+        ok = issue_pv(i);
+        if (ok && i + 1 < n_tiles) ok = issue_qk(i + 1);
       }
       if (!ok) {
         *abort = 1;
@@ -539,7 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       sm100::tc_commit(final_bar);
       sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
     }
-  }
   }
   sm100::tc_fence_before();
   __syncthreads();
