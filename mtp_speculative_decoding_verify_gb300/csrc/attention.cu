@@ -103,6 +103,10 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
     p.ws_bytes = p.ws_partial_lse + rows * p.n_splits * sizeof(float);
     p.ws_bytes = (p.ws_bytes + 255) / 256 * 256;
   }
+  if (attention_uses_mla_tc(a)) {   // one int per (split, request, row block) at most
+    p.ws_order = p.ws_bytes;
+    p.ws_bytes += ((size_t)p.n_splits * a.B * row_tiles * sizeof(int32_t) + 255) / 256 * 256;
+  }
   return p;
 }
 

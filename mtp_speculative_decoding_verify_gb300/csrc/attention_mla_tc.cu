@@ -94,8 +94,10 @@ struct Params {
   float* part_lse;
   const int32_t* block_table;
   const int32_t* ctx_lens;
+  const int32_t* order;   // work items, longest first (mla_schedule_kernel)
   unsigned* err;
-  int R, Hq, max_blocks, num_blocks, split_len, n_splits;
+  int B, R, Hq, max_blocks, num_blocks, split_len, n_splits;
+  int groups;           // row-block clusters per request
   int cluster;          // CTAs per cluster (row blocks of one request sharing each KV tile by multicast)
   float scale_log2;
 };
@@ -171,6 +173,61 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
   return v[0];
 }
 
+// A work item is (split, request, cluster g of C row blocks): item index
+// i = (split * B + b) * groups + g. Every CTA of the cluster walks the keys
+// [t0, t_end) visible to the cluster's last row.
+struct Item {
+  int split, b, g;
+};
+
+__device__ __forceinline__ Item decode_item(int i, int B, int groups) {
+  Item it;
+  it.g = i % groups;
+  it.b = (i / groups) % B;
+  it.split = i / (groups * B);
+  return it;
+}
+
+__device__ __forceinline__ int item_key_end(const Item& it, int ctx, int R, int Hq, int rows, int C, int split_len) {
+  const int cluster_rows_end = min((it.g + 1) * C * kRows, rows);
+  const int j_max = min(R - 1, (cluster_rows_end - 1) / Hq);
+  return min(it.split * split_len + split_len, ctx + j_max + 1);
+}
+
+constexpr int kMaxItemTiles = 64;   // split_len <= 4096 keys = 32 tiles
+
+// Orders the work items by tile count, longest first (counting sort, one
+// CTA). Clusters are dispatched in index order, so long items start first
+// and short ones fill the tail.
+__global__ void __launch_bounds__(1024) mla_schedule_kernel(const int32_t* __restrict__ ctx_lens, int B, int R, int Hq,
+                                                           int C, int groups, int split_len, int n_splits,
+                                                           int max_len, int32_t* __restrict__ order) {
+  __shared__ int hist[kMaxItemTiles + 1];
+  const int rows = R * Hq, n = n_splits * B * groups;
+  auto tiles_of = [&](int i) -> int {
+    const Item it = decode_item(i, B, groups);
+    const int ctx = ctx_lens[it.b];
+    if (ctx < 0 || ctx + R > max_len) return 0;   // rejected by the attention kernel itself
+    const int t0 = it.split * split_len;
+    const int t_end = item_key_end(it, ctx, R, Hq, rows, C, split_len);
+    return t0 < t_end ? min((t_end - t0 + kKeys - 1) / kKeys, kMaxItemTiles) : 0;
+  };
+  for (int k = threadIdx.x; k <= kMaxItemTiles; k += blockDim.x) hist[k] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[tiles_of(i)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {   // hist[k] becomes the first position of tile count k
+    int acc = 0;
+    for (int k = kMaxItemTiles; k >= 0; --k) {
+      const int h = hist[k];
+      hist[k] = acc;
+      acc += h;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) order[atomicAdd(&hist[tiles_of(i)], 1)] = i;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                   const __grid_constant__ CUtensorMap tm_kv,
                                                                   const Params p) {
@@ -196,23 +253,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int split = blockIdx.x, b = blockIdx.y;
-  const int rows = p.R * p.Hq;
-  const int row_base = blockIdx.z * kRows;
   const int C = p.cluster;
   const uint32_t rank = C > 1 ? sm100::cluster_ctarank() : 0u;
+  const Item item = decode_item(p.order[blockIdx.x / C], p.B, p.groups);
+  const int split = item.split, b = item.b;
+  const int rows = p.R * p.Hq;
+  const int row_base = (item.g * C + (int)rank) * kRows;
   const uint16_t peers = (uint16_t)((1u << C) - 1u);
   const int ctx = p.ctx_lens[b];
   if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {   // uniform over the cluster (same request)
-    if (threadIdx.x == 0 && split == 0 && blockIdx.z == 0) raise_error(p.err, MTP_ERR_LENGTH);
+    if (threadIdx.x == 0 && split == 0 && row_base == 0) raise_error(p.err, MTP_ERR_LENGTH);
     return;
   }
   // Every CTA of a cluster walks the same keys (those visible to the cluster's
   // last row); rows that see fewer keys mask the rest.
-  const int cluster_rows_end = min((int)(blockIdx.z / C + 1) * C * kRows, rows);
-  const int j_max = min(p.R - 1, (cluster_rows_end - 1) / p.Hq);
   const int t0 = split * p.split_len;
-  const int t_end = min(t0 + p.split_len, ctx + j_max + 1);
+  const int t_end = item_key_end(item, ctx, p.R, p.Hq, rows, C, p.split_len);
   if (t0 >= t_end) return;  // no key of this split is visible to these rows: the combine skips it
   const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
 
@@ -581,7 +637,9 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   p.part_lse = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_lse) : nullptr;
   p.block_table = a.block_table;
   p.ctx_lens = a.ctx_lens;
+  p.order = (const int32_t*)((const char*)a.workspace + pl.ws_order);
   p.err = err;
+  p.B = a.B;
   p.R = R;
   p.Hq = a.Hq;
   p.max_blocks = a.max_blocks;
@@ -593,18 +651,24 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   int C = kMaxCluster;
   while (row_blocks % C) --C;   // cluster = row blocks of one request, at most kMaxCluster
   p.cluster = C;
-  cudaError_t e = cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  p.groups = row_blocks / C;
+  const int n_items = pl.n_splits * a.B * p.groups;
+  mla_schedule_kernel<<<1, 1024, 0, s>>>(a.ctx_lens, a.B, R, a.Hq, C, p.groups, pl.split_len, pl.n_splits,
+                                         a.max_blocks * kBlock, (int32_t*)((char*)a.workspace + pl.ws_order));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.n_splits, a.B, row_blocks);
+  cfg.gridDim = dim3(n_items * C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = C;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tq, tkv, p);

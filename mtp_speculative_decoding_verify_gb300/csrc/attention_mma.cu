@@ -363,6 +363,8 @@ cudaError_t launch_attention_mma(const mtp_attn_args& a, const AttnPlan& p, unsi
   return a.d_qk == 128 ? run_gqa<128>(a, p, err, s) : run_gqa<64>(a, p, err, s);
 }
 
+bool attention_uses_mla_tc(const mtp_attn_args& a) { return a.is_mla && attention_mma_supported(a); }
+
 cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s) {
   return launch_attention_mla_tc(a, p, err, s);
 }

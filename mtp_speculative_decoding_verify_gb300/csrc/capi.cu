@@ -220,14 +220,14 @@ int mtp_verify_attention(const mtp_attn_args* a, void* stream) {
   cudaError_t e = mtp::launch_kv_append(*a, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "kv append launch");
   if ((e = record(a->timing_events[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-  if (a->dtype == MTP_BF16 && a->is_mla && mtp::attention_mma_supported(*a)) e = mtp::launch_attention_mla(*a, p, c->err, s);
+  if (mtp::attention_uses_mla_tc(*a)) e = mtp::launch_attention_mla(*a, p, c->err, s);
   else if (a->dtype == MTP_BF16 && mtp::attention_mma_supported(*a)) e = mtp::launch_attention_mma(*a, p, c->err, s);
   else e = mtp::launch_attention_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_attention_combine(*a, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention combine launch");
-  g_launches = 2 + (p.n_splits > 1 ? 1 : 0);
+  g_launches = 2 + (p.n_splits > 1 ? 1 : 0) + (mtp::attention_uses_mla_tc(*a) ? 1 : 0);
   return MTP_OK;
 }
 

@@ -17,6 +17,7 @@ struct AttnPlan {
   int split_len;       // keys per split (multiple of 64)
   size_t ws_partial_o; // byte offset of the split partial outputs in the workspace
   size_t ws_partial_lse;
+  size_t ws_order;     // MLA tensor-core path: work-item order (int32 per item)
   size_t ws_bytes;
 };
 
@@ -26,6 +27,7 @@ cudaError_t launch_attention_simt(const mtp_attn_args& a, const AttnPlan& p, uns
 cudaError_t launch_attention_mma(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
+bool attention_uses_mla_tc(const mtp_attn_args& a);
 cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ LM head
