@@ -36,10 +36,6 @@ struct Decision {
   int pad;
 };
 
-struct RacePair {
-  Race resid;  // race on max(0, p - q) (or p for the bonus row)
-  Race plain;  // race on p, the fallback when every residual weight is zero
-};
 }  // namespace
 
 // One CTA per request: reduce the R rows' partials, then warp 0 takes the
@@ -108,13 +104,29 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
   tie_flags[b] = (uint8_t)tie;
 }
 
+// Block-wide merge of one race per thread; the result is valid in thread 0.
+__device__ __forceinline__ Race block_race_merge(Race r, Race* s_part) {
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  r = warp_race_merge(r);
+  __syncthreads();   // s_part may still be read from an earlier merge
+  if (lane == 0) s_part[warp] = r;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int w = 1; w < kWarps; ++w) r = race_merge(r, s_part[w]);
+  return r;
+}
+
 // Grid (B, race_slices): each CTA races one vocabulary slice of the row that
-// needs a draw; the last CTA of a request to finish merges the slices.
+// needs a draw, on the residual weights max(0, p - q) (p itself for the
+// bonus row); only entries with positive weight draw their exponential. The
+// last CTA of a request to finish merges the slices. If no entry of the row
+// has positive weight (p = q everywhere) that CTA races the whole row on p.
 __global__ void __launch_bounds__(kThreads) accept_race_kernel(
     const float* __restrict__ samp_logits, const float* __restrict__ q_draft, const float* __restrict__ ws_lse,
-    const Decision* __restrict__ dec, RacePair* __restrict__ parts, int* __restrict__ race_count, uint64_t seed,
+    const Decision* __restrict__ dec, Race* __restrict__ parts, int* __restrict__ race_count, uint64_t seed,
     int D, int V, int32_t* __restrict__ out_tokens, uint8_t* __restrict__ tie_flags) {
-  __shared__ RacePair s_part[kWarps];
+  __shared__ Race s_part[kWarps];
+  __shared__ Race s_win;
   __shared__ int s_last;
   const int b = blockIdx.x;
   const int nsl = gridDim.y, sl_id = blockIdx.y;
@@ -131,44 +143,39 @@ __global__ void __launch_bounds__(kThreads) accept_race_kernel(
   const int v0 = sl_id * per;
   const int v1 = min(V, v0 + per);
 
-  Race resid = race_empty(), plain = race_empty();
+  Race resid = race_empty();
   for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
     const float p = expf(lrow[v] - lse);
-    const float qv = qrow ? qrow[v] : 0.0f;
-    const float r = p - qv;
-    const float w = r > 0.0f ? r : 0.0f;
-    const float E = race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag);
-    if (w > 0.0f) race_add(resid, w / E, v);
-    if (p > 0.0f) race_add(plain, p / E, v);
+    const float w = p - (qrow ? qrow[v] : 0.0f);
+    if (w > 0.0f) race_add(resid, w / race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag), v);
   }
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  resid = warp_race_merge(resid);
-  plain = warp_race_merge(plain);
-  if (lane == 0) s_part[warp] = RacePair{resid, plain};
-  __syncthreads();
+  resid = block_race_merge(resid, s_part);
   if (threadIdx.x == 0) {
-    RacePair acc = s_part[0];
-    for (int w = 1; w < kWarps; ++w) {
-      acc.resid = race_merge(acc.resid, s_part[w].resid);
-      acc.plain = race_merge(acc.plain, s_part[w].plain);
-    }
-    parts[(int64_t)b * nsl + sl_id] = acc;
+    parts[(int64_t)b * nsl + sl_id] = resid;
     __threadfence();
     const int done = atomicAdd(&race_count[b], 1);
     s_last = (done == nsl - 1);
   }
   __syncthreads();
-  if (!s_last || threadIdx.x != 0) return;
-  __threadfence();
-  const volatile RacePair* vp = parts + (int64_t)b * nsl;
-  Race r1 = race_empty(), r2 = race_empty();
-  for (int sl = 0; sl < nsl; ++sl) {
-    Race a{vp[sl].resid.k1, vp[sl].resid.i1, vp[sl].resid.k2};
-    Race c{vp[sl].plain.k1, vp[sl].plain.i1, vp[sl].plain.k2};
-    r1 = race_merge(r1, a);
-    r2 = race_merge(r2, c);
+  if (!s_last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const volatile Race* vp = parts + (int64_t)b * nsl;
+    Race acc = race_empty();
+    for (int sl = 0; sl < nsl; ++sl) acc = race_merge(acc, Race{vp[sl].k1, vp[sl].i1, vp[sl].k2});
+    s_win = acc;
   }
-  const Race win = r1.i1 >= 0 ? r1 : r2;
+  __syncthreads();
+  Race win = s_win;
+  if (win.i1 < 0) {   // every residual weight is zero: the draw falls back to p
+    Race plain = race_empty();
+    for (int v = threadIdx.x; v < V; v += kThreads) {
+      const float p = expf(lrow[v] - lse);
+      if (p > 0.0f) race_add(plain, p / race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag), v);
+    }
+    win = block_race_merge(plain, s_part);
+  }
+  if (threadIdx.x != 0) return;
   out_tokens[row] = win.i1;
   if (race_near_tie(win)) tie_flags[b] = (uint8_t)(tie_flags[b] | 2);
 }
@@ -187,7 +194,7 @@ cudaError_t launch_accept(const mtp_lmhead_args& a, const LmPlan& p, unsigned* e
   dim3 grid(a.B, p.race_slices);
   accept_race_kernel<<<grid, kThreads, 0, s>>>((const float*)(ws + p.off_logits), a.q_draft,
                                                (const float*)(ws + p.off_lse), (const Decision*)(ws + p.off_dec),
-                                               (RacePair*)(ws + p.off_race), (int*)(ws + p.off_count), a.seed, a.D,
+                                               (Race*)(ws + p.off_race), (int*)(ws + p.off_count), a.seed, a.D,
                                                a.V, a.out_tokens, a.tie_flags);
   return cudaGetLastError();
 }
@@ -211,6 +218,6 @@ cudaError_t launch_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag
 }
 
 size_t accept_decision_bytes() { return sizeof(Decision); }
-size_t accept_race_part_bytes() { return sizeof(RacePair); }
+size_t accept_race_part_bytes() { return sizeof(Race); }
 
 }  // namespace mtp

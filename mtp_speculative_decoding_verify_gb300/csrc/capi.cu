@@ -146,7 +146,8 @@ mtp::LmPlan mtp::plan_lmhead(const mtp_lmhead_args& a, int sm_count) {
   p.M = a.B * R;
   p.tc = mtp::lmhead_tc_supported(a) ? 1 : 0;
   p.slices = p.tc ? mtp::lmhead_tc_slices(a.V, p.M, sm_count) : mtp::lmhead_simt_slices(a.V, sm_count);
-  p.race_slices = std::max(1, std::min(64, (2 * sm_count + a.B - 1) / std::max(a.B, 1)));
+  // race grid: about 8 CTAs per SM over the batch (requests that need no draw exit at once)
+  p.race_slices = std::max(1, std::min(64, (8 * sm_count + a.B - 1) / std::max(a.B, 1)));
   p.race_slices = std::min(p.race_slices, std::max(1, a.V / 1024));
   size_t off = 0;
   const size_t part = align256((size_t)p.slices * p.M * 4);

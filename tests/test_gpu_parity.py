@@ -198,6 +198,21 @@ def test_edge_cases(name):
     _check_rollback(w, att, gpu["num_accepted"])
 
 
+@pytest.mark.parametrize("V", [7, 3001])
+def test_residual_fallback_race(V):
+    """q_draft = 1 everywhere (an input the ABI accepts): drafts are rejected
+    and every residual weight max(0, p - q) is zero, so the draw falls back to
+    p itself; the multi-slice race and the oracle must agree."""
+    w = synth.CFG0.with_(name="fallback race V=%d" % V, V=V, H=64, sampling="all", B=12, dtype="bf16")
+    lm = synth.make_lmhead_inputs(w, DEV)
+    lm["q_draft"].fill_(1.0)
+    gpu = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    assert (gpu["num_accepted"].cpu().numpy() < w.D).any()
+    _full_check_lm(w, lm, gpu, range(w.B), logits=True)
+    check_invariants(w, lm, gpu)
+
+
 def test_rng_streams_bit_exact():
     n = 1 << 20
     for seed, b, j, tag in ((0, 0, 0, 2), (0x1234_5678_9ABC, 77, 5, 3)):
