@@ -71,10 +71,11 @@ struct SmemLayout {
   int a_off, b_off, stage_bytes, bar_off, misc_off, epi_off, rows_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
+// pair: the CTA holds half of the group's N rows of hidden (CTA-pair MMA).
+__host__ __device__ inline SmemLayout smem_layout(int N, int stages, bool pair) {
   SmemLayout L;
   const int a_bytes = kTileV * kTileK * 2;       // 16 KB
-  const int b_bytes = N * kTileK * 2;            // N x 128 B
+  const int b_bytes = (pair ? N / 2 : N) * kTileK * 2;   // rows x 128 B
   L.stage_bytes = a_bytes + b_bytes;
   L.a_off = 0;                                   // stage s: A at s*stage_bytes, B right after A
   L.b_off = a_bytes;
@@ -97,14 +98,20 @@ __device__ __forceinline__ void abort_all(volatile int* abort, unsigned* err) {
   raise_error(err, MTP_ERR_TIMEOUT);
 }
 
-template <int NCH>
+// kPair: CTA pairs (clusters of 2) share each MMA: a pair covers 256 vocab
+// rows per tile (128 per CTA, its A half) and each CTA stages half of the
+// group's hidden rows (its B half), so each SM streams half of the hidden
+// tile through shared memory. The even CTA issues the MMAs; both CTAs' loads
+// of a stage complete on the even CTA's full barrier.
+template <int NCH, bool kPair>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                      const TcParams p) {
   constexpr int N = NCH * 32;
+  constexpr int kBRows = kPair ? N / 2 : N;      // hidden rows staged by this CTA
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemLayout L = smem_layout(N, p.stages);
+  const SmemLayout L = smem_layout(N, p.stages, kPair);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* acc_full = empty + p.stages;
@@ -119,9 +126,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int group = blockIdx.x / p.cpg;
-  const int cta_in_group = blockIdx.x % p.cpg;
+  const int cta_in_group = blockIdx.x % p.cpg;   // also the partial-statistics slice of this CTA
   const int row0 = group * N;
   const int k_steps = p.H / kTileK;
+  const uint32_t rank = kPair ? sm100::cluster_ctarank() : 0u;   // == cta_in_group % 2 (cpg is even)
+  const bool leader = rank == 0;
+  // Vocabulary units: 128 rows (one CTA) or 256 rows (a pair, 128 per CTA).
+  constexpr int kUnit = kPair ? 2 * kTileV : kTileV;
+  const int slot = kPair ? cta_in_group / 2 : cta_in_group;
+  const int nslots = kPair ? p.cpg / 2 : p.cpg;
+  const int n_units = (p.V + kUnit - 1) / kUnit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -130,7 +144,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     for (int b = 0; b < 2; ++b) {
       sm100::mbar_init(&acc_full[b], 1);
-      sm100::mbar_init(&acc_empty[b], 4);
+      sm100::mbar_init(&acc_empty[b], kPair ? 8 : 4);   // epilogue warps of both CTAs drain it
     }
     sm100::mbar_init(final_bar, 1);
     *abort = 0;
@@ -139,8 +153,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     sm100::tma_prefetch_desc(&tm_h);
   }
   if (warp == 1) {
-    sm100::tmem_alloc(tmem_base_slot, p.tmem_cols);
-    sm100::tmem_relinquish();
+    if (kPair) {
+      sm100::tmem_alloc_pair(tmem_base_slot, p.tmem_cols);
+      sm100::tmem_relinquish_pair();
+    } else {
+      sm100::tmem_alloc(tmem_base_slot, p.tmem_cols);
+      sm100::tmem_relinquish();
+    }
   }
   // Per-row information of this CTA's row group.
   for (int r = threadIdx.x; r < N; r += kThreadsTc) {
@@ -161,11 +180,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   sm100::tc_fence_before();
   __syncthreads();
+  if (kPair) sm100::cluster_sync();   // the peer's barriers and TMEM exist before any remote arrive or MMA
   sm100::tc_fence_after();
   const uint32_t tmem_base = *tmem_base_slot;
 
-  // Tiles of this CTA: t = cta_in_group + i * cpg.
-  const int my_tiles = cta_in_group < p.n_tiles ? (p.n_tiles - 1 - cta_in_group) / p.cpg + 1 : 0;
+  // Units of this CTA (pair): u = slot + i * nslots; its vocabulary rows
+  // start at u * kUnit + rank * 128.
+  const int my_tiles = slot < n_units ? (n_units - 1 - slot) / nslots + 1 : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -177,17 +198,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       int issued = 0;
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
-        const int v0 = (cta_in_group + i * p.cpg) * kTileV;
+        const int v0 = (slot + i * nslots) * kUnit + (int)rank * kTileV;
         for (int k = 0; k < k_steps; ++k) {
-          if (!sm100::mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+          const bool free_ = kPair ? sm100::mbar_wait_cluster(&empty[stage], phase ^ 1u, abort)
+                                   : sm100::mbar_wait(&empty[stage], phase ^ 1u, abort);
+          if (!free_) {
             abort_all(abort, p.err);
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * L.stage_bytes;
-          sm100::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
-          sm100::tma_load_2d(st + L.a_off, &tm_w, &full[stage], k * kTileK, v0, pol_w);
-          sm100::tma_load_2d(st + L.b_off, &tm_h, &full[stage], k * kTileK, row0, pol_h);
+          if (kPair) {
+            // both CTAs' halves complete on the leader's full barrier
+            if (leader) sm100::mbar_arrive_expect_tx(&full[stage], 2 * L.stage_bytes);
+            sm100::tma_load_2d_pair(st + L.a_off, &tm_w, &full[stage], 0, k * kTileK, v0, pol_w);
+            sm100::tma_load_2d_pair(st + L.b_off, &tm_h, &full[stage], 0, k * kTileK, row0 + (int)rank * kBRows,
+                                    pol_h);
+          } else {
+            sm100::mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+            sm100::tma_load_2d(st + L.a_off, &tm_w, &full[stage], k * kTileK, v0, pol_w);
+            sm100::tma_load_2d(st + L.b_off, &tm_h, &full[stage], k * kTileK, row0, pol_h);
+          }
           ++issued;
           if (++stage == p.stages) {
             stage = 0;
@@ -197,29 +228,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       // Every issued load must have landed before the CTA exits: wait (time
       // limited) for the completion of the most recent fill of each stage.
-      for (int j = 0; j < min(issued, p.stages); ++j) {
+      // (A pair's loads all complete on the leader's barriers; the odd CTA
+      // leaves only after the closing cluster barrier.)
+      for (int j = 0; j < (kPair && !leader ? 0 : min(issued, p.stages)); ++j) {
         const int idx = issued - 1 - j;
         sm100::mbar_wait_timeout(&full[idx % p.stages], (uint32_t)((idx / p.stages) & 1), sm100::kWaitTimeoutNs);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && (!kPair || leader)) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = sm100::idesc_bf16_f32(kTileV, N);
+      constexpr uint32_t idesc = sm100::idesc_bf16_f32(kPair ? 2 * kTileV : kTileV, N);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
         const int buf = i & 1;
         const uint32_t acc_phase = (i >> 1) & 1;
-        if (!sm100::mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort)) {
+        const bool drained = kPair ? sm100::mbar_wait_cluster(&acc_empty[buf], acc_phase ^ 1u, abort)
+                                   : sm100::mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort);
+        if (!drained) {
           abort_all(abort, p.err);
           break;
         }
         sm100::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * (p.tmem_cols / 2);
         for (int k = 0; k < k_steps; ++k) {
-          if (!sm100::mbar_wait(&full[stage], phase, abort)) {
+          const bool landed = kPair ? sm100::mbar_wait_cluster(&full[stage], phase, abort)
+                                    : sm100::mbar_wait(&full[stage], phase, abort);
+          if (!landed) {
             abort_all(abort, p.err);
             ok = false;
             break;
@@ -232,21 +269,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             // Advance 16 elements (32 B) along K inside the 128-B swizzled row.
-            sm100::tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                               (k > 0 || kk > 0) ? 1u : 0u);
+            if (kPair)
+              sm100::tc_mma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                      (k > 0 || kk > 0) ? 1u : 0u);
+            else
+              sm100::tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                                 (k > 0 || kk > 0) ? 1u : 0u);
           }
-          sm100::tc_commit(&empty[stage]);  // stage free once these MMAs have read it
+          // stage free (in both CTAs of a pair) once these MMAs have read it
+          if (kPair) sm100::tc_commit_pair_mc(&empty[stage], 3);
+          else sm100::tc_commit(&empty[stage]);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) sm100::tc_commit(&acc_full[buf]);
+        if (ok) {
+          if (kPair) sm100::tc_commit_pair_mc(&acc_full[buf], 3);
+          else sm100::tc_commit(&acc_full[buf]);
+        }
       }
       // Every MMA issued so far has completed before TMEM is released.
-      sm100::tc_commit(final_bar);
+      if (kPair) sm100::tc_commit_pair_mc(final_bar, 3);
+      else sm100::tc_commit(final_bar);
       sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
     }
+  } else if (warp == 1) {
+    // pair, odd CTA: the even CTA's MMAs write this CTA's TMEM; wait for the
+    // last one before the closing barriers.
+    if (lane == 0) sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp % 4;                       // TMEM lane quarter
@@ -257,13 +308,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = i & 1;
       const uint32_t acc_phase = (i >> 1) & 1;
-      const bool ok = __all_sync(0xffffffffu, sm100::mbar_wait(&acc_full[buf], acc_phase, abort) ? 1 : 0) != 0;
+      const bool ok = __all_sync(0xffffffffu, (kPair ? sm100::mbar_wait_cluster(&acc_full[buf], acc_phase, abort)
+                                                     : sm100::mbar_wait(&acc_full[buf], acc_phase, abort))
+                                                  ? 1
+                                                  : 0) != 0;
       if (!ok) {
         if (lane == 0) abort_all(abort, p.err);
         break;
       }
       sm100::tc_fence_after();
-      const int vbase = (cta_in_group + i * p.cpg) * kTileV + 32 * q;   // vocab of lane 0 of this warp
+      const int vbase = (slot + i * nslots) * kUnit + (int)rank * kTileV + 32 * q;   // vocab of lane 0 of this warp
       const int nvalid = min(32, p.V - vbase);                          // may be <= 0 in the tail tile
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
@@ -320,7 +374,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       sm100::tc_fence_before();
       __syncwarp();
-      if (lane == 0) sm100::mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) {
+        if (kPair) sm100::mbar_arrive_remote(&acc_empty[buf], 0);
+        else sm100::mbar_arrive(&acc_empty[buf]);
+      }
     }
     // Merge the four lane quarters' statistics through shared memory, then
     // write one partial per (CTA, row): slice = cta_in_group.
@@ -342,9 +399,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   sm100::tc_fence_before();
   __syncthreads();
+  if (kPair) sm100::cluster_sync();   // both CTAs done with TMEM and with each other's barriers
   if (warp == 1) {
     sm100::tc_fence_after();
-    sm100::tmem_dealloc(tmem_base, p.tmem_cols);
+    if (kPair) sm100::tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    else sm100::tmem_dealloc(tmem_base, p.tmem_cols);
   }
 }
 
@@ -360,17 +419,91 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
 
 struct TcShape {
   int N, groups, cpg, stages;
+  bool pair;
   uint32_t tmem_cols;
 };
+
+constexpr int kPairMinRows = 193;   // from here on a 128-lane tile is bound by shared-memory traffic
+
+template <int NCH, bool kPair>
+cudaError_t set_smem(int smem) {
+  return cudaFuncSetAttribute(lmhead_tc_kernel<NCH, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+// How many 2-CTA clusters of the pair kernel for this N can be resident at
+// once (the persistent grid must not exceed it, or a second wave would run).
+template <int NCH>
+int pair_clusters(int stages) {
+  const int smem = smem_layout(NCH * 32, stages, true).total;
+  if (set_smem<NCH, true>(smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, lmhead_tc_kernel<NCH, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int pair_clusters_for(int nch, int stages) {
+  switch (nch) {
+    case 1: return pair_clusters<1>(stages);
+    case 2: return pair_clusters<2>(stages);
+    case 3: return pair_clusters<3>(stages);
+    case 4: return pair_clusters<4>(stages);
+    case 5: return pair_clusters<5>(stages);
+    case 6: return pair_clusters<6>(stages);
+    case 7: return pair_clusters<7>(stages);
+    case 8: return pair_clusters<8>(stages);
+    default: return 0;
+  }
+}
+
+// Resident 2-CTA clusters per (device, N), queried once.
+int cached_pair_clusters(int nch, int stages) {
+  static std::mutex mu;
+  static int cache[64][9];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& row : cache)
+      for (int& v : row) v = -1;
+    init = true;
+  }
+  if (cache[dev][nch] < 0) cache[dev][nch] = pair_clusters_for(nch, stages);
+  return cache[dev][nch];
+}
 
 TcShape tc_shape(int M, int sm_count) {
   TcShape s;
   s.groups = (M + kMaxN - 1) / kMaxN;
   const int per = (M + s.groups - 1) / s.groups;
   s.N = std::max(32, (per + 31) / 32 * 32);
-  s.cpg = std::max(1, sm_count / s.groups);
+  s.pair = M >= kPairMinRows;
   s.stages = kMaxStages;
-  while (s.stages > 2 && smem_layout(s.N, s.stages).total > kSmemLimit) --s.stages;
+  while (s.stages > 2 && smem_layout(s.N, s.stages, s.pair).total > kSmemLimit) --s.stages;
+  s.cpg = std::max(1, sm_count / s.groups);
+  if (s.pair) {
+    const int clusters = std::min(sm_count / 2, cached_pair_clusters(s.N / 32, s.stages));
+    if (clusters >= s.groups) s.cpg = 2 * (clusters / s.groups);
+    else s.pair = false;   // cannot place one pair per group: single-CTA tiles
+    if (!s.pair) {
+      s.stages = kMaxStages;
+      while (s.stages > 2 && smem_layout(s.N, s.stages, false).total > kSmemLimit) --s.stages;
+    }
+  }
   s.tmem_cols = 64;
   while (s.tmem_cols < (uint32_t)(2 * s.N)) s.tmem_cols *= 2;
   return s;
@@ -379,10 +512,29 @@ TcShape tc_shape(int M, int sm_count) {
 template <int NCH>
 cudaError_t launch_nch(const TcShape& sh, const CUtensorMap& tw, const CUtensorMap& th, const TcParams& p,
                        cudaStream_t s) {
-  const int smem = smem_layout(NCH * 32, sh.stages).total;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = smem_layout(NCH * 32, sh.stages, sh.pair).total;
+  if (!sh.pair) {
+    cudaError_t e = set_smem<NCH, false>(smem);
+    if (e != cudaSuccess) return e;
+    lmhead_tc_kernel<NCH, false><<<sh.groups * sh.cpg, kThreadsTc, smem, s>>>(tw, th, p);
+    return cudaGetLastError();
+  }
+  cudaError_t e = set_smem<NCH, true>(smem);
   if (e != cudaSuccess) return e;
-  lmhead_tc_kernel<NCH><<<sh.groups * sh.cpg, kThreadsTc, smem, s>>>(tw, th, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sh.groups * sh.cpg, 1, 1);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<NCH, true>, tw, th, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -406,7 +558,8 @@ cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& pl, unsigne
   if (sh.cpg != pl.slices) return cudaErrorInvalidValue;
   CUtensorMap tw, th;
   if (!make_map(&tw, a.lm_head, (uint64_t)a.V, (uint64_t)a.H, kTileV)) return cudaErrorInvalidValue;
-  if (!make_map(&th, a.hidden, (uint64_t)pl.M, (uint64_t)a.H, (uint32_t)sh.N)) return cudaErrorInvalidValue;
+  if (!make_map(&th, a.hidden, (uint64_t)pl.M, (uint64_t)a.H, (uint32_t)(sh.pair ? sh.N / 2 : sh.N)))
+    return cudaErrorInvalidValue;
   char* ws = (char*)a.workspace;
   TcParams p;
   p.tokens = a.tokens;
