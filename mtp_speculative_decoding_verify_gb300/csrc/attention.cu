@@ -86,9 +86,19 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
   const int row_tiles = (p.rows_per_kv + rows_per_cta(a) - 1) / rows_per_cta(a);
   const int max_len = a.max_blocks * kBlock;
   const long long base = (long long)a.B * (a.is_mla ? 1 : a.Hkv) * row_tiles;
-  const int kMaxSplitLen = 4096, kMinSplitLen = 256;
-  int n = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));
-  n = std::max(n, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
+  const int kMinSplitLen = 256;
+  int n;
+  if (attention_uses_mla_tc(a)) {
+    // MLA tiles are long and dispatched longest first: split only until the
+    // (request, row block) CTAs fill one wave, since every split adds a
+    // partial write and the combine pass. Keys per split <= 8192.
+    n = base >= sm_count ? 1 : (int)((sm_count + base - 1) / std::max<long long>(base, 1));
+    n = std::max(n, (max_len + 8191) / 8192);
+  } else {
+    const int kMaxSplitLen = 4096;
+    n = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));
+    n = std::max(n, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
+  }
   n = std::min(n, std::max(1, (max_len + kMinSplitLen - 1) / kMinSplitLen));
   int split_len = (max_len + n - 1) / n;
   const int gran = (a.is_mla && a.dtype == MTP_BF16) ? 128 : kBlock;   // MLA tensor-core tiles are 128 keys

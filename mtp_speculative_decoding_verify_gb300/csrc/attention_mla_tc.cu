@@ -194,7 +194,7 @@ __device__ __forceinline__ int item_key_end(const Item& it, int ctx, int R, int 
   return min(it.split * split_len + split_len, ctx + j_max + 1);
 }
 
-constexpr int kMaxItemTiles = 64;   // split_len <= 4096 keys = 32 tiles
+constexpr int kMaxItemTiles = 64;   // split_len <= 8192 keys = 64 tiles
 
 // Orders the work items by tile count, longest first (counting sort, one
 // CTA). Clusters are dispatched in index order, so long items start first
