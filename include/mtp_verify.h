@@ -261,6 +261,20 @@ typedef struct {
 int kv_rollback(const mtp_rollback_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Bounded-wait check (validation only, not on the verify path).
+ *
+ * The tensor-core kernels wait on shared-memory mbarriers (TMA copies, MMA
+ * completion, stage hand-offs); every such wait gives up after a time limit,
+ * sets MTP_ERR_TIMEOUT in the device error word, stops issuing work and
+ * returns, so the context stays usable. This call runs that same wait on an
+ * mbarrier nothing ever arrives on, with a limit of timeout_ns nanoseconds
+ * (1 .. 1e9), so that a test can see the path work: afterwards
+ * mtp_sync_status() returns MTP_DEVICE_ERROR with the timeout bit set (and
+ * clears it). Asynchronous on `stream`; MTP_INVALID_ARG for a limit outside
+ * the range. */
+int mtp_wait_selftest(uint64_t timeout_ns, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Random-stream check (validation only, not on the verify path).
  *
  * The generator is Philox4x32-10 of Salmon, Moraes, Dror and Shaw, "Parallel

@@ -79,6 +79,8 @@ def lib():
         L.mtp_rng_debug.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     ctypes.c_uint32, ctypes.c_int32, _P, _P, _P, _P]
         L.mtp_rng_debug.restype = ctypes.c_int
+        L.mtp_wait_selftest.argtypes = [ctypes.c_uint64, _P]
+        L.mtp_wait_selftest.restype = ctypes.c_int
         L.mtp_verify_logits_accept_noalloc.argtypes = [ctypes.POINTER(LmArgs), _P]
         L.mtp_verify_logits_accept_noalloc.restype = ctypes.c_int
         L.mtp_noalloc_scratch_bytes.argtypes = []
@@ -290,3 +292,9 @@ def rng_debug(seed, b, j, tag, v0, n, device="cuda", stream=None):
     u = torch.empty(n, dtype=torch.float32, device=device)
     _check(lib().mtp_rng_debug(int(seed), b, j, tag, v0, n, _ptr(w), _ptr(e), _ptr(u), _stream_handle(stream)))
     return w.cpu().numpy().view("uint32"), e.cpu().numpy(), u.cpu().numpy()
+
+
+def wait_selftest(timeout_ns, stream=None):
+    """Run the kernels' bounded mbarrier wait on a barrier nothing arrives on
+    (it must give up after timeout_ns and flag a timeout)."""
+    _check(lib().mtp_wait_selftest(int(timeout_ns), _stream_handle(stream)))

@@ -18,6 +18,7 @@ int lmhead_tc_slices(int V, int M, int sm_count);
 bool lmhead_tc_supported(const mtp_lmhead_args& a);
 bool attention_mma_supported(const mtp_attn_args& a);
 size_t accept_decision_bytes();
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* err, cudaStream_t s);
 size_t accept_race_part_bytes();
 cudaError_t launch_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t v0, int n,
                              uint32_t* word0, float* race_e, float* accept_u, cudaStream_t s);
@@ -281,6 +282,18 @@ int mtp_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t 
   cudaError_t e = mtp::launch_rng_debug(seed, b, j, tag, v0, n, word0, race_e, accept_u,
                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rng debug launch");
+  return MTP_OK;
+}
+
+int mtp_wait_selftest(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1 || timeout_ns > 1000000000ull)
+    return fail(MTP_INVALID_ARG, "mtp_wait_selftest: timeout %llu ns outside 1 .. 1e9", (unsigned long long)timeout_ns);
+  DeviceCtx* c = nullptr;
+  int rc = device_ctx(&c);
+  if (rc != MTP_OK) return rc;
+  cudaError_t e = mtp::launch_wait_selftest(timeout_ns, c->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait selftest launch");
+  g_launches = 1;
   return MTP_OK;
 }
 

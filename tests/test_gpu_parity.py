@@ -316,3 +316,25 @@ def test_device_range_checks_report_and_recover():
     w0 = SMALL["cfg0"]
     gpu_lmhead(w0, synth.make_lmhead_inputs(w0, DEV))
     mv.sync_status()
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """The kernels' time-limited mbarrier wait, on a barrier nothing arrives on
+    (no fault, no trap): it returns after the limit and flags a timeout that
+    the host reads; the next calls run normally."""
+    import time
+    t0 = time.perf_counter()
+    mv._binding.wait_selftest(50_000_000)        # 50 ms
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert ei.value.code == 4 and "timeout" in str(ei.value)
+    assert time.perf_counter() - t0 >= 0.04
+    mv.sync_status()                               # the flag was cleared
+    with pytest.raises(mv.MtpError) as ei:
+        mv._binding.wait_selftest(0)
+    assert ei.value.code == 1
+    w = SMALL["cfg1_small_mla"]
+    att = synth.make_attention_inputs(w, DEV)
+    out = gpu_attention(w, att)
+    mv.sync_status()
+    _check_attention(w, att, out, range(w.B))
