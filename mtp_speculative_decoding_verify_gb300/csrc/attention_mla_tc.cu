@@ -23,11 +23,11 @@
 // cluster with a TMA multicast (fills spread round-robin over the CTAs) and
 // released by a multicast tcgen05.commit from each CTA's MMA thread.
 //
-// Warps (4 warpgroups): 0 MMA issuer, 1-3 and 13-15 TMA producers (one 8 KB
-// box per issue, so six warps keep many copies in flight), 4..11 softmax /
-// epilogue (warp w owns TMEM lanes 32*(w%4)..+31 = keys of S^T, dv of O^T,
-// and one half of the 64 row columns), 12 idle. setmaxnreg moves registers
-// from warpgroups 0 and 3 to the softmax warpgroups.
+// Warps (5 warpgroups): 0 MMA issuer, 1-3 TMA producers (lanes 0 and 1 of
+// each issue one 8 KB box at a time, so six copies stay in flight), 4..19
+// softmax / epilogue (warp w owns TMEM lanes 32*(w%4)..+31 = keys of S^T, dv
+// of O^T, and one quarter of the 64 row columns). setmaxnreg moves registers
+// from warpgroup 0 to the softmax warpgroups.
 //
 // Online softmax with a lazy rescale: the reference row max only moves when
 // a score exceeds it by more than 8 (log2 units); one barrier reduction tells
@@ -64,12 +64,14 @@ constexpr int kSlotBytes = 16384;     // one [128 keys x 64 dims] chunk of the t
 constexpr int kSlots = kQChunks;      // the whole tile is resident: slot c = dims 64c .. 64c+63
 constexpr int kPSlot = 8;             // the rope chunk's slot receives P^T once QK is done
 constexpr int kSBufs = 2;
-constexpr int kSoftWarps = 8;
+constexpr int kSoftWarps = 16;        // 4 per TMEM lane quarter, 16 row columns each
 constexpr int kProducers = 6;         // TMA issuing warps (warps 1-3 and 13-15)         // 2 per TMEM lane quarter (row halves)
-constexpr int kThreads = 512;         // 4 warpgroups: [MMA, producer x 3], softmax x 2, idle
-constexpr int kRegsLight = 64;        // producer / MMA / idle warpgroups after setmaxnreg
-constexpr int kRegsSoftmax = 192;     // softmax warpgroups: 128 * (64 + 192 + 192 + 64) = 65536
-static_assert(128 * (2 * kRegsLight + 2 * kRegsSoftmax) <= 65536, "register split exceeds the launch's file");
+constexpr int kThreads = 640;         // 5 warpgroups: [MMA, producer x 3], softmax x 4
+constexpr int kLaunchRegs = 96;       // registers per thread at launch (65536 / 640, rounded down to 8)
+constexpr int kRegsLight = 56;        // MMA / producer warpgroup after setmaxnreg
+constexpr int kRegsSoftmax = 104;     // softmax warpgroups
+static_assert(128 * kRegsLight + 4 * 128 * kRegsSoftmax <= kThreads * kLaunchRegs,
+              "register split exceeds the registers the block is launched with");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyRescale = 8.0f;  // log2 units
@@ -130,14 +132,14 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 // Named barrier 1 over the 256 softmax threads that also returns whether any
 // of them passed true.
 __device__ __forceinline__ bool softmax_barrier_any(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 256, pi;\n\t"
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 512, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -228,6 +230,45 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(const int32_t* __res
   for (int i = threadIdx.x; i < n; i += blockDim.x) order[atomicAdd(&hist[tiles_of(i)], 1)] = i;
 }
 
+// 16 values per lane: lane l (and l ^ 16) ends up with the op-reduction over
+// all 32 lanes of element l % 16 (butterfly over lane bits 3..0, then one
+// exchange across bit 4).
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = upper ? v[k] : v[k + w];
+      const float keep = upper ? v[k + w] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], other) : v[0] + other;
+}
+
+// 32 lanes x 16 consecutive 32-bit columns (thread t: lane base + t).
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                   const __grid_constant__ CUtensorMap tm_kv,
                                                                   const Params p) {
@@ -309,18 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 
   auto softmax_role = [&]() {
     // ------------------------------------------------------- softmax warps
-    const int sw = warp - 4;                 // 0..7
+    const int sw = warp - 4;                 // 0..15
     const int qq = warp % 4;                 // TMEM lane quarter: keys / dv 32*qq + lane
-    const int ch = sw >> 2;                  // row half: rows 32*ch .. 32*ch+31
-    const int st = sw * 32 + lane;           // 0..255
+    const int cq = sw >> 2;                  // row quarter: rows 16*cq .. 16*cq+15
+    const int st = sw * 32 + lane;           // 0..511
     const uint32_t lane_addr = (uint32_t)(32 * qq) << 16;
-    // Thread (qq, lane) sees key 32*qq + lane of every tile for the 32 rows of
-    // its half. It keeps each row's reference max (the same in every thread
-    // of the half) and its own partial row sums; the sums are reduced over
-    // the keys once, after the last tile.
-    float acc[32];
+    // Thread (qq, lane) sees key 32*qq + lane of every tile for the 16 rows of
+    // its quarter and keeps its own partial row sums; the sums are reduced
+    // over the keys once, after the last tile.
+    float acc[16];
 #pragma unroll
-    for (int x = 0; x < 32; ++x) acc[x] = 0.0f;
+    for (int x = 0; x < 16; ++x) acc[x] = 0.0f;
     const int lim_min = ctx + row_base / p.Hq;   // smallest key limit of the block's rows
     // Every softmax warp runs the same sequence of named barriers for every
     // tile; after an abort the tensor-memory work is skipped but the barrier
@@ -332,40 +372,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       // tile's rope chunk was refilled only after PV(i-1) released its slot).
       ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait(&s_full[buf], (i / kSBufs) & 1, abort) ? 1 : 0);
       // d = score (log2 units) - reference max of the row.
-      float d[32];
+      float d[16];
       if (ok) {
         sm100::tc_fence_after();
-        uint32_t r[32];
-        sm100::tmem_ld_32x32b_x32(tmem + lane_addr + kColS + buf * 64 + ch * 32, r);
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem + lane_addr + kColS + buf * 64 + cq * 16, r);
         sm100::tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) d[x] = fmaf(__uint_as_float(r[x]), p.scale_log2, -m_ref[ch * 32 + x]);
+        for (int x = 0; x < 16; ++x) d[x] = fmaf(__uint_as_float(r[x]), p.scale_log2, -m_ref[cq * 16 + x]);
         sm100::tc_fence_before();
         __syncwarp();
         if (lane == 0) sm100::mbar_arrive(&s_empty[buf]);
       } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) d[x] = -INFINITY;
+        for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
       }
       const int tile0 = t0 + i * kKeys;
       if (tile0 + kKeys - 1 > lim_min || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
         const int key = tile0 + 32 * qq + lane;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) d[x] = (key > lim[ch * 32 + x] || key >= t_end) ? -INFINITY : d[x];
+        for (int x = 0; x < 16; ++x) d[x] = (key > lim[cq * 16 + x] || key >= t_end) ? -INFINITY : d[x];
       }
       // The reference only moves when a score exceeds it by more than
       // kLazyRescale: then (and on the first tile) the tile's row maxima are
       // taken and the references updated.
       bool exceed = (i == 0);
 #pragma unroll
-      for (int x = 0; x < 32; ++x) exceed |= d[x] > kLazyRescale;
+      for (int x = 0; x < 16; ++x) exceed |= d[x] > kLazyRescale;
       if (softmax_barrier_any(exceed)) {
         {
-          float t[32];
+          float t[16];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) t[x] = d[x];
+          for (int x = 0; x < 16; ++x) t[x] = d[x];
           // max of d over the warp's keys; the reference is the same for all of them
-          red_max[qq * 64 + ch * 32 + lane] = transpose_reduce<true>(t, lane) + m_ref[ch * 32 + lane];
+          const float mx = transpose_reduce16<true>(t, lane);
+          if (lane < 16) red_max[qq * 64 + cq * 16 + lane] = mx + m_ref[cq * 16 + lane];
         }
         softmax_barrier();
         if (st < kRows) {
@@ -385,23 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         softmax_barrier();
         bool rescale = false;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const float sc = rscale[ch * 32 + x];
+        for (int x = 0; x < 16; ++x) {
+          const float sc = rscale[cq * 16 + x];
           rescale |= sc != 1.0f;
           acc[x] *= sc;
-          d[x] += m_shift[ch * 32 + x];
+          d[x] += m_shift[cq * 16 + x];
         }
         // O^T columns of these rows hold PV up to tile i-1 (complete): rescale them.
         if (ok && i > 0 && rescale) {
 #pragma unroll 1
           for (int dc = 0; dc < 4; ++dc) {
-            uint32_t r[32];
-            const uint32_t ta = tmem + lane_addr + kColO + dc * 64 + ch * 32;
-            sm100::tmem_ld_32x32b_x32(ta, r);
+            uint32_t r[16];
+            const uint32_t ta = tmem + lane_addr + kColO + dc * 64 + cq * 16;
+            tmem_ld_32x32b_x16(ta, r);
             sm100::tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * rscale[ch * 32 + x]);
-            tmem_st_32x32b_x32(ta, r);
+            for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * rscale[cq * 16 + x]);
+            tmem_st_32x32b_x16(ta, r);
           }
           tmem_st_wait();
         }
@@ -413,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         uint8_t* pb = smem + kSlotOff + kPSlot * kSlotBytes + (k >> 6) * 8192;
         const int kin = k & 63;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
+        for (int x = 0; x < 16; ++x) {
           const float pv = fast_exp2(d[x]);
           acc[x] += pv;
-          const int r = ch * 32 + x;
+          const int r = cq * 16 + x;
           *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kin >> 3) ^ (r & 7))) << 4) + (kin & 7) * 2) =
               __float2bfloat16_rn(pv);
         }
@@ -431,7 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       raise_error(p.err, MTP_ERR_TIMEOUT);
     }
     // Row sums: over the warp's 32 keys, then over the 4 lane quarters.
-    red_sum[qq * 64 + ch * 32 + lane] = transpose_reduce<false>(acc, lane);
+    {
+      const float sm = transpose_reduce16<false>(acc, lane);
+      if (lane < 16) red_sum[qq * 64 + cq * 16 + lane] = sm;
+    }
     softmax_barrier();
     if (st < kRows) l_run[st] = red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
     // -------------------------------------------------------- epilogue
@@ -443,12 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 #pragma unroll 1
       for (int dc = 0; dc < 4; ++dc) {
         const int dv = dc * 128 + dvl;
-        uint32_t r[32];
-        sm100::tmem_ld_32x32b_x32(tmem + lane_addr + kColO + dc * 64 + ch * 32, r);
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem + lane_addr + kColO + dc * 64 + cq * 16, r);
         sm100::tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const int rloc = ch * 32 + x;
+        for (int x = 0; x < 16; ++x) {
+          const int rloc = cq * 16 + x;
           const int rr = row_base + rloc;
           if (rr >= rows) continue;
           const float l = l_run[rloc];
@@ -469,13 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   // Warp roles. Warpgroups 0 and 3 hand registers to the softmax warpgroups
   // (every warp of a warpgroup runs the same setmaxnreg).
   const int wg = warp / 4;
-  if (wg == 1 || wg == 2) {
+  if (wg >= 1) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     softmax_role();
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
-    const int pw = warp <= 3 ? warp - 1 : (warp >= 13 ? warp - 10 : -1);   // producer 0..5, or -1
-    if (pw >= 0 && lane == 0) {
+    const int pw = (warp >= 1 && lane < 2) ? 2 * (warp - 1) + lane : -1;   // producer 0..5 (warps 1-3, lanes 0-1)
+    if (pw >= 0) {
       // ------------------------------------------------------ TMA producers
       // A tile is 18 boxes of [64 keys x 64 dims] (8 KB): box x = slot x/2,
       // keys 64*(x%2).. of the tile. Producer pw owns boxes pw, pw+6, pw+12
