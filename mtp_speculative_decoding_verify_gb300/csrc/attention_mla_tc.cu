@@ -155,6 +155,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Two floats to bf16 (round to nearest even) in one instruction: lo in bits
+// 0..15, hi in bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void store_b16(uint8_t* p, uint32_t v) {
+  *reinterpret_cast<uint16_t*>(p) = (uint16_t)v;
+}
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Lane l ends up with op-reduction over the 32 lanes of element l of v[]
@@ -454,12 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         uint8_t* pb = smem + kSlotOff + kPSlot * kSlotBytes + (k >> 6) * 8192;
         const int kin = k & 63;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const float pv = fast_exp2(d[x]);
-          acc[x] += pv;
+        for (int x = 0; x < 16; x += 2) {   // rows r, r+1: one packed conversion, two 16-bit stores
+          const float p0 = fast_exp2(d[x]), p1 = fast_exp2(d[x + 1]);
+          acc[x] += p0;
+          acc[x + 1] += p1;
           const int r = cq * 16 + x;
-          *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((((kin >> 3) ^ (r & 7))) << 4) + (kin & 7) * 2) =
-              __float2bfloat16_rn(pv);
+          const uint32_t pair = pack_bf16x2(p0, p1);
+          store_b16(pb + r * 128 + ((((kin >> 3) ^ (r & 7))) << 4) + (kin & 7) * 2, pair);
+          store_b16(pb + (r + 1) * 128 + ((((kin >> 3) ^ ((r + 1) & 7))) << 4) + (kin & 7) * 2, pair >> 16);
         }
       }
       fence_async_smem();
