@@ -53,6 +53,8 @@ def workloads():
         "profile_mla_V32k": synth.CFG1.with_(name="profiling case: DeepSeek-V3-shaped MLA B=32 D=3, vocab 32768",
                                              V=32768),
         "profile_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, B=16", B=16),
+        "profile_sampling_V32k": synth.CFG2.with_(
+            name="profiling case: Llama-70B-shaped rejection sampling B=64 D=5, vocab 32768", V=32768),
     }
 
 
@@ -70,7 +72,7 @@ def load_peaks():
 # a reduced vocabulary (32768) of the same kernel and shapes; traffic grows in
 # proportion to the vocabulary, so it is scaled to the full one. Only valid
 # while the kernel is unchanged since the capture (profiles/ names the file).
-LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.688704e6 + 3.054592e6) / 32768}
+LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.689728e6 + 3.065088e6) / 32768}
 
 
 def elem_bytes(w):
