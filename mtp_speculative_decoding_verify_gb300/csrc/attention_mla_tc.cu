@@ -118,18 +118,6 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
   return d;
 }
 
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
@@ -668,6 +656,464 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   if (C > 1) sm100::cluster_sync();   // no peer may still multicast into, or arrive on, this CTA
 }
 
+// ----------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2): the two CTAs of a cluster hold 64
+// query rows each (two row blocks of one request) and share every MMA:
+//   S [128 rows x 128 keys]   = Q . K^T   pair M = 128 (64 rows per CTA), N = 128 keys;
+//                                           each CTA stages 64 of the tile's keys, all 576 dims
+//   O [128 rows x 512 dv]    += P . V     pair M = 128, N = 256 dv, twice (dv 0..255, 256..511);
+//                                           each CTA stages V of all 128 keys for its 128-dv
+//                                           half of each product (B operand, MN-major)
+// Each CTA's TMEM then holds S and O of its own 64 rows only (TMEM lane l: row
+// l % 64; lanes 64..127 carry the second half of the columns), so the softmax,
+// its lazy rescale, the row sums and the normalisation stay local to the CTA.
+// Per 128-key tile a CTA stages 136 KB and reads ~250 KB of operands, against
+// 147 KB and ~410 KB for one 64-row CTA on its own; the MMAs have N = 128/256.
+namespace pr {
+constexpr int kQOff = 0;                          // 9 x [64 rows x 64 dims]
+constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]; slots 7, 8 take P after QK
+constexpr int kVOff = kKOff + 9 * 8192;           // 8 x [64 keys x 64 dv]: slot (h * 2 + kb) * 2 + j
+constexpr int kRedOff = kVOff + 8 * 8192;         // red_max[8][64], red_sum[8][64]
+constexpr int kRowOff = kRedOff + 2 * 8 * 64 * 4; // m_run, m_ref, rscale, m_shift, l_run [64] f32, lim [64] i32
+constexpr int kBarOff = kRowOff + 6 * 64 * 4;
+constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull uses 3 of its 9)
+constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+constexpr uint32_t kColO = 0;                     // O of product h at columns 128 h .. +127
+constexpr uint32_t kColS = 256;                   // S buffer b at 256 + 64 b
+}  // namespace pr
+
+__global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                    const __grid_constant__ CUtensorMap tm_kv,
+                                                                    const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* red_max = reinterpret_cast<float*>(smem + pr::kRedOff);   // [8][64]
+  float* red_sum = red_max + 8 * 64;
+  float* m_run = reinterpret_cast<float*>(smem + pr::kRowOff);
+  float* m_ref = m_run + 64;
+  float* rscale = m_run + 128;
+  float* m_shift = m_run + 192;
+  float* l_run = m_run + 256;
+  int* lim = reinterpret_cast<int*>(m_run + 320);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // [3] leader: both CTAs' chunks 3g..3g+2 landed
+  uint64_t* kempty = kfull + 9;                                         // [9] both: slot c free
+  uint64_t* vfull = kempty + 9;                                         // [2] leader: V boxes of key half kb landed
+  uint64_t* vempty = vfull + 2;                                         // [2] both
+  uint64_t* qbar = vempty + 2;                                          // leader: both CTAs' Q landed
+  uint64_t* s_full = qbar + 1;                                          // [2] both
+  uint64_t* s_empty = s_full + 2;                                       // [2] leader, one arrive per CTA
+  uint64_t* p_full = s_empty + 2;                                       // leader, one arrive per CTA
+  uint64_t* o_done = p_full + 1;                                        // both
+  uint64_t* final_bar = o_done + 1;                                     // both
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pr::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + pr::kMiscOff + 4);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = sm100::cluster_ctarank();
+  const bool leader = rank == 0;
+  const Item item = decode_item(p.order[blockIdx.x / 2], p.B, p.groups);
+  const int split = item.split, b = item.b;
+  const int rows = p.R * p.Hq;
+  const int row_base = (item.g * 2 + (int)rank) * kRows;
+  const int ctx = p.ctx_lens[b];
+  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {   // uniform over the pair (same request)
+    if (threadIdx.x == 0 && split == 0 && row_base == 0) raise_error(p.err, MTP_ERR_LENGTH);
+    return;
+  }
+  const int t0 = split * p.split_len;
+  const int t_end = item_key_end(item, ctx, p.R, p.Hq, rows, 2, p.split_len);
+  if (t0 >= t_end) return;
+  const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
+
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < 9; ++c) {
+      if (c < 3) sm100::mbar_init(&kfull[c], 1);
+      sm100::mbar_init(&kempty[c], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      sm100::mbar_init(&vfull[k], 1);
+      sm100::mbar_init(&vempty[k], 1);
+      sm100::mbar_init(&s_full[k], 1);
+      sm100::mbar_init(&s_empty[k], 2);   // one arrive per CTA
+    }
+    sm100::mbar_init(qbar, 1);
+    sm100::mbar_init(p_full, 2);
+    sm100::mbar_init(o_done, 1);
+    sm100::mbar_init(final_bar, 1);
+    *abort = 0;
+    sm100::fence_barrier_init();
+  }
+  if (warp == 0) {
+    sm100::tmem_alloc_pair(tmem_slot, kTmemCols);
+    sm100::tmem_relinquish_pair();
+  }
+  if (threadIdx.x < kRows) {
+    const int rr = min(row_base + (int)threadIdx.x, rows - 1);
+    lim[threadIdx.x] = ctx + rr / p.Hq;
+    m_run[threadIdx.x] = -INFINITY;
+    m_ref[threadIdx.x] = 0.0f;
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::cluster_sync();   // both CTAs' barriers and TMEM exist before any remote arrive, load or MMA
+  sm100::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t smem_base = sm100::smem_u32(smem);
+
+  auto softmax_role = [&]() {
+    // ------------------------------------------------------- softmax warps
+    // Warp (q = warp % 4, sub = (warp - 4) / 4): TMEM lanes 32 q .. 32 q + 31,
+    // i.e. rows r = 32 (q % 2) + lane, keys 64 (q / 2) + 16 sub .. + 15 of S.
+    const int sw = warp - 4;
+    const int q = warp % 4, sub = sw >> 2;
+    const int r = 32 * (q & 1) + lane;
+    const int khalf = q >> 1;
+    const int part = khalf * 4 + sub;                 // which of the row's 8 partials this thread holds
+    const int st = sw * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
+    const int lim_r = lim[r];
+    const int lim_min = ctx + row_base / p.Hq;
+    float acc = 0.0f;                                 // partial row sum over this thread's keys
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int buf = i & 1;
+      ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(&s_full[buf], (i >> 1) & 1, abort) ? 1 : 0);
+      float d[16];
+      const float mr = m_ref[r];
+      if (ok) {
+        sm100::tc_fence_after();
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColS + buf * 64 + sub * 16, v);
+        sm100::tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 16; ++x) d[x] = fmaf(__uint_as_float(v[x]), p.scale_log2, -mr);
+        sm100::tc_fence_before();
+      } else {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
+      }
+      const int tile0 = t0 + i * kKeys;
+      if (tile0 + kKeys - 1 > lim_min || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
+        const int key0 = tile0 + 64 * khalf + 16 * sub;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) d[x] = (key0 + x > lim_r || key0 + x >= t_end) ? -INFINITY : d[x];
+      }
+      bool exceed = (i == 0);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) exceed |= d[x] > kLazyRescale;
+      const bool any_exceed = softmax_barrier_any(exceed);
+      // every softmax warp of this CTA has read S(i) from TMEM: one arrive
+      if (st == 0) sm100::mbar_arrive_remote_relaxed(&s_empty[buf], 0);
+      if (any_exceed) {
+        float mx = d[0];
+#pragma unroll
+        for (int x = 1; x < 16; ++x) mx = fmaxf(mx, d[x]);
+        red_max[part * 64 + r] = mx + mr;
+        softmax_barrier();
+        if (st < kRows) {
+          float mt = red_max[st];
+#pragma unroll
+          for (int k = 1; k < 8; ++k) mt = fmaxf(mt, red_max[k * 64 + st]);
+          const float mo = m_run[st];
+          float mn = mo, sc = 1.0f;
+          if (mt > mo + kLazyRescale) {
+            mn = mt;
+            sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+          }
+          m_run[st] = mn;
+          const float ref = mn == -INFINITY ? 0.0f : mn;   // rows with no visible key yet: p = 2^-inf = 0
+          m_shift[st] = m_ref[st] - ref;
+          m_ref[st] = ref;
+          rscale[st] = sc;
+        }
+        softmax_barrier();
+        const float sc = rscale[r];
+        acc *= sc;
+        const float sh = m_shift[r];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) d[x] += sh;
+        // O of these rows holds PV up to tile i-1 (complete): rescale it. This
+        // warp owns 64 of the 256 O columns of its TMEM lanes.
+        if (ok && i > 0 && __any_sync(0xffffffffu, sc != 1.0f)) {
+          const int h = sub >> 1, c0 = (sub & 1) * 64;
+#pragma unroll 1
+          for (int t = 0; t < 4; ++t) {
+            uint32_t v[16];
+            const uint32_t ta = tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16;
+            tmem_ld_32x32b_x16(ta, v);
+            sm100::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * sc);
+            tmem_st_32x32b_x16(ta, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      // p = 2^d into P [64 rows x 128 keys] (K-major A operand of PV, two
+      // 64-key blocks in K slots 7 and 8) and into the partial row sum.
+      {
+        uint8_t* pb = smem + pr::kKOff + (7 + khalf) * 8192 + r * 128;
+        uint32_t w[8];
+#pragma unroll
+        for (int x = 0; x < 16; x += 2) {
+          const float p0 = fast_exp2(d[x]), p1 = fast_exp2(d[x + 1]);
+          acc += p0 + p1;
+          w[x / 2] = pack_bf16x2(p0, p1);
+        }
+        const int ch = 2 * sub;   // 16-byte chunks 2 sub, 2 sub + 1 of the row
+        *reinterpret_cast<uint4*>(pb + (((ch) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(pb + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      fence_async_smem();
+      sm100::tc_fence_before();
+      softmax_barrier();   // all of this CTA's P is written
+      if (st == 0 && ok) sm100::mbar_arrive_remote(p_full, 0);
+    }
+    if (!ok && lane == 0) {
+      *abort = 1;
+      raise_error(p.err, MTP_ERR_TIMEOUT);
+    }
+    red_sum[part * 64 + r] = acc;
+    softmax_barrier();
+    if (st < kRows) {
+      float l = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) l += red_sum[k * 64 + st];
+      l_run[st] = l;
+    }
+    // -------------------------------------------------------- epilogue
+    const bool done =
+        ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (n_tiles - 1) & 1, abort) ? 1 : 0);
+    softmax_barrier();
+    if (done) {
+      sm100::tc_fence_after();
+      const int h = sub >> 1, c0 = (sub & 1) * 64;
+      const int rr = row_base + r;
+      const float l = l_run[r];
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      const int dv0 = 256 * h + 128 * khalf + c0;     // this thread's TMEM lane 32 q + lane: dv half q / 2
+#pragma unroll 1
+      for (int t = 0; t < 4; ++t) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16, v);
+        sm100::tmem_ld_wait();
+        if (rr < rows) {
+          const int64_t orow = (int64_t)b * rows + rr;
+          const int dv = dv0 + t * 16;
+          if (p.n_splits == 1) {
+            uint32_t w[8];
+#pragma unroll
+            for (int x = 0; x < 16; x += 2)
+              w[x / 2] = pack_bf16x2(__uint_as_float(v[x]) * inv, __uint_as_float(v[x + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDV + dv);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            float* dst = p.part_o + (orow * p.n_splits + split) * kDV + dv;
+#pragma unroll
+            for (int x = 0; x < 16; x += 4)
+              *reinterpret_cast<float4*>(dst + x) =
+                  make_float4(__uint_as_float(v[x]) * inv, __uint_as_float(v[x + 1]) * inv,
+                              __uint_as_float(v[x + 2]) * inv, __uint_as_float(v[x + 3]) * inv);
+          }
+        }
+      }
+      if (p.n_splits > 1 && st < kRows && row_base + st < rows) {
+        const float l2 = l_run[st];
+        const int64_t orow = (int64_t)b * rows + row_base + st;
+        p.part_lse[orow * p.n_splits + split] = l2 > 0.0f ? (m_run[st] + log2f(l2)) * kLn2 : -INFINITY;
+      }
+    }
+  };
+
+  const int wg = warp / 4;
+  if (wg >= 1) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    softmax_role();
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
+    const int pw = (warp >= 1 && lane < 2) ? 2 * (warp - 1) + lane : -1;   // producer 0..5
+    if (pw >= 0) {
+      // ------------------------------------------------------ TMA producers
+      // Per tile a CTA loads 17 boxes of [64 keys x 64 dims]: K chunk c of its
+      // own key half (slot c), and V boxes (h, kb, j) = dims 64 (4 h + 2 rank + j)
+      // of key half kb. Both CTAs' boxes complete on the leader's barriers.
+      // Producer pw owns K chunk pw (and pw + 6 for pw < 3); producers 3-5
+      // also own the V boxes: 3 -> (h 0, kb 0), 4 -> (h 1, kb 0), 5 -> kb 1.
+      const uint64_t pol_kv = sm100::l2_policy_evict_last();
+      const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
+      auto block_of = [&](int key0) -> int {
+        if (key0 >= t_end) return -1;
+        const int blk = tbl[key0 / kBlock];
+        if (blk < 0 || blk >= p.num_blocks) {
+          raise_error(p.err, MTP_ERR_BLOCK_ID);
+          return -1;
+        }
+        return blk;
+      };
+      if (pw == 0) {
+        sm100::tma_prefetch_desc(&tm_q);
+        sm100::tma_prefetch_desc(&tm_kv);
+        if (leader) sm100::mbar_arrive_expect_tx(qbar, 2 * kQChunks * 8192);
+        const uint64_t pol_q = sm100::l2_policy_evict_first();
+        for (int c = 0; c < kQChunks; ++c)   // both CTAs' Q complete on the leader's barrier
+          sm100::tma_load_2d_pair(smem + pr::kQOff + c * 8192, &tm_q, qbar, 0, c * 64, b * rows + row_base, pol_q);
+      }
+      bool ok = true;
+      const int kc0 = pw, kc1 = pw + 6;   // K chunks of this producer (kc1 valid for pw < 3)
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const uint32_t par = (uint32_t)((i & 1) ^ 1);
+        const int own_key0 = t0 + i * kKeys + 64 * (int)rank;
+        // K chunk kc0 (released after QK)
+        {
+          ok = sm100::mbar_wait_cluster(&kempty[kc0], par, abort);
+          if (!ok) break;
+          if (leader && kc0 % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[kc0 / 3], 2 * 3 * 8192);
+          sm100::tma_load_3d_pair(smem + pr::kKOff + kc0 * 8192, &tm_kv, &kfull[kc0 / 3], 0, kc0 * 64, 0,
+                                  block_of(own_key0), pol_kv);
+        }
+        // V boxes
+        if (pw >= 3) {
+          const int kb = pw == 5 ? 1 : 0;
+          ok = sm100::mbar_wait_cluster(&vempty[kb], par, abort);
+          if (!ok) break;
+          if (leader && pw != 4) sm100::mbar_arrive_expect_tx(&vfull[kb], 2 * 4 * 8192);
+          const int key0 = t0 + i * kKeys + 64 * kb;
+          const int blk = block_of(key0);
+          for (int h = 0; h < 2; ++h) {
+            if (pw == 3 && h == 1) continue;
+            if (pw == 4 && h == 0) continue;
+            for (int j = 0; j < 2; ++j) {
+              const int slot = (h * 2 + kb) * 2 + j;
+              const int dchunk = 4 * h + 2 * (int)rank + j;
+              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[kb], 0, dchunk * 64, 0, blk,
+                                      pol_kv);
+            }
+          }
+        }
+        // K chunk kc1 (slots 6, 7, 8; 7 and 8 are released after PV)
+        if (kc1 < 9) {
+          ok = sm100::mbar_wait_cluster(&kempty[kc1], par, abort);
+          if (!ok) break;
+          if (leader && kc1 % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[kc1 / 3], 2 * 3 * 8192);
+          sm100::tma_load_3d_pair(smem + pr::kKOff + kc1 * 8192, &tm_kv, &kfull[kc1 / 3], 0, kc1 * 64, 0,
+                                  block_of(own_key0), pol_kv);
+        }
+      }
+      if (!ok) {
+        *abort = 1;
+        raise_error(p.err, MTP_ERR_TIMEOUT);
+      }
+      // The leader's producers wait (time-limited) for the last fill of each
+      // barrier they armed; the odd CTA's copies complete on those barriers.
+      if (leader) {
+        if (pw == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
+        const uint32_t last = (uint32_t)((n_tiles - 1) & 1);
+        if (kc0 % 3 == 0) sm100::mbar_wait_timeout(&kfull[kc0 / 3], last, sm100::kWaitTimeoutNs);
+        if (kc1 < 9 && kc1 % 3 == 0) sm100::mbar_wait_timeout(&kfull[kc1 / 3], last, sm100::kWaitTimeoutNs);
+        if (pw == 3 || pw == 5) sm100::mbar_wait_timeout(&vfull[pw == 5 ? 1 : 0], last, sm100::kWaitTimeoutNs);
+      }
+    } else if (warp == 0 && leader) {
+      // ---------------------------------------------------------------- MMA
+      // The whole warp runs the issue loop (descriptors stay warp-uniform) and
+      // one elected lane issues. The next chunk's barrier is probed before the
+      // current chunk's MMAs go out, so its latency overlaps the issue.
+      constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, 128);
+      constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, 256) | (1u << 16);   // B (V) MN-major
+      const uint64_t d_q = desc_kmajor(smem_base + pr::kQOff);
+      const uint64_t d_k = desc_kmajor(smem_base + pr::kKOff);
+      const uint64_t d_p = desc_kmajor(smem_base + pr::kKOff + 7 * 8192);
+      const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
+      auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, sm100::mbar_wait_cluster(bar, par, abort) ? 1 : 0) != 0;
+      };
+      auto landed = [&](uint64_t* bar, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, sm100::mbar_test_wait_cluster(bar, par) ? 1 : 0) != 0;
+      };
+      bool ok = wait_all(qbar, 0);
+      auto issue_qk = [&](int i) -> bool {
+        const int buf = i & 1;
+        const uint32_t par = (uint32_t)(i & 1);
+        if (!wait_all(&s_empty[buf], ((i >> 1) & 1) ^ 1u)) return false;
+        const uint32_t d = tmem + pr::kColS + buf * 64;
+        bool ready = landed(&kfull[0], par);
+#pragma unroll 1
+        for (int c = 0; c < 9; ++c) {
+          if (c % 3 == 0) {   // chunks 3g .. 3g+2 land together
+            if (!ready && !wait_all(&kfull[c / 3], par)) return false;
+            sm100::tc_fence_after();
+            ready = c + 3 < 9 ? landed(&kfull[c / 3 + 1], par) : true;
+          }
+          if (sm100::elect_one()) {
+            const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
+            sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
+            if (c < 7) sm100::tc_commit_pair_mc(&kempty[c], 3);
+          }
+          __syncwarp();
+        }
+        if (sm100::elect_one()) sm100::tc_commit_pair_mc(&s_full[buf], 3);
+        __syncwarp();
+        return true;
+      };
+      auto issue_pv = [&](int i) -> bool {
+        const uint32_t par = (uint32_t)(i & 1);
+        if (!wait_all(p_full, par)) return false;
+        bool ready = landed(&vfull[0], par);
+#pragma unroll 1
+        for (int kb = 0; kb < 2; ++kb) {
+          if (!ready && !wait_all(&vfull[kb], par)) return false;
+          sm100::tc_fence_after();
+          ready = kb == 0 ? landed(&vfull[1], par) : true;
+          if (sm100::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, d_p + (uint64_t)(kb * 512 + kk * 2),
+                                        d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
+                                        (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            sm100::tc_commit_pair_mc(&vempty[kb], 3);
+          }
+          __syncwarp();
+        }
+        if (sm100::elect_one()) {
+          sm100::tc_commit_pair_mc(&kempty[7], 3);
+          sm100::tc_commit_pair_mc(&kempty[8], 3);
+          sm100::tc_commit_pair_mc(o_done, 3);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        ok = issue_pv(i);
+        if (ok && i + 1 < n_tiles) ok = issue_qk(i + 1);
+      }
+      if (!ok && lane == 0) {
+        *abort = 1;
+        raise_error(p.err, MTP_ERR_TIMEOUT);
+      }
+      if (sm100::elect_one()) sm100::tc_commit_pair_mc(final_bar, 3);
+      __syncwarp();
+      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
+    } else if (warp == 0 && lane == 0) {
+      // odd CTA: the leader's MMAs write this CTA's TMEM; wait for the last one
+      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
+    }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::cluster_sync();   // neither CTA leaves while the pair's MMAs, copies or arrives may touch it
+  if (warp == 0) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 int mla_tc_split_granularity() { return kKeys; }
@@ -706,8 +1152,11 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   p.n_splits = pl.n_splits;
   p.scale_log2 = a.sm_scale * kLog2e;
   const int row_blocks = (rows + kRows - 1) / kRows;
-  int C = kMaxCluster;
-  while (row_blocks % C) --C;   // cluster = row blocks of one request, at most kMaxCluster
+  // Row blocks pair up: the CTA-pair kernel; otherwise single-CTA MMAs, with
+  // clusters of up to kMaxCluster row blocks sharing each fill by multicast.
+  const bool paired = row_blocks % 2 == 0;
+  int C = paired ? 2 : kMaxCluster;
+  while (row_blocks % C) --C;
   p.cluster = C;
   p.groups = row_blocks / C;
   const int n_items = pl.n_splits * a.B * p.groups;
@@ -715,12 +1164,14 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
                                          a.max_blocks * kBlock, (int32_t*)((char*)a.workspace + pl.ws_order));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const int smem_bytes = paired ? pr::kSmemBytes : kSmemBytes;
+  e = paired ? cudaFuncSetAttribute(attn_mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
+             : cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_items * C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -729,7 +1180,8 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tq, tkv, p);
+  e = paired ? cudaLaunchKernelEx(&cfg, attn_mla_pair_kernel, tq, tkv, p)
+             : cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tq, tkv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
