@@ -669,12 +669,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 // its lazy rescale, the row sums and the normalisation stay local to the CTA.
 // Per 128-key tile a CTA stages 136 KB and reads ~250 KB of operands, against
 // 147 KB and ~410 KB for one 64-row CTA on its own; the MMAs have N = 128/256.
+// The nine K chunks of a tile land on one barrier and are released together
+// once QK has read them, and likewise the eight V boxes: the next tile's keys
+// and values load during the softmax and PV, and the issue loop only waits
+// four times per tile (each wait costs the issuing warp a few hundred clocks
+// even when the phase is already complete). The softmax's reduction scratch
+// shares the P buffer (used only while no PV reads it).
 namespace pr {
 constexpr int kQOff = 0;                          // 9 x [64 rows x 64 dims]
-constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]; slots 7, 8 take P after QK
+constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]
 constexpr int kVOff = kKOff + 9 * 8192;           // 8 x [64 keys x 64 dv]: slot (h * 2 + kb) * 2 + j
-constexpr int kRedOff = kVOff + 8 * 8192;         // red_max[8][64], red_sum[8][64]
-constexpr int kRowOff = kRedOff + 2 * 8 * 64 * 4; // m_run, m_ref, rscale, m_shift, l_run [64] f32, lim [64] i32
+constexpr int kPOff = kVOff + 8 * 8192;           // P [64 rows x 128 keys]: keys 0..63, then 64..127
+constexpr int kRedOff = kPOff + 8192;             // red_max[8][64], red_sum[8][64] alias P keys 64..127
+constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, lim [64] i32
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
 constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull uses 3 of its 9)
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
@@ -696,10 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   float* m_shift = m_run + 192;
   float* l_run = m_run + 256;
   int* lim = reinterpret_cast<int*>(m_run + 320);
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // [3] leader: both CTAs' chunks 3g..3g+2 landed
-  uint64_t* kempty = kfull + 9;                                         // [9] both: slot c free
-  uint64_t* vfull = kempty + 9;                                         // [2] leader: V boxes of key half kb landed
-  uint64_t* vempty = vfull + 2;                                         // [2] both
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // leader: both CTAs' 9 K chunks landed
+  uint64_t* kempty = kfull + 9;                                         // both: the K slots are free
+  uint64_t* vfull = kempty + 9;                                         // leader: both CTAs' 8 V boxes landed
+  uint64_t* vempty = vfull + 2;                                         // both: the V slots are free
   uint64_t* qbar = vempty + 2;                                          // leader: both CTAs' Q landed
   uint64_t* s_full = qbar + 1;                                          // [2] both
   uint64_t* s_empty = s_full + 2;                                       // [2] leader, one arrive per CTA
@@ -727,13 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
-    for (int c = 0; c < 9; ++c) {
-      if (c < 3) sm100::mbar_init(&kfull[c], 1);
-      sm100::mbar_init(&kempty[c], 1);
-    }
+    sm100::mbar_init(kfull, 1);
+    sm100::mbar_init(kempty, 1);
+    sm100::mbar_init(vfull, 1);
+    sm100::mbar_init(vempty, 1);
     for (int k = 0; k < 2; ++k) {
-      sm100::mbar_init(&vfull[k], 1);
-      sm100::mbar_init(&vempty[k], 1);
       sm100::mbar_init(&s_full[k], 1);
       sm100::mbar_init(&s_empty[k], 2);   // one arrive per CTA
     }
@@ -851,9 +856,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         }
       }
       // p = 2^d into P [64 rows x 128 keys] (K-major A operand of PV, two
-      // 64-key blocks in K slots 7 and 8) and into the partial row sum.
+      // 64-key blocks) and into the partial row sum. (PV(i-1) is complete and
+      // no thread reads red_max any more, which shares the second block.)
       {
-        uint8_t* pb = smem + pr::kKOff + (7 + khalf) * 8192 + r * 128;
+        uint8_t* pb = smem + pr::kPOff + khalf * 8192 + r * 128;
         uint32_t w[8];
 #pragma unroll
         for (int x = 0; x < 16; x += 2) {
@@ -874,6 +880,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       *abort = 1;
       raise_error(p.err, MTP_ERR_TIMEOUT);
     }
+    // -------------------------------------------------------- epilogue
+    // The last PV is complete (so P, which red_sum shares, is free).
+    const bool done =
+        ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (n_tiles - 1) & 1, abort) ? 1 : 0);
+    softmax_barrier();
     red_sum[part * 64 + r] = acc;
     softmax_barrier();
     if (st < kRows) {
@@ -882,9 +893,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       for (int k = 0; k < 8; ++k) l += red_sum[k * 64 + st];
       l_run[st] = l;
     }
-    // -------------------------------------------------------- epilogue
-    const bool done =
-        ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (n_tiles - 1) & 1, abort) ? 1 : 0);
     softmax_barrier();
     if (done) {
       sm100::tc_fence_after();
@@ -967,18 +975,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         const int own_key0 = t0 + i * kKeys + 64 * (int)rank;
         // K chunk kc0 (released after QK)
         {
-          ok = sm100::mbar_wait_cluster(&kempty[kc0], par, abort);
+          ok = sm100::mbar_wait_cluster(kempty, par, abort);
           if (!ok) break;
-          if (leader && kc0 % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[kc0 / 3], 2 * 3 * 8192);
-          sm100::tma_load_3d_pair(smem + pr::kKOff + kc0 * 8192, &tm_kv, &kfull[kc0 / 3], 0, kc0 * 64, 0,
-                                  block_of(own_key0), pol_kv);
+          if (leader && pw == 0) sm100::mbar_arrive_expect_tx(kfull, 2 * 9 * 8192);
+          sm100::tma_load_3d_pair(smem + pr::kKOff + kc0 * 8192, &tm_kv, kfull, 0, kc0 * 64, 0, block_of(own_key0),
+                                  pol_kv);
         }
         // V boxes
         if (pw >= 3) {
           const int kb = pw == 5 ? 1 : 0;
-          ok = sm100::mbar_wait_cluster(&vempty[kb], par, abort);
+          ok = sm100::mbar_wait_cluster(vempty, par, abort);
           if (!ok) break;
-          if (leader && pw != 4) sm100::mbar_arrive_expect_tx(&vfull[kb], 2 * 4 * 8192);
+          if (leader && pw == 3) sm100::mbar_arrive_expect_tx(vfull, 2 * 8 * 8192);
           const int key0 = t0 + i * kKeys + 64 * kb;
           const int blk = block_of(key0);
           for (int h = 0; h < 2; ++h) {
@@ -987,19 +995,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
             for (int j = 0; j < 2; ++j) {
               const int slot = (h * 2 + kb) * 2 + j;
               const int dchunk = 4 * h + 2 * (int)rank + j;
-              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[kb], 0, dchunk * 64, 0, blk,
+              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, vfull, 0, dchunk * 64, 0, blk,
                                       pol_kv);
             }
           }
         }
-        // K chunk kc1 (slots 6, 7, 8; 7 and 8 are released after PV)
-        if (kc1 < 9) {
-          ok = sm100::mbar_wait_cluster(&kempty[kc1], par, abort);
-          if (!ok) break;
-          if (leader && kc1 % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[kc1 / 3], 2 * 3 * 8192);
-          sm100::tma_load_3d_pair(smem + pr::kKOff + kc1 * 8192, &tm_kv, &kfull[kc1 / 3], 0, kc1 * 64, 0,
-                                  block_of(own_key0), pol_kv);
-        }
+        // K chunk kc1 (slots 6, 7, 8)
+        if (kc1 < 9)   // the K slots were free already (same phase)
+          sm100::tma_load_3d_pair(smem + pr::kKOff + kc1 * 8192, &tm_kv, kfull, 0, kc1 * 64, 0, block_of(own_key0),
+                                  pol_kv);
       }
       if (!ok) {
         *abort = 1;
@@ -1010,79 +1014,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       if (leader) {
         if (pw == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
         const uint32_t last = (uint32_t)((n_tiles - 1) & 1);
-        if (kc0 % 3 == 0) sm100::mbar_wait_timeout(&kfull[kc0 / 3], last, sm100::kWaitTimeoutNs);
-        if (kc1 < 9 && kc1 % 3 == 0) sm100::mbar_wait_timeout(&kfull[kc1 / 3], last, sm100::kWaitTimeoutNs);
-        if (pw == 3 || pw == 5) sm100::mbar_wait_timeout(&vfull[pw == 5 ? 1 : 0], last, sm100::kWaitTimeoutNs);
+        if (pw == 0) sm100::mbar_wait_timeout(kfull, last, sm100::kWaitTimeoutNs);
+        if (pw == 3) sm100::mbar_wait_timeout(vfull, last, sm100::kWaitTimeoutNs);
       }
     } else if (warp == 0 && leader) {
       // ---------------------------------------------------------------- MMA
       // The whole warp runs the issue loop (descriptors stay warp-uniform) and
-      // one elected lane issues. The next chunk's barrier is probed before the
-      // current chunk's MMAs go out, so its latency overlaps the issue.
+      // one elected lane issues each product's MMAs back to back.
       constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, 256) | (1u << 16);   // B (V) MN-major
       const uint64_t d_q = desc_kmajor(smem_base + pr::kQOff);
       const uint64_t d_k = desc_kmajor(smem_base + pr::kKOff);
-      const uint64_t d_p = desc_kmajor(smem_base + pr::kKOff + 7 * 8192);
+      const uint64_t d_p0 = desc_kmajor(smem_base + pr::kPOff);          // P keys 0..63
+      const uint64_t d_p1 = desc_kmajor(smem_base + pr::kPOff + 8192);   // P keys 64..127
       const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
       auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
         return __all_sync(0xffffffffu, sm100::mbar_wait_cluster(bar, par, abort) ? 1 : 0) != 0;
-      };
-      auto landed = [&](uint64_t* bar, uint32_t par) -> bool {
-        return __all_sync(0xffffffffu, sm100::mbar_test_wait_cluster(bar, par) ? 1 : 0) != 0;
       };
       bool ok = wait_all(qbar, 0);
       auto issue_qk = [&](int i) -> bool {
         const int buf = i & 1;
         const uint32_t par = (uint32_t)(i & 1);
         if (!wait_all(&s_empty[buf], ((i >> 1) & 1) ^ 1u)) return false;
+        if (!wait_all(kfull, par)) return false;
+        sm100::tc_fence_after();
         const uint32_t d = tmem + pr::kColS + buf * 64;
-        bool ready = landed(&kfull[0], par);
+        if (sm100::elect_one()) {
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
-          if (c % 3 == 0) {   // chunks 3g .. 3g+2 land together
-            if (!ready && !wait_all(&kfull[c / 3], par)) return false;
-            sm100::tc_fence_after();
-            ready = c + 3 < 9 ? landed(&kfull[c / 3 + 1], par) : true;
-          }
-          if (sm100::elect_one()) {
+          for (int c = 0; c < 9; ++c) {
             const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
             sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
-            if (c < 7) sm100::tc_commit_pair_mc(&kempty[c], 3);
           }
-          __syncwarp();
+          sm100::tc_commit_pair_mc(kempty, 3);
+          sm100::tc_commit_pair_mc(&s_full[buf], 3);
         }
-        if (sm100::elect_one()) sm100::tc_commit_pair_mc(&s_full[buf], 3);
         __syncwarp();
         return true;
       };
       auto issue_pv = [&](int i) -> bool {
         const uint32_t par = (uint32_t)(i & 1);
         if (!wait_all(p_full, par)) return false;
-        bool ready = landed(&vfull[0], par);
+        if (!wait_all(vfull, par)) return false;
+        sm100::tc_fence_after();
+        if (sm100::elect_one()) {
 #pragma unroll 1
-        for (int kb = 0; kb < 2; ++kb) {
-          if (!ready && !wait_all(&vfull[kb], par)) return false;
-          sm100::tc_fence_after();
-          ready = kb == 0 ? landed(&vfull[1], par) : true;
-          if (sm100::elect_one()) {
+          for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, d_p + (uint64_t)(kb * 512 + kk * 2),
+                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
                                         d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
                                         (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
             }
-            sm100::tc_commit_pair_mc(&vempty[kb], 3);
           }
-          __syncwarp();
-        }
-        if (sm100::elect_one()) {
-          sm100::tc_commit_pair_mc(&kempty[7], 3);
-          sm100::tc_commit_pair_mc(&kempty[8], 3);
+          sm100::tc_commit_pair_mc(vempty, 3);
           sm100::tc_commit_pair_mc(o_done, 3);
         }
         __syncwarp();
