@@ -871,10 +871,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         *reinterpret_cast<uint4*>(pb + (((ch) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(pb + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
+      // Every writer makes its P stores visible to the async proxy, then the
+      // named barrier orders all of them before the one arrive; a release at
+      // cluster scope would add about a microsecond here (measured) without
+      // ordering anything the fence and the barrier have not.
       fence_async_smem();
       sm100::tc_fence_before();
       softmax_barrier();   // all of this CTA's P is written
-      if (st == 0 && ok) sm100::mbar_arrive_remote(p_full, 0);
+      if (st == 0 && ok) sm100::mbar_arrive_remote_relaxed(p_full, 0);
     }
     if (!ok && lane == 0) {
       *abort = 1;
@@ -1029,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       const uint64_t d_p1 = desc_kmajor(smem_base + pr::kPOff + 8192);   // P keys 64..127
       const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
       auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
-        return __all_sync(0xffffffffu, sm100::mbar_wait_cluster(bar, par, abort) ? 1 : 0) != 0;
+        return __all_sync(0xffffffffu, sm100::mbar_poll_cluster(bar, par, abort) ? 1 : 0) != 0;
       };
       bool ok = wait_all(qbar, 0);
       auto issue_qk = [&](int i) -> bool {

@@ -126,6 +126,22 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t p
   return ok != 0;
 }
 
+// mbar_wait_cluster for a phase that another SM completes, polled with the
+// non-suspending test_wait: a warp suspended in try_wait can wake late when
+// the completing arrive comes from another SM of the cluster.
+__device__ __forceinline__ bool mbar_poll_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(20);
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+
 // One lane of a converged warp (the MMA issue loops run on a whole warp so
 // that descriptors stay warp-uniform; one elected lane issues).
 __device__ __forceinline__ bool elect_one() {
