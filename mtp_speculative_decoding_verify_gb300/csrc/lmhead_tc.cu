@@ -237,63 +237,89 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else if (warp == 1 && (!kPair || leader)) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      constexpr uint32_t idesc = sm100::idesc_bf16_f32(kPair ? 2 * kTileV : kTileV, N);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int i = 0; i < my_tiles && ok; ++i) {
-        const int buf = i & 1;
-        const uint32_t acc_phase = (i >> 1) & 1;
-        const bool drained = kPair ? sm100::mbar_wait_cluster(&acc_empty[buf], acc_phase ^ 1u, abort)
-                                   : sm100::mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort);
-        if (!drained) {
-          abort_all(abort, p.err);
+    // The whole warp runs the loop (descriptors stay warp-uniform) and one
+    // elected lane issues. Two pipeline stages are waited for together and
+    // their eight MMAs go out back to back: every wait or tcgen05 fence in
+    // the issue stream costs the warp a few hundred clocks (measured), about
+    // the time of one stage's MMAs.
+    constexpr uint32_t idesc = sm100::idesc_bf16_f32(kPair ? 2 * kTileV : kTileV, N);
+    auto landed = [&](int st, uint32_t ph) -> bool {
+      const bool r = kPair ? sm100::mbar_poll_cluster(&full[st], ph, abort) : sm100::mbar_wait(&full[st], ph, abort);
+      return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int buf = i & 1;
+      const uint32_t acc_phase = (i >> 1) & 1;
+      const bool drained = kPair ? sm100::mbar_poll_cluster(&acc_empty[buf], acc_phase ^ 1u, abort)
+                                 : sm100::mbar_wait(&acc_empty[buf], acc_phase ^ 1u, abort);
+      if (!__all_sync(0xffffffffu, drained ? 1 : 0)) {
+        if (lane == 0) abort_all(abort, p.err);
+        break;
+      }
+      sm100::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * (p.tmem_cols / 2);
+      for (int k = 0; k < k_steps;) {
+        const int nk = k + 1 < k_steps ? 2 : 1;
+        int st2 = stage + 1;
+        uint32_t ph2 = phase;
+        if (st2 == p.stages) {
+          st2 = 0;
+          ph2 ^= 1u;
+        }
+        if (!landed(stage, phase) || (nk == 2 && !landed(st2, ph2))) {
+          if (lane == 0) abort_all(abort, p.err);
+          ok = false;
           break;
         }
         sm100::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * (p.tmem_cols / 2);
-        for (int k = 0; k < k_steps; ++k) {
-          const bool landed = kPair ? sm100::mbar_wait_cluster(&full[stage], phase, abort)
-                                    : sm100::mbar_wait(&full[stage], phase, abort);
-          if (!landed) {
-            abort_all(abort, p.err);
-            ok = false;
-            break;
-          }
-          sm100::tc_fence_after();
-          const uint32_t a_addr = sm100::smem_u32(smem + stage * L.stage_bytes + L.a_off);
-          const uint32_t b_addr = sm100::smem_u32(smem + stage * L.stage_bytes + L.b_off);
-          const uint64_t adesc = sm100::smem_desc_sw128_kmajor(a_addr);
-          const uint64_t bdesc = sm100::smem_desc_sw128_kmajor(b_addr);
+        if (sm100::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            // Advance 16 elements (32 B) along K inside the 128-B swizzled row.
-            if (kPair)
-              sm100::tc_mma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                      (k > 0 || kk > 0) ? 1u : 0u);
-            else
-              sm100::tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                                 (k > 0 || kk > 0) ? 1u : 0u);
+          for (int u = 0; u < 2; ++u) {
+            if (u < nk) {
+              const int su = u == 0 ? stage : st2;
+              const uint64_t adesc = sm100::smem_desc_sw128_kmajor(sm100::smem_u32(smem + su * L.stage_bytes + L.a_off));
+              const uint64_t bdesc = sm100::smem_desc_sw128_kmajor(sm100::smem_u32(smem + su * L.stage_bytes + L.b_off));
+#pragma unroll
+              for (int kk = 0; kk < kTileK / 16; ++kk) {
+                // Advance 16 elements (32 B) along K inside the 128-B swizzled row.
+                const uint32_t acc = (k + u > 0 || kk > 0) ? 1u : 0u;
+                if (kPair)
+                  sm100::tc_mma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, acc);
+                else
+                  sm100::tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, acc);
+              }
+              // stage free (in both CTAs of a pair) once these MMAs have read it
+              if (kPair) sm100::tc_commit_pair_mc(&empty[su], 3);
+              else sm100::tc_commit(&empty[su]);
+            }
           }
-          // stage free (in both CTAs of a pair) once these MMAs have read it
-          if (kPair) sm100::tc_commit_pair_mc(&empty[stage], 3);
-          else sm100::tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        for (int u = 0; u < nk; ++u)
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
-        }
-        if (ok) {
+        k += nk;
+      }
+      if (ok) {
+        if (sm100::elect_one()) {
           if (kPair) sm100::tc_commit_pair_mc(&acc_full[buf], 3);
           else sm100::tc_commit(&acc_full[buf]);
         }
+        __syncwarp();
       }
-      // Every MMA issued so far has completed before TMEM is released.
+    }
+    // Every MMA issued so far has completed before TMEM is released.
+    if (sm100::elect_one()) {
       if (kPair) sm100::tc_commit_pair_mc(final_bar, 3);
       else sm100::tc_commit(final_bar);
-      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
     }
+    __syncwarp();
+    sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
   } else if (warp == 1) {
     // pair, odd CTA: the even CTA's MMAs write this CTA's TMEM; wait for the
     // last one before the closing barriers.
@@ -375,7 +401,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       sm100::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (kPair) sm100::mbar_arrive_remote(&acc_empty[buf], 0);
+        if (kPair) sm100::mbar_arrive_remote_relaxed(&acc_empty[buf], 0);   // TMEM reads done: nothing to publish
         else sm100::mbar_arrive(&acc_empty[buf]);
       }
     }
