@@ -27,11 +27,13 @@ def lib():
         L.oracle_philox4x32_10.restype = None
         L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 8
         L.oracle_verify_attention.restype = i32
-        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7
+        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7 + [i32, ctypes.c_float]
         L.oracle_lmhead_accept.restype = i32
         L.oracle_kv_rollback.argtypes = [i32] * 4 + [P] * 5
         L.oracle_kv_rollback.restype = i32
         L.oracle_accept_prefix.argtypes = [i32, P, P, P, P]
+        L.oracle_relaxed_accept.argtypes = [i32, P, ctypes.c_float, i32, i32, ctypes.c_float, P]
+        L.oracle_relaxed_accept.restype = i32
         L.oracle_accept_prefix.restype = i32
         L.oracle_race.argtypes = [i32, P, P, P]
         L.oracle_race.restype = i32
@@ -113,7 +115,7 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *
 
 
 def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, want_logits=False,
-                  request_index=None):
+                  request_index=None, relaxed_topk=0, relaxed_delta=0.0):
     """LM head + row statistics + acceptance. Returns a dict of numpy arrays."""
     hidden, dt = _storage(hidden)
     lm_head, dt2 = _storage(lm_head)
@@ -134,7 +136,8 @@ def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, 
     rid = None if request_index is None else _c(request_index, np.int32)
     rc = lib().oracle_lmhead_accept(B, D, H, V, dt, _ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode),
                                     _ptr(temperature), _ptr(q_draft), ctypes.c_uint64(seed), _ptr(rid), _ptr(out_tokens),
-                                    _ptr(num_acc), _ptr(ties), _ptr(lse), _ptr(amax), _ptr(logits))
+                                    _ptr(num_acc), _ptr(ties), _ptr(lse), _ptr(amax), _ptr(logits),
+                                    int(relaxed_topk), ctypes.c_float(relaxed_delta))
     if rc != 0:
         raise ValueError("oracle_lmhead_accept returned %d" % rc)
     res = dict(out_tokens=out_tokens, num_accepted=num_acc, tie_flags=ties, lse=lse, argmax=amax)
@@ -153,3 +156,12 @@ def kv_rollback(block_table, seq_lens, num_accepted, free_list, free_count, *, D
                                   _ptr(free_list), _ptr(free_count))
     if rc != 0:
         raise ValueError("oracle_kv_rollback returned %d" % rc)
+
+
+def relaxed_accept(logits, lse, d, topk, delta):
+    """Relaxed acceptance of one row: (accepted 0/1, tie flag byte)."""
+    logits = _c(logits, np.float32)
+    tie = np.zeros(1, np.uint8)
+    r = lib().oracle_relaxed_accept(logits.size, _ptr(logits), ctypes.c_float(lse), int(d), int(topk),
+                                    ctypes.c_float(delta), _ptr(tie))
+    return int(r), int(tie[0])

@@ -19,6 +19,12 @@
  *                 with probability min(1, p/q)); at the first rejection draw
  *                 from normalised max(0, p_j - q_j); if all D are accepted
  *                 draw the bonus from p_D.
+ *       relaxed:  ("MTP in TensorRT-LLM", MTP optimization: relaxed
+ *                 acceptance) the candidates of row j are its top-N tokens
+ *                 by logit, minus those whose probability is below the top-1
+ *                 probability minus delta; d_{j+1} is accepted iff it is a
+ *                 candidate. The first miss is replaced by the argmax and the
+ *                 bonus is the argmax of row D, as for greedy requests.
  *     Every step emits n + 1 tokens, 1 .. D+1 ("MTP principles" stage 4).
  *  4. A categorical draw is an exponential race: argmax_v w_v / E_v with
  *     E_v ~ Exp(1) from the counter-based generator (philox.cpp); this picks
@@ -34,6 +40,33 @@
 #include "oracle_internal.h"
 
 static const float kTieRel = 1e-5f;
+static const float kRelaxedTieAbs = 1e-4f;    /* |p_d - (p_1 - delta)| below this: flagged */
+static const float kRelaxedRankEps = 1e-3f;   /* logit band (x (1 + |l_d|)) for an unstable rank */
+
+extern "C" int oracle_relaxed_accept(int V, const float* logits, float lse, int d, int topk, float delta,
+                                     uint8_t* tie) {
+  const float ld = logits[d];
+  /* Rank of d: the tokens ordered before it (larger logit, or equal logit
+   * and lower index). Also count the tokens that are surely above it and
+   * those that might be, within a band around l_d. */
+  const float eps = kRelaxedRankEps * (1.0f + fabsf(ld));
+  int before = 0, surely_above = 0, maybe_above = 0;
+  int top = 0;
+  for (int v = 0; v < V; ++v) {
+    if (logits[v] > logits[top]) top = v;
+    if (v == d) continue;
+    if (logits[v] > ld || (logits[v] == ld && v < d)) ++before;
+    if (logits[v] > ld + eps) ++surely_above;
+    if (logits[v] >= ld - eps) ++maybe_above;
+  }
+  const int in_top = before < topk;
+  if (surely_above < topk && maybe_above >= topk) *tie |= 1;
+  const float pd = expf(ld - lse);
+  const float thr = expf(logits[top] - lse) - delta;
+  /* (The top-1 token itself meets the probability condition exactly.) */
+  if (d != top && fabsf(pd - thr) < kRelaxedTieAbs) *tie |= 1;
+  return in_top && pd >= thr;
+}
 
 extern "C" int oracle_accept_prefix(int D, const float* p, const float* q, const float* U, uint8_t* tie) {
   int n = 0;
@@ -74,8 +107,10 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                                     uint64_t seed, const int32_t* request_index,
                                     int32_t* out_tokens, int32_t* num_accepted,
                                     uint8_t* tie_flags, float* lse_out,
-                                    int32_t* argmax_out, float* logits_out) {
+                                    int32_t* argmax_out, float* logits_out,
+                                    int relaxed_topk, float relaxed_delta) {
   if (B < 0 || D < 0 || H <= 0 || V <= 0 || (dtype != 0 && dtype != 1)) return ORACLE_BAD_ARG;
+  if (relaxed_delta < 0.0f) return ORACLE_BAD_ARG;
   const int R = D + 1;
   std::vector<float> logits((size_t)R * V);
   std::vector<float> lse(R);
@@ -89,7 +124,9 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
     }
     const uint32_t rid = request_index ? (uint32_t)request_index[b] : (uint32_t)b;
     const bool sampling = mode[b] == 1 && temperature != NULL && temperature[b] > 0.0f;
+    const bool relaxed = mode[b] == 2;
     if (sampling && q_draft == NULL) return ORACLE_BAD_ARG;
+    if (relaxed && relaxed_topk < 1) return ORACLE_BAD_ARG;
     const float inv_t = sampling ? 1.0f / temperature[b] : 1.0f;
 
     /* Steps 1-2 for the R rows of request b. */
@@ -127,7 +164,14 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
     for (int j = 0; j < R; ++j) out[j] = -1;
     uint8_t tie = 0;
     int n;
-    if (!sampling) {
+    if (relaxed) {
+      n = 0;
+      while (n < D && oracle_relaxed_accept(V, &logits[(size_t)n * V], lse[n], tok[n + 1], relaxed_topk,
+                                            relaxed_delta, &tie))
+        ++n;
+      for (int j = 0; j < n; ++j) out[j] = tok[j + 1];
+      out[n] = amax[n];
+    } else if (!sampling) {
       n = 0;
       while (n < D && amax[n] == tok[n + 1]) ++n;
       for (int j = 0; j < n; ++j) out[j] = tok[j + 1];

@@ -71,16 +71,26 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
  * [SDMTP] §2.3, §4.4).
  *   hidden [B*R, H], lm_head [V, H] (dtype), tokens [B, R] = [input, d1..dD]
  *   mode [B]: 0 greedy, 1 rejection sampling (a request with mode 1 and
- *   temperature <= 0 is decided greedily: the T -> 0 limit)
+ *   temperature <= 0 is decided greedily: the T -> 0 limit), 2 relaxed
+ *   acceptance ([TRT] "MTP optimization: relaxed acceptance", Fig. 6): draft
+ *   d of row j is accepted iff d is among the row's relaxed_topk largest
+ *   logits (lowest index first on equal logits) and its probability is at
+ *   least the top-1 probability minus relaxed_delta (p = softmax of the
+ *   logits, T = 1); the first miss is replaced by the row's argmax and the
+ *   bonus is the argmax of row D, as for greedy requests
  *   temperature [B] (may be NULL when every request is greedy)
  *   q_draft [B, D, V] fp32 (may be NULL when every request is greedy)
  *   request_index [B]: the request number used as counter word 0 of the
  *   random stream (NULL: 0 .. B-1), so that a subset of a batch draws the
  *   same numbers as the full batch
+ *   relaxed_topk, relaxed_delta: the relaxed rule's N (>= 1 when a request
+ *   has mode 2) and delta (>= 0)
  * Outputs: out_tokens [B, R] (-1 padded), num_accepted [B] (drafts accepted,
  * 0..D; emitted = num_accepted + 1), tie_flags [B] (bit0: |p - U q| < 1e-5 q
- * at a decision; bit1: top-2 race keys within 1e-5 relative), and optional
- * lse_out [B, R], argmax_out [B, R], logits_out [B*R, V] (fp32, / T). */
+ * at a decision, or for a relaxed decision |p_d - (p_1 - delta)| < 1e-4 or a
+ * draft rank that moves across N when its logit moves by 1e-3 (1 + |l_d|);
+ * bit1: top-2 race keys within 1e-5 relative), and optional lse_out [B, R],
+ * argmax_out [B, R], logits_out [B*R, V] (fp32, / T). */
 int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                          const void* hidden, const void* lm_head,
                          const int32_t* tokens, const uint8_t* mode,
@@ -88,7 +98,8 @@ int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                          uint64_t seed, const int32_t* request_index,
                          int32_t* out_tokens, int32_t* num_accepted,
                          uint8_t* tie_flags, float* lse_out,
-                         int32_t* argmax_out, float* logits_out);
+                         int32_t* argmax_out, float* logits_out,
+                         int relaxed_topk, float relaxed_delta);
 
 /* KV-cache rollback ([TRT] "MTP Vanilla"/"MTP Eagle": KV of discarded drafts
  * is cleared; [K3] "rollback keeps the correct prefix").
@@ -102,6 +113,14 @@ int oracle_kv_rollback(int B, int D, int block_size, int max_blocks,
                        int32_t* free_list, int32_t* free_count);
 
 /* Pieces of the acceptance rule exposed for pinning with fixed inputs. */
+
+/* Relaxed acceptance of one row ([TRT] "MTP optimization: relaxed
+ * acceptance"): logits [V] of the row (binary32), its log-sum-exp, the draft
+ * token d. Returns 1 iff d is among the topk largest logits (lowest index
+ * first on equal logits) and expf(l_d - lse) >= expf(l_max - lse) - delta,
+ * both decided in binary32; *tie gets bit0 as described above. */
+int oracle_relaxed_accept(int V, const float* logits, float lse, int d, int topk, float delta,
+                          uint8_t* tie);
 
 /* Rejection-sampling prefix rule ([VLLM] §三 stage 3, [SDMTP] §4.4):
  * accept draft j iff p[j] >= U[j] * q[j]; stop at the first failure.
