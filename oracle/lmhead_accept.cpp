@@ -40,7 +40,7 @@
 #include "oracle_internal.h"
 
 static const float kTieRel = 1e-5f;
-static const float kRelaxedTieAbs = 1e-4f;    /* |p_d - (p_1 - delta)| below this: flagged */
+static const float kRelaxedTieAbs = 1e-3f;    /* |p_d - (p_1 - delta)| below this: flagged */
 static const float kRelaxedRankEps = 1e-3f;   /* logit band (x (1 + |l_d|)) for an unstable rank */
 
 extern "C" int oracle_relaxed_accept(int V, const float* logits, float lse, int d, int topk, float delta,

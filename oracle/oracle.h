@@ -87,7 +87,7 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
  *   has mode 2) and delta (>= 0)
  * Outputs: out_tokens [B, R] (-1 padded), num_accepted [B] (drafts accepted,
  * 0..D; emitted = num_accepted + 1), tie_flags [B] (bit0: |p - U q| < 1e-5 q
- * at a decision, or for a relaxed decision |p_d - (p_1 - delta)| < 1e-4 or a
+ * at a decision, or for a relaxed decision |p_d - (p_1 - delta)| < 1e-3 or a
  * draft rank that moves across N when its logit moves by 1e-3 (1 + |l_d|);
  * bit1: top-2 race keys within 1e-5 relative), and optional lse_out [B, R],
  * argmax_out [B, R], logits_out [B*R, V] (fp32, / T). */

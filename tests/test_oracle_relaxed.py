@@ -50,7 +50,7 @@ def test_brute_force_sort_definition():
             delta = float(rng.choice([0.0, 0.05, 0.3, 0.6, 1.0]))
             acc, tie = oracle.relaxed_accept(lg, lse, d, N, delta)
             margin = abs(p[d] - (p.max() - delta))
-            if tie or margin < 1e-4:
+            if tie or margin < 1e-3:
                 continue
             want = int(d in order[:N] and p[d] >= p.max() - delta)
             assert acc == want, (V, d, N, delta)
