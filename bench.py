@@ -45,6 +45,9 @@ def workloads():
     return {
         "cfg1_D3": synth.CFG1,
         "cfg1_D1": synth.CFG1.with_(D=1),
+        # Relaxed acceptance (top-10, delta 0.6) on the DeepSeek-V3-shaped step.
+        "cfg1_D3_relaxed": synth.CFG1.with_(name=synth.CFG1.name + ", relaxed acceptance N=10 delta=0.6",
+                                            relaxed="all", relaxed_topk=10, relaxed_delta=0.6),
         "cfg0": synth.CFG0,
         "cfg2": synth.CFG2,
         "cfg3": synth.CFG3,
@@ -166,7 +169,8 @@ class Step:
         self.a_attn = B.attn_args(att["q"], att["k_new"], att["v_new"], att["k_cache"], att["v_cache"],
                                   att["block_table"], att["ctx_lens"], self.out, sm_scale=w.sm_scale)
         self.a_lm = B.lm_args(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
-                              lm["q_draft"], lm["seed"], self.out_tokens, self.num_acc, self.ties)
+                              lm["q_draft"], lm["seed"], self.out_tokens, self.num_acc, self.ties,
+                              relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta)
         self.a_rb = B.rollback_args(self.table_work, self.seq, self.num_acc, self.free_list, self.free_count, D=w.D)
         self.launches = 0
 

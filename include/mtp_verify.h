@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MTP_ABI_VERSION 1
+#define MTP_ABI_VERSION 2
 
 typedef enum {
   MTP_OK = 0,
@@ -77,6 +77,7 @@ typedef enum { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
 #define MTP_ERR_ACCEPTED   0x8u  /* num_accepted outside [0, D] */
 #define MTP_ERR_FREE_LIST  0x10u /* free list capacity exceeded */
 #define MTP_ERR_TIMEOUT    0x20u /* a bounded wait inside a kernel gave up */
+#define MTP_ERR_MODE       0x40u /* mode > 2, or mode 2 while relaxed_topk is 0 (decided greedily) */
 
 /* ------------------------------------------------------------------------ */
 /* 1. Verify attention with KV append.
@@ -150,6 +151,12 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  *   greedy request (mode 0, or mode 1 with temperature <= 0):
  *     n = number of leading j < D with argmax(row j) == tokens[b, j+1];
  *     out_tokens[b] = [d_1 .. d_n, argmax(row n)].
+ *   relaxed request (mode 2; "MTP in TensorRT-LLM on Blackwell", MTP
+ *   optimization: relaxed acceptance, used in a reasoning model's thinking
+ *   phase): p_j = softmax(l_j) (no temperature). Draft d_{j+1} is accepted
+ *   iff it is among the relaxed_topk largest logits of row j (lowest id first
+ *   on equal logits) and p_j(d_{j+1}) >= max_v p_j(v) - relaxed_delta; stop
+ *   at the first miss; out_tokens[b] = [d_1 .. d_n, argmax(row n)].
  *   rejection-sampling request (mode 1, temperature > 0):
  *     p_j = softmax(l_j / T). For j = 0 .. D-1: accept d_{j+1} iff
  *     p_j(d_{j+1}) >= U_j * q[b, j, d_{j+1}] (U_j uniform in [0,1)), stop at
@@ -165,7 +172,7 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  * Layouts:
  *   hidden      [B*R, H]   dtype;   lm_head [V, H] dtype (row v = token v)
  *   tokens      [B, R] int32 = [input/bonus, d_1 .. d_D]
- *   mode        [B] uint8 (0 greedy, 1 rejection sampling)
+ *   mode        [B] uint8 (0 greedy, 1 rejection sampling, 2 relaxed)
  *   temperature [B] float (NULL allowed when no request samples)
  *   q_draft     [B, D, V] float, the drafter's distributions (NULL allowed
  *               when no request samples); only rows of sampling requests
@@ -174,7 +181,10 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  *   out_tokens   [B, R] int32: n+1 emitted tokens then -1
  *   num_accepted [B] int32: n in [0, D] (tokens emitted = n + 1)
  *   tie_flags    [B] uint8: bit0 = an accept decision had |p - U q| < 1e-5 q,
- *                bit1 = the two best race keys were within 1e-5 relative
+ *                or a relaxed decision had |p_d - (p_1 - delta)| < 1e-3 or a
+ *                rank that crosses relaxed_topk when l_d moves by
+ *                1e-3 (1 + |l_d|); bit1 = the two best race keys were within
+ *                1e-5 relative
  *   lse_out      [B*R] float (optional): log-sum-exp of row (scaled) logits
  *   argmax_out   [B*R] int32 (optional): argmax of row, lowest id on ties
  *   logits_debug [B*R, V] float (optional, validation only): scaled logits
@@ -197,6 +207,8 @@ typedef struct {
   int32_t B, D, H, V;
   int32_t dtype;             /* mtp_dtype */
   int32_t any_sampling;      /* 0: every request is greedy (q_draft/temperature unused) */
+  int32_t relaxed_topk;      /* N of the relaxed rule (0: no request uses mode 2), <= V */
+  float relaxed_delta;       /* delta of the relaxed rule, >= 0 */
   void* workspace;           /* device, >= mtp_lmhead_workspace_size() bytes */
   size_t workspace_bytes;
   void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just

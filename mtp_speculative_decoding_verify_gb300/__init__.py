@@ -10,5 +10,6 @@ from ._binding import (  # noqa: F401
     lib,
     mtp_verify_attention,
     mtp_verify_logits_accept,
+    mtp_verify_logits_accept_noalloc,
     sync_status,
 )

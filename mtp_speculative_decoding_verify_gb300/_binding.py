@@ -14,6 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libmtpverify.so")
 
 MTP_OK, MTP_INVALID_ARG, MTP_UNSUPPORTED, MTP_CUDA_ERROR, MTP_DEVICE_ERROR = range(5)
+ABI_VERSION = 2   # MTP_ABI_VERSION of the header the structs below mirror
 MTP_F32, MTP_BF16 = 0, 1
 MAX_DRAFTS = 15
 BLOCK_SIZE = 64
@@ -36,6 +37,7 @@ class LmArgs(ctypes.Structure):
                 ("q_draft", _P), ("seed", ctypes.c_uint64), ("out_tokens", _P), ("num_accepted", _P),
                 ("tie_flags", _P), ("lse_out", _P), ("argmax_out", _P), ("logits_debug", _P),
                 ("B", _I), ("D", _I), ("H", _I), ("V", _I), ("dtype", _I), ("any_sampling", _I),
+                ("relaxed_topk", _I), ("relaxed_delta", ctypes.c_float),
                 ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
 
 
@@ -91,6 +93,8 @@ def lib():
         L.mtp_abi_version.restype = ctypes.c_int
         L.mtp_abi_struct_size.argtypes = [ctypes.c_int]
         L.mtp_abi_struct_size.restype = ctypes.c_size_t
+        if L.mtp_abi_version() != ABI_VERSION:
+            raise RuntimeError("library ABI version %d, binding expects %d" % (L.mtp_abi_version(), ABI_VERSION))
         for which, st in enumerate((AttnArgs, LmArgs, RollbackArgs)):
             if L.mtp_abi_struct_size(which) != ctypes.sizeof(st):
                 raise RuntimeError("ABI mismatch for %s" % st.__name__)
@@ -197,7 +201,7 @@ def mtp_verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_len
 
 
 def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
-            lse_out=None, argmax_out=None, logits_debug=None, workspace=None):
+            lse_out=None, argmax_out=None, logits_debug=None, workspace=None, relaxed_topk=0, relaxed_delta=0.0):
     """Fill LmArgs from tensors (see mtp_verify_logits_accept for shapes)."""
     B, R = tokens.shape
     D = R - 1
@@ -218,7 +222,8 @@ def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_token
     _dev(logits_debug, "logits_debug", torch.float32, (B * R, V))
     a = LmArgs(_ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode), _ptr(temperature), _ptr(q_draft),
                int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_tokens), _ptr(num_accepted), _ptr(tie_flags), _ptr(lse_out),
-               _ptr(argmax_out), _ptr(logits_debug), B, D, H, V, _dtype_code(lm_head), int(any_sampling), None, 0)
+               _ptr(argmax_out), _ptr(logits_debug), B, D, H, V, _dtype_code(lm_head), int(any_sampling),
+               int(relaxed_topk), float(relaxed_delta), None, 0)
     n = lib().mtp_lmhead_workspace_size(ctypes.byref(a))
     if n == 0:
         _check(MTP_INVALID_ARG)
@@ -231,22 +236,22 @@ def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_token
 
 def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted,
                              tie_flags, lse_out=None, argmax_out=None, logits_debug=None, workspace=None,
-                             stream=None):
-    """LM head + streaming softmax statistics + greedy / rejection-sampling acceptance.
+                             stream=None, relaxed_topk=0, relaxed_delta=0.0):
+    """LM head + streaming softmax statistics + greedy / rejection-sampling / relaxed acceptance.
 
     hidden [B*R, H], lm_head [V, H] (float32 or bfloat16), tokens [B, R] int32, mode [B] uint8,
     temperature [B] float32 or None, q_draft [B, D, V] float32 or None (None: every request greedy),
     outputs out_tokens [B, R] int32, num_accepted [B] int32, tie_flags [B] uint8, optional lse_out / argmax_out
-    [B, R] and logits_debug [B*R, V].
+    [B, R] and logits_debug [B*R, V]. relaxed_topk / relaxed_delta: the relaxed rule of mode-2 requests.
     """
     a = lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
-                lse_out, argmax_out, logits_debug, workspace)
+                lse_out, argmax_out, logits_debug, workspace, relaxed_topk, relaxed_delta)
     _check(lib().mtp_verify_logits_accept(ctypes.byref(a), _stream_handle(stream)))
 
 
 def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens,
                                      num_accepted, tie_flags, lse_out=None, argmax_out=None, logits_debug=None,
-                                     stream=None):
+                                     stream=None, relaxed_topk=0, relaxed_delta=0.0):
     """mtp_verify_logits_accept for callers that cannot allocate device memory:
     the scratch lives in a fixed array owned by the library (no workspace is
     allocated or passed). Raises MtpError if the batch needs more scratch
@@ -254,7 +259,8 @@ def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature,
     a = LmArgs(_ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode), _ptr(temperature), _ptr(q_draft),
                int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_tokens), _ptr(num_accepted), _ptr(tie_flags), _ptr(lse_out),
                _ptr(argmax_out), _ptr(logits_debug), tokens.shape[0], tokens.shape[1] - 1, lm_head.shape[1],
-               lm_head.shape[0], _dtype_code(lm_head), int(q_draft is not None), None, 0)
+               lm_head.shape[0], _dtype_code(lm_head), int(q_draft is not None), int(relaxed_topk),
+               float(relaxed_delta), None, 0)
     for t, n in ((hidden, "hidden"), (lm_head, "lm_head"), (tokens, "tokens"), (mode, "mode"),
                  (temperature, "temperature"), (q_draft, "q_draft"), (out_tokens, "out_tokens"),
                  (num_accepted, "num_accepted"), (tie_flags, "tie_flags"), (lse_out, "lse_out"),

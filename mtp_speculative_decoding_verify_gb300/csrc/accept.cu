@@ -11,7 +11,10 @@
 // probability; §4.4: accept with probability min(1, p/q), and at temperature
 // 0 accept only when argmax(p) is the draft, replacing it otherwise.
 // "MTP in TensorRT-LLM" Fig. 1: when every draft is accepted the target's
-// own next token is accepted too (the bonus).
+// own next token is accepted too (the bonus). Relaxed requests ("MTP in
+// TensorRT-LLM on Blackwell", MTP optimization: relaxed acceptance): a draft
+// is accepted while it ranks among the row's relaxed_topk largest logits and
+// p(d) >= p(top-1) - relaxed_delta; the first miss is replaced by the argmax.
 //
 // The redraw uses the residual max(0, p - q) (normalised) so that the
 // emitted tokens follow p exactly; a categorical draw is an exponential race
@@ -47,13 +50,18 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
     int any_sampling, uint64_t seed, int B, int D, int V, float* __restrict__ ws_lse, int* __restrict__ ws_amax,
     Decision* __restrict__ dec, int* __restrict__ race_count, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ num_accepted, uint8_t* __restrict__ tie_flags, float* __restrict__ lse_out,
-    int32_t* __restrict__ argmax_out, unsigned* err) {
+    int32_t* __restrict__ argmax_out, const int* __restrict__ rcnt, int relaxed_topk, float relaxed_delta,
+    unsigned* err) {
   __shared__ float s_lse[kMaxRows];
+  __shared__ float s_top[kMaxRows];
   __shared__ int s_amax[kMaxRows];
+  __shared__ int s_cnt[kMaxRows][3];
   const int b = blockIdx.x;
   const int R = D + 1;
   const int M = B * R;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  const int md = mode[b];
+  const bool relaxed = md == 2 && relaxed_topk > 0;
 
   for (int j = warp; j < R; j += kWarps) {
     const int m = b * R + j;
@@ -63,9 +71,31 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
       st = rowstat_merge(st, RowStat{pmax[o], psum[o], pbest[o], pidx[o]});
     }
     st = warp_merge(st);
+    if (relaxed && j < D) {   // the draft's rank counts, summed over the LM head's slices
+      const int64_t plane = (int64_t)slices * M;
+      int c0 = 0, c1 = 0, c2 = 0;
+      for (int sl = lane; sl < slices; sl += kWarp) {
+        const int64_t o = (int64_t)sl * M + m;
+        c0 += rcnt[o];
+        c1 += rcnt[plane + o];
+        c2 += rcnt[2 * plane + o];
+      }
+#pragma unroll
+      for (int off = kWarp / 2; off > 0; off >>= 1) {
+        c0 += __shfl_xor_sync(0xffffffffu, c0, off);
+        c1 += __shfl_xor_sync(0xffffffffu, c1, off);
+        c2 += __shfl_xor_sync(0xffffffffu, c2, off);
+      }
+      if (lane == 0) {
+        s_cnt[j][0] = c0;
+        s_cnt[j][1] = c1;
+        s_cnt[j][2] = c2;
+      }
+    }
     if (lane == 0) {
       const float lse = st.m + logf(st.s);
       s_lse[j] = lse;
+      s_top[j] = st.best;
       s_amax[j] = st.idx;
       ws_lse[m] = lse;
       ws_amax[m] = st.idx;
@@ -81,9 +111,21 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
   bool bad = false;
   for (int j = 0; j < R; ++j) bad |= (tok[j] < 0 || tok[j] >= V);
   if (bad) raise_error(err, MTP_ERR_TOKEN_ID);
-  const bool sampling = any_sampling && mode[b] == 1 && temperature[b] > 0.0f;
+  if (md > 2 || (md == 2 && !relaxed)) raise_error(err, MTP_ERR_MODE);   // decided greedily
+  const bool sampling = any_sampling && md == 1 && temperature[b] > 0.0f;
   int n = 0, tie = 0;
-  if (!sampling || bad) {
+  if (relaxed && !bad) {
+    for (; n < D; ++n) {
+      const int d = tok[n + 1];
+      const int before = s_cnt[n][0], sure = s_cnt[n][1], maybe = s_cnt[n][2];
+      if (sure < relaxed_topk && maybe >= relaxed_topk) tie |= 1;
+      const float pd = expf(ldraft[b * R + n] - s_lse[n]);
+      const float thr = expf(s_top[n] - s_lse[n]) - relaxed_delta;
+      if (d != s_amax[n] && fabsf(pd - thr) < kRelaxedTieAbs) tie |= 1;
+      if (!(before < relaxed_topk && pd >= thr)) break;
+    }
+    for (int j = 0; j < R; ++j) out[j] = j < n ? tok[j + 1] : (j == n ? s_amax[n] : -1);
+  } else if (!sampling || bad) {
     while (!bad && n < D && s_amax[n] == tok[n + 1]) ++n;
     for (int j = 0; j < R; ++j) out[j] = j < n ? tok[j + 1] : (j == n ? s_amax[n] : -1);
   } else {
@@ -188,7 +230,8 @@ cudaError_t launch_accept(const mtp_lmhead_args& a, const LmPlan& p, unsigned* e
       (const int*)(ws + p.off_pidx), (const float*)(ws + p.off_ldraft), p.slices, a.tokens, a.mode, a.temperature,
       a.q_draft, a.any_sampling, a.seed, a.B, a.D, a.V, (float*)(ws + p.off_lse), (int*)(ws + p.off_amax),
       (Decision*)(ws + p.off_dec), (int*)(ws + p.off_count), a.out_tokens, a.num_accepted, a.tie_flags, a.lse_out,
-      a.argmax_out, err);
+      a.argmax_out, a.relaxed_topk > 0 ? (const int*)(ws + p.off_rcnt) : nullptr, a.relaxed_topk, a.relaxed_delta,
+      err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.any_sampling) return e;
   dim3 grid(a.B, p.race_slices);

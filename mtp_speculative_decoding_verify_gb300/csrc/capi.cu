@@ -124,6 +124,10 @@ int check_lm(const mtp_lmhead_args* a) {
     return fail(MTP_INVALID_ARG, "a required pointer is NULL");
   if (a->any_sampling && a->B > 0 && (!a->q_draft || !a->temperature))
     return fail(MTP_INVALID_ARG, "any_sampling = 1 needs q_draft and temperature");
+  if (a->relaxed_topk < 0 || a->relaxed_topk > a->V)
+    return fail(MTP_INVALID_ARG, "relaxed_topk = %d outside [0, V]", a->relaxed_topk);
+  if (a->relaxed_topk > 0 && !(a->relaxed_delta >= 0.0f && a->relaxed_delta <= 1e30f))
+    return fail(MTP_INVALID_ARG, "relaxed_delta must be finite and >= 0");
   return MTP_OK;
 }
 
@@ -164,6 +168,13 @@ mtp::LmPlan mtp::plan_lmhead(const mtp_lmhead_args& a, int sm_count) {
   p.off_count = off; off += align256((size_t)a.B * 4);
   p.off_logits = off;
   if (a.any_sampling) off += align256((size_t)p.M * a.V * 4);
+  p.off_lpre = off;
+  p.off_rcnt = off;
+  if (a.relaxed_topk > 0) {
+    off += align256((size_t)p.M * 4);
+    p.off_rcnt = off;
+    off += align256((size_t)3 * p.slices * p.M * 4);
+  }
   p.ws_bytes = off;
   return p;
 }
@@ -252,14 +263,15 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
     return fail(MTP_INVALID_ARG, "workspace of %zu bytes needed, %zu given", p.ws_bytes, a->workspace_bytes);
   if (((uintptr_t)a->workspace) % 256) return fail(MTP_INVALID_ARG, "workspace must be 256-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = record(a->timing_events[0], s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  cudaError_t e = mtp::launch_relaxed_prepass(*a, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "relaxed pre-pass launch");
+  if ((e = record(a->timing_events[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = p.tc ? mtp::launch_lmhead_tc(*a, p, c->err, s) : mtp::launch_lmhead_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM head launch");
   if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_accept(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");
-  g_launches = 2 + (a->any_sampling ? 1 : 0);
+  g_launches = 2 + (a->any_sampling ? 1 : 0) + (a->relaxed_topk > 0 ? 1 : 0);
   return MTP_OK;
 }
 
@@ -309,10 +321,11 @@ int mtp_sync_status(void* stream) {
   if (word == 0) return MTP_OK;
   e = cudaMemset(c->err, 0, sizeof word);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
-  return fail(MTP_DEVICE_ERROR, "device range check failed: 0x%x%s%s%s%s%s%s", word,
+  return fail(MTP_DEVICE_ERROR, "device range check failed: 0x%x%s%s%s%s%s%s%s", word,
               (word & MTP_ERR_BLOCK_ID) ? " block-id" : "", (word & MTP_ERR_TOKEN_ID) ? " token-id" : "",
               (word & MTP_ERR_LENGTH) ? " length" : "", (word & MTP_ERR_ACCEPTED) ? " num-accepted" : "",
-              (word & MTP_ERR_FREE_LIST) ? " free-list" : "", (word & MTP_ERR_TIMEOUT) ? " timeout" : "");
+              (word & MTP_ERR_FREE_LIST) ? " free-list" : "", (word & MTP_ERR_TIMEOUT) ? " timeout" : "",
+              (word & MTP_ERR_MODE) ? " mode" : "");
 }
 
 }  // extern "C"

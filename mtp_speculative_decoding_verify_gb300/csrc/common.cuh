@@ -78,6 +78,25 @@ __device__ __forceinline__ RowStat warp_merge(RowStat v) {
   return v;
 }
 
+// Relaxed acceptance ("MTP in TensorRT-LLM on Blackwell", MTP optimization:
+// relaxed acceptance): rank counts of draft d (logit lp) over the logits l of the
+// vocabulary entries v a CTA sees: cnt[0] entries ordered before d (larger
+// logit, or equal logit and lower id), cnt[1] entries surely above it
+// (l > lp + eps), cnt[2] entries that may be above it (l >= lp - eps), with
+// eps = kRelaxedRankEps (1 + |lp|). A decision is a near-tie when
+// cnt[1] < N <= cnt[2], or when |p_d - (p_1 - delta)| < kRelaxedTieAbs for a
+// draft that is not the top-1 token.
+constexpr float kRelaxedRankEps = 1e-3f;
+constexpr float kRelaxedTieAbs = 1e-3f;
+
+__device__ __forceinline__ void relaxed_count(float l, int v, float lp, int d, float eps, int& before, int& sure,
+                                              int& maybe) {
+  if (v == d) return;
+  before += (l > lp || (l == lp && v < d)) ? 1 : 0;
+  sure += l > lp + eps ? 1 : 0;
+  maybe += l >= lp - eps ? 1 : 0;
+}
+
 // Top-2 of an exponential race: best key k1 at index i1, runner-up key k2.
 struct Race {
   float k1;

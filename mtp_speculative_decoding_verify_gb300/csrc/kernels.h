@@ -44,6 +44,8 @@ struct LmPlan {
   size_t off_race;                                 // [B][race_slices] race partials (2 x Race)
   size_t off_count;                                // [B] int arrival counters
   size_t off_logits;                               // [M][V] float, sampling rows only
+  size_t off_lpre;                                 // [M] float: draft logit of relaxed rows (pre-pass)
+  size_t off_rcnt;                                 // [3][slices][M] int: relaxed rank counts per slice
   size_t ws_bytes;
 };
 
@@ -51,6 +53,7 @@ LmPlan plan_lmhead(const mtp_lmhead_args& a, int sm_count);
 cudaError_t launch_lmhead_simt(const mtp_lmhead_args& a, const LmPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_accept(const mtp_lmhead_args& a, const LmPlan& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_relaxed_prepass(const mtp_lmhead_args& a, const LmPlan& p, cudaStream_t s);
 
 // ----------------------------------------------------------------- rollback
 cudaError_t launch_rollback(const mtp_rollback_args& a, unsigned* err, cudaStream_t s);

@@ -31,13 +31,14 @@ __global__ void __launch_bounds__(kThreads) lmhead_simt_kernel(
     const uint8_t* __restrict__ mode, const float* __restrict__ temperature, int any_sampling, int M, int R, int H,
     int V, int tiles_per_slice, float* __restrict__ pmax, float* __restrict__ psum, float* __restrict__ pbest,
     int* __restrict__ pidx, float* __restrict__ ldraft, float* __restrict__ samp_logits,
-    float* __restrict__ logits_debug) {
+    float* __restrict__ logits_debug, const float* __restrict__ lpre, int* __restrict__ rcnt, int slices) {
   __shared__ float Hs[kMR][kKC + 1];
   __shared__ float Ws[kTV][kKC + 1];
   __shared__ float Lt[kMR][kTV + 1];
   __shared__ float s_inv_t[kMR];
   __shared__ int s_draft[kMR];
   __shared__ int s_samp[kMR];
+  __shared__ float s_lpre[kMR];
 
   const int tid = threadIdx.x;
   const int slice = blockIdx.x;
@@ -61,8 +62,10 @@ __global__ void __launch_bounds__(kThreads) lmhead_simt_kernel(
     s_inv_t[tid] = inv_t;
     s_draft[tid] = draft;
     s_samp[tid] = samp;
+    s_lpre[tid] = (lpre && m < M) ? lpre[m] : __int_as_float(0x7fc00000);
   }
   RowStat st = rowstat_empty();
+  int cnt0 = 0, cnt1 = 0, cnt2 = 0;   // relaxed rank counts of the row of thread tid
 
   const int c = tid % kWarp;        // vocab column of this thread
   const int rbase = tid / kWarp;    // rows rbase + 8 i
@@ -117,6 +120,11 @@ __global__ void __launch_bounds__(kThreads) lmhead_simt_kernel(
       st = rowstat_merge(st, RowStat{cmax, csum, cmax, v0 + cidx});
       const int d = s_draft[tid];
       if (d >= v0 && d < v0 + nv) ldraft[row0 + tid] = Lt[tid][d - v0];
+      const float lp = s_lpre[tid];
+      if (lp == lp) {   // relaxed row
+        const float eps = kRelaxedRankEps * (1.0f + fabsf(lp));
+        for (int x = 0; x < nv; ++x) relaxed_count(Lt[tid][x], v0 + x, lp, d, eps, cnt0, cnt1, cnt2);
+      }
     }
     // Rows that sample (and the optional debug copy) keep the full logits.
     for (int e = tid; e < kMR * kTV; e += kThreads) {
@@ -134,6 +142,12 @@ __global__ void __launch_bounds__(kThreads) lmhead_simt_kernel(
     psum[o] = st.s;
     pbest[o] = st.best;
     pidx[o] = st.idx;
+    if (rcnt) {
+      const int64_t plane = (int64_t)slices * M;
+      rcnt[o] = cnt0;
+      rcnt[plane + o] = cnt1;
+      rcnt[2 * plane + o] = cnt2;
+    }
   }
 }
 
@@ -148,7 +162,8 @@ cudaError_t launch_lmhead_simt(const mtp_lmhead_args& a, const LmPlan& p, unsign
 #define MTP_SIMT_ARGS                                                                                          \
   a.tokens, a.mode, a.temperature, a.any_sampling, p.M, R, a.H, a.V, tps, (float*)(ws + p.off_pmax),          \
       (float*)(ws + p.off_psum), (float*)(ws + p.off_pbest), (int*)(ws + p.off_pidx), (float*)(ws + p.off_ldraft), \
-      samp, a.logits_debug
+      samp, a.logits_debug, a.relaxed_topk > 0 ? (const float*)(ws + p.off_lpre) : nullptr,                     \
+      a.relaxed_topk > 0 ? (int*)(ws + p.off_rcnt) : nullptr, p.slices
   if (a.dtype == MTP_F32)
     lmhead_simt_kernel<float><<<grid, kThreads, 0, s>>>((const float*)a.hidden, (const float*)a.lm_head,
                                                         MTP_SIMT_ARGS);

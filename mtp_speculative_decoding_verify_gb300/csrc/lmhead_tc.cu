@@ -57,6 +57,8 @@ struct TcParams {
   float* ldraft;
   float* samp_logits;   // [M, V], rows of sampling requests only (nullptr: none)
   float* logits_debug;  // [M, V] optional
+  const float* lpre;    // [M] draft logits of relaxed rows (NaN: not relaxed), nullptr: no relaxed request
+  int* rcnt;            // [3][cpg][M] relaxed rank counts per CTA
   unsigned* err;
   int any_sampling;
   int M, R, H, V;
@@ -88,7 +90,7 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages, bool pair) 
   L.epi_off = off;
   off += 4 * 32 * 33 * 4;                        // per-epilogue-warp 32x33 transpose buffers (later: 4 x N row stats)
   L.rows_off = off;
-  off += N * 12;                                 // per-row draft id, 1/T, sampling flag
+  off += N * 28;                                 // per-row draft id, 1/T, sampling flag, relaxed draft logit, 3 counts
   L.total = off + 1024;                          // + alignment slack for the 1024-B aligned base
   return L;
 }
@@ -123,6 +125,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   int* row_draft = reinterpret_cast<int*>(smem + L.rows_off);
   float* row_inv_t = reinterpret_cast<float*>(smem + L.rows_off + N * 4);
   int* row_samp = reinterpret_cast<int*>(smem + L.rows_off + N * 8);
+  float* row_lpre = reinterpret_cast<float*>(smem + L.rows_off + N * 12);
+  int* row_cnt = reinterpret_cast<int*>(smem + L.rows_off + N * 16);   // [N][3]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int group = blockIdx.x / p.cpg;
@@ -177,6 +181,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     row_draft[r] = draft;
     row_inv_t[r] = inv_t;
     row_samp[r] = samp;
+    row_lpre[r] = (p.lpre && m < p.M) ? p.lpre[m] : __int_as_float(0x7fc00000);
+    row_cnt[3 * r] = row_cnt[3 * r + 1] = row_cnt[3 * r + 2] = 0;
   }
   sm100::tc_fence_before();
   __syncthreads();
@@ -378,6 +384,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           st[c] = rowstat_merge(st[c], RowStat{cmax, csum, cmax, vbase + cidx});
           const int d = row_draft[rr];
           if (d >= vbase && d < vbase + nvalid) p.ldraft[m] = rowv[d - vbase];
+          const float lp = row_lpre[rr];
+          if (lp == lp) {   // relaxed row: rank counts of its draft over these entries
+            const float eps = kRelaxedRankEps * (1.0f + fabsf(lp));
+            int c0 = 0, c1 = 0, c2 = 0;
+            for (int x = 0; x < nvalid; ++x) relaxed_count(rowv[x], vbase + x, lp, d, eps, c0, c1, c2);
+            atomicAdd(&row_cnt[3 * rr], c0);
+            atomicAdd(&row_cnt[3 * rr + 1], c1);
+            atomicAdd(&row_cnt[3 * rr + 2], c2);
+          }
           float* dst_s = (samp && p.samp_logits) ? p.samp_logits + (int64_t)m * p.V + vbase : nullptr;
           float* dst_d = p.logits_debug ? p.logits_debug + (int64_t)m * p.V + vbase : nullptr;
           if (dst_s || dst_d) {
@@ -421,6 +436,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       p.psum[o] = a.s;
       p.pbest[o] = a.best;
       p.pidx[o] = a.idx;
+      if (p.rcnt) {
+        const int64_t plane = (int64_t)p.cpg * p.M;
+        p.rcnt[o] = row_cnt[3 * r];
+        p.rcnt[plane + o] = row_cnt[3 * r + 1];
+        p.rcnt[2 * plane + o] = row_cnt[3 * r + 2];
+      }
     }
   }
   sm100::tc_fence_before();
@@ -598,6 +619,8 @@ cudaError_t launch_lmhead_tc(const mtp_lmhead_args& a, const LmPlan& pl, unsigne
   p.ldraft = (float*)(ws + pl.off_ldraft);
   p.samp_logits = a.any_sampling ? (float*)(ws + pl.off_logits) : nullptr;
   p.logits_debug = a.logits_debug;
+  p.lpre = a.relaxed_topk > 0 ? (const float*)(ws + pl.off_lpre) : nullptr;
+  p.rcnt = a.relaxed_topk > 0 ? (int*)(ws + pl.off_rcnt) : nullptr;
   p.err = err;
   p.any_sampling = a.any_sampling;
   p.M = pl.M;

@@ -79,7 +79,9 @@ extern "C" int mtp_verify_logits_accept_noalloc(const mtp_lmhead_args* args, voi
   a.workspace = scratch;
   a.workspace_bytes = kNoAllocScratchBytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = a.timing_events[0] ? cudaEventRecord(static_cast<cudaEvent_t>(a.timing_events[0]), s) : cudaSuccess;
+  cudaError_t e = mtp::launch_relaxed_prepass(a, p, s);
+  if (e != cudaSuccess) return mtp::set_cuda_error(e, "relaxed pre-pass launch");
+  e = a.timing_events[0] ? cudaEventRecord(static_cast<cudaEvent_t>(a.timing_events[0]), s) : cudaSuccess;
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaEventRecord");
   e = p.tc ? mtp::launch_lmhead_tc(a, p, err, s) : mtp::launch_lmhead_simt(a, p, err, s);
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "LM head launch");
@@ -87,6 +89,6 @@ extern "C" int mtp_verify_logits_accept_noalloc(const mtp_lmhead_args* args, voi
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaEventRecord");
   e = mtp::launch_accept(a, p, err, s);
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "accept launch");
-  mtp::set_launch_count(2 + (a.any_sampling ? 1 : 0));
+  mtp::set_launch_count(2 + (a.any_sampling ? 1 : 0) + (a.relaxed_topk > 0 ? 1 : 0));
   return MTP_OK;
 }

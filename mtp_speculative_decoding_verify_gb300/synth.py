@@ -17,7 +17,13 @@ Workload recipe (what the five standard workloads contain):
     agreement probability, else a uniform token;
   * for rejection-sampling requests the draft distribution of row j is
     q_j = softmax(logits_j / T + N(0, 0.5)) (logits = h W^T, a plain float32
-    matmul used only to shape the input) and draft d_{j+1} ~ q_j.
+    matmul used only to shape the input) and draft d_{j+1} ~ q_j;
+  * relaxed requests (mode 2) get sharper rows with a planted runner-up:
+    h = L1 W[t] / ||W[t]||^2 + L2 W[s] / ||W[s]||^2 + N(0, 0.01) with
+    L1 ~ U(ln V - 1, ln V + 3) and L2 = L1 - U(0, 3), so that token t leads
+    with probability ~0.3-0.95 and s follows it by a random gap; the draft is
+    s with probability 0.5, t with 0.25, else a uniform token (which ranks
+    far outside any small top-N).
 """
 from dataclasses import dataclass, field, replace
 import math
@@ -47,6 +53,9 @@ class Workload:
     seed: int = 0
     stream: int = 0
     spare_blocks: int = 4
+    relaxed: str = "none"       # "none" | "all" | "half" (first half of the batch), mode 2 over the sampling mask
+    relaxed_topk: int = 0       # N of the relaxed rule
+    relaxed_delta: float = 0.0  # delta of the relaxed rule
 
     @property
     def R(self):
@@ -109,6 +118,16 @@ def _sampling_mask(w):
     return m
 
 
+def _relaxed_mask(w):
+    if w.relaxed == "none":
+        return torch.zeros(w.B, dtype=torch.bool)
+    if w.relaxed == "all":
+        return torch.ones(w.B, dtype=torch.bool)
+    m = torch.zeros(w.B, dtype=torch.bool)
+    m[:w.B // 2] = True
+    return m
+
+
 def make_attention_inputs(w, device):
     """Paged KV cache, block table, context lengths, Q and the verify tokens' new K/V."""
     g = _gen(w, device, 1)
@@ -149,11 +168,24 @@ def make_lmhead_inputs(w, device, chunk=16384):
     planted = torch.randint(0, w.V, (w.B, R), generator=gc, dtype=torch.int64)
     Wp = W[planted.reshape(-1).to(device)]
     h = 4.0 * Wp / Wp.norm(dim=1, keepdim=True)
+    relx = _relaxed_mask(w)
+    runner = None
+    if bool(relx.any()):
+        gr = _gen(w, "cpu", 6)
+        runner = torch.randint(0, w.V, (w.B, R), generator=gr, dtype=torch.int64)
+        lv = math.log(w.V)
+        L1 = lv - 1.0 + 4.0 * torch.rand((w.B, R), generator=gr)
+        L2 = L1 - 3.0 * torch.rand((w.B, R), generator=gr)
+        Ws = W[runner.reshape(-1).to(device)]
+        sharp = (L1.reshape(-1, 1).to(device) * Wp / (Wp * Wp).sum(dim=1, keepdim=True) +
+                 L2.reshape(-1, 1).to(device) * Ws / (Ws * Ws).sum(dim=1, keepdim=True))
+        rows = relx.repeat_interleave(R).to(device)
+        h = torch.where(rows.reshape(-1, 1), sharp, h)
     h = h + 0.01 * torch.randn((M, w.H), generator=g, device=device, dtype=torch.float32)
     W = W.to(dt)
     h = h.to(dt)
-    samp = _sampling_mask(w)
-    mode = samp.to(torch.uint8)
+    samp = _sampling_mask(w) & ~relx
+    mode = torch.where(relx, torch.tensor(2, dtype=torch.uint8), samp.to(torch.uint8))
     temperature = torch.where(samp, torch.tensor(w.temperature), torch.tensor(1.0)).to(torch.float32)
 
     # Greedy drafts: d_{j+1} = planted[j] with the agreement probability, else uniform.
@@ -162,6 +194,10 @@ def make_lmhead_inputs(w, device, chunk=16384):
     agree = torch.rand((w.B, w.D), generator=gc) < w.agreement
     rand_tok = torch.randint(0, w.V, (w.B, w.D), generator=gc)
     tokens[:, 1:] = torch.where(agree, planted[:, :w.D], rand_tok)
+    if runner is not None:
+        pick = torch.rand((w.B, w.D), generator=_gen(w, "cpu", 7))
+        rtok = torch.where(pick < 0.5, runner[:, :w.D], torch.where(pick < 0.75, planted[:, :w.D], rand_tok))
+        tokens[:, 1:] = torch.where(relx.reshape(-1, 1), rtok, tokens[:, 1:])
 
     q_draft = None
     if bool(samp.any()):
@@ -181,7 +217,8 @@ def make_lmhead_inputs(w, device, chunk=16384):
             q_draft[b] = qs[i]
             tokens[b, 1:] = draws[i]
     return dict(hidden=h, lm_head=W, tokens=tokens.to(torch.int32).to(device), mode=mode.to(device),
-                temperature=temperature.to(device), q_draft=q_draft, planted=planted.to(torch.int32), seed=w.seed)
+                temperature=temperature.to(device), q_draft=q_draft, planted=planted.to(torch.int32), seed=w.seed,
+                relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta)
 
 
 def as_oracle_array(t):

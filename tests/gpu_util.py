@@ -37,7 +37,8 @@ def gpu_lmhead(w, lm, debug_logits=False):
         res["logits"] = torch.empty((w.M, w.V), dtype=torch.float32, device=dev)
     mv.mtp_verify_logits_accept(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
                                 lm["q_draft"], lm["seed"], res["out_tokens"], res["num_accepted"], res["tie_flags"],
-                                res["lse"], res["argmax"], res.get("logits"))
+                                res["lse"], res["argmax"], res.get("logits"), relaxed_topk=lm.get("relaxed_topk", 0),
+                                relaxed_delta=lm.get("relaxed_delta", 0.0))
     return res
 
 
@@ -88,7 +89,8 @@ def oracle_lmhead(w, lm, reqs, W_host=None, want_logits=False):
     q = None if lm["q_draft"] is None else A(lm["q_draft"].index_select(0, idx))
     return oracle.lmhead_accept(A(lm["hidden"].index_select(0, rows)), W, A(lm["tokens"].index_select(0, idx)),
                                 A(lm["mode"].index_select(0, idx)), A(lm["temperature"].index_select(0, idx)), q,
-                                lm["seed"], want_logits=want_logits, request_index=np.array(reqs, np.int32))
+                                lm["seed"], want_logits=want_logits, request_index=np.array(reqs, np.int32),
+                                relaxed_topk=lm.get("relaxed_topk", 0), relaxed_delta=lm.get("relaxed_delta", 0.0))
 
 
 def compare_accept(gpu, ref, reqs):
@@ -122,7 +124,9 @@ def check_invariants(w, lm, gpu):
         assert (out[b, :k] == tok[b, 1:k + 1]).all()
         assert 0 <= out[b, k] < w.V
         assert (out[b, k + 1:] == -1).all()
-        if not (mode[b] == 1 and temp[b] > 0):
+        if mode[b] == 2:
+            assert out[b, k] == amax[b, k]
+        elif not (mode[b] == 1 and temp[b] > 0):
             assert all(amax[b, j] == tok[b, j + 1] for j in range(k))
             assert k == w.D or amax[b, k] != tok[b, k + 1]
             assert out[b, k] == amax[b, k]

@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(mtplib):
 
 def test_struct_layouts_match(mtplib):
     L = mtplib.lib()
-    assert L.mtp_abi_version() == 1
+    assert L.mtp_abi_version() == mtplib.ABI_VERSION == 2
     for which, st in enumerate((mtplib.AttnArgs, mtplib.LmArgs, mtplib.RollbackArgs)):
         assert L.mtp_abi_struct_size(which) == ctypes.sizeof(st)
 
@@ -85,6 +85,8 @@ def _lm_ok(mtplib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(D=16), 1), (dict(H=0), 1), (dict(dtype=1, H=100), 2), (dict(any_sampling=1), 1),
     (dict(tokens=None), 1), (dict(dtype=9), 1),
+    (dict(relaxed_topk=-1), 1), (dict(relaxed_topk=8193), 1), (dict(relaxed_topk=4, relaxed_delta=-0.1), 1),
+    (dict(relaxed_topk=4, relaxed_delta=float("nan")), 1), (dict(relaxed_topk=4, relaxed_delta=float("inf")), 1),
 ])
 def test_lmhead_rejects_bad_args_on_host(mtplib, kw, code):
     L = mtplib.lib()
