@@ -38,6 +38,7 @@ if ROOT not in sys.path:
 from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
 
 METRIC = "verify-step requests/s and accepted tokens/s on 1 GB300; % of HBM/TC roofline"
+DRAFT_METRIC = "draft-step requests/s (D sequential greedy LM-head calls) on 1 GB300; % of HBM/TC roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -58,7 +59,18 @@ def workloads():
         "profile_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, B=16", B=16),
         "profile_sampling_V32k": synth.CFG2.with_(
             name="profiling case: Llama-70B-shaped rejection sampling B=64 D=5, vocab 32768", V=32768),
+        # MTP-Eagle draft steps: D sequential greedy top-1 calls over the shared LM head, B rows each.
+        "draft_cfg0": synth.CFG0.with_(name="MTP-Eagle draft steps, tiny fp32 LM head: B=4, 3 sequential greedy "
+                                            "top-1 calls, H=512 V=8192"),
+        "draft_cfg1_D3": synth.CFG1.with_(name="MTP-Eagle draft steps, DeepSeek-V3-shaped LM head: B=32, 3 "
+                                               "sequential greedy top-1 calls, H=7168 V=129280"),
+        "draft_cfg2_D5": synth.CFG2.with_(name="MTP-Eagle draft steps, Llama-70B-shaped LM head: B=64, 5 "
+                                               "sequential greedy top-1 calls, H=8192 V=128256"),
     }
+
+
+def is_draft(name):
+    return name.startswith("draft_")
 
 
 def load_peaks():
@@ -82,10 +94,14 @@ def elem_bytes(w):
     return 4 if w.dtype == "f32" else 2
 
 
-def algorithmic(w, ctx):
+def algorithmic(w, ctx, draft=False):
     """Algorithmic bytes and flops of one step: KV read once (ctx + R keys per
-    request and KV head), W read once; flops of the LM head and attention."""
+    request and KV head), W read once; flops of the LM head and attention.
+    A draft-step workload reads W once per call (D calls, B rows each)."""
     eb = elem_bytes(w)
+    if draft:
+        return dict(kv_bytes=0.0, w_bytes=float(w.V) * w.H * eb * w.D, attn_flops=0.0,
+                    lm_flops=2.0 * w.B * w.H * w.V * w.D, calls=w.D)
     R = w.R
     keys = float(np.sum(ctx + R))
     if w.is_mla:
@@ -96,7 +112,7 @@ def algorithmic(w, ctx):
         attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * float(np.sum([sum(c + j + 1 for j in range(R)) for c in ctx]))
     w_bytes = float(w.V) * w.H * eb
     lm_flops = 2.0 * w.M * w.H * w.V
-    return dict(kv_bytes=kv_bytes, w_bytes=w_bytes, attn_flops=attn_flops, lm_flops=lm_flops)
+    return dict(kv_bytes=kv_bytes, w_bytes=w_bytes, attn_flops=attn_flops, lm_flops=lm_flops, calls=1)
 
 
 class ClockSampler:
@@ -194,6 +210,57 @@ class Step:
         n += L.mtp_last_launch_count()
         self.launches = n
 
+    def host_inputs(self):
+        """Device tensors that carry a step's inputs (copied from host memory in the e2e timing)."""
+        return {"q": self.att["q"], "k_new": self.att["k_new"], "ctx_lens": self.att["ctx_lens"],
+                "hidden": self.lm["hidden"], "tokens": self.lm["tokens"]}
+
+    def results(self):
+        return [self.out_tokens, self.num_acc]
+
+    def summary(self):
+        n_acc = self.num_acc.cpu().numpy()
+        ctx = self.att["ctx_lens"].cpu().numpy().astype(np.int64)
+        return n_acc, ctx, float(n_acc.sum() + self.w.B)
+
+
+class DraftStep:
+    """D sequential greedy draft steps of MTP Eagle over the shared LM head
+    (mtp_draft_argmax, B rows per call); each call's hidden states are their
+    own synthetic input (the MTP module between calls is not part of the path)."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        from mtp_speculative_decoding_verify_gb300 import _binding as B
+        self.B = B
+        self.L = B.lib()
+        self.w = w.with_(seed=w.seed + seed_offset)
+        w = self.w
+        self.inp = synth.make_draft_inputs(w, dev)
+        self.tokens = torch.empty((w.D, w.B), dtype=torch.int32, device=dev)
+        self.args = [B.draft_args(self.inp["hidden"][k], self.inp["lm_head"], self.tokens[k]) for k in range(w.D)]
+        self.launches = 0
+
+    def set_events(self, attn_pair, lm_pair):
+        self.args[0].timing_events[0] = lm_pair[0].cuda_event if lm_pair else None
+        self.args[0].timing_events[1] = lm_pair[1].cuda_event if lm_pair else None
+
+    def run(self, stream):
+        h = ctypes.c_void_p(stream.cuda_stream)
+        n = 0
+        for a in self.args:
+            self.B._check(self.L.mtp_draft_argmax(ctypes.byref(a), h))
+            n += self.L.mtp_last_launch_count()
+        self.launches = n
+
+    def host_inputs(self):
+        return {"hidden": self.inp["hidden"]}
+
+    def results(self):
+        return [self.tokens]
+
+    def summary(self):
+        return np.zeros(self.w.B, np.int64), np.zeros(self.w.B, np.int64), float(self.w.B * self.w.D)
+
 
 def combine_ranks(ms, e2e_ms, emitted, world, device):
     """Whole-job figures: the slowest rank's times and the total tokens emitted."""
@@ -219,7 +286,7 @@ def event_pairs(n):
 
 def run_gpu(args, w, rank, world, dev):
     stream = torch.cuda.current_stream()
-    step = Step(w, dev, seed_offset=rank)
+    step = (DraftStep if is_draft(args.workload) else Step)(w, dev, seed_offset=rank)
     for _ in range(args.warmup):
         step.run(stream)
     torch.cuda.synchronize()
@@ -285,22 +352,18 @@ def run_gpu(args, w, rank, world, dev):
         if clocks_g:
             clocks = clocks_g
     ms = graph_ms if graph_ms is not None else ms_eager
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn) if not is_draft(args.workload) else 0.0
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_lm)
-    n_acc = step.num_acc.cpu().numpy()
-    ctx = step.att["ctx_lens"].cpu().numpy().astype(np.int64)
+    n_acc, ctx, emitted = step.summary()
 
     # End to end through the public API with host buffers: each step copies its
-    # inputs from pinned host memory, runs the three calls and reads the
-    # accept result back.
-    host = {k: step.att[k].cpu().pin_memory() for k in ("q", "k_new", "ctx_lens")}
-    host.update({k: step.lm[k].cpu().pin_memory() for k in ("hidden", "tokens")})
-    dev_t = {"q": step.att["q"], "k_new": step.att["k_new"], "ctx_lens": step.att["ctx_lens"],
-             "hidden": step.lm["hidden"], "tokens": step.lm["tokens"]}
-    res_tok = torch.empty_like(step.out_tokens, device="cpu").pin_memory()
-    res_n = torch.empty_like(step.num_acc, device="cpu").pin_memory()
+    # inputs from pinned host memory, runs the calls and reads the results back.
+    dev_t = step.host_inputs()
+    host = {k: t.cpu().pin_memory() for k, t in dev_t.items()}
+    res_dev = step.results()
+    res_host = [torch.empty_like(t, device="cpu").pin_memory() for t in res_dev]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = res_tok.numel() * 4 + res_n.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in res_host)
     for _ in range(max(1, args.warmup // 2)):
         step.run(stream)
     torch.cuda.synchronize()
@@ -311,24 +374,80 @@ def run_gpu(args, w, rank, world, dev):
         for k, t in host.items():
             dev_t[k].copy_(t, non_blocking=True)
         step.run(stream)
-        res_tok.copy_(step.out_tokens, non_blocking=True)
-        res_n.copy_(step.num_acc, non_blocking=True)
+        for th, td in zip(res_host, res_dev):
+            th.copy_(td, non_blocking=True)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - e2e_t0) * 1e3 / K
 
-    ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, float(n_acc.sum() + w.B), world, dev)
+    ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, emitted, world, dev)
     ms_eager, _, _ = combine_ranks(ms_eager, 0.0, 0.0, world, dev)
     return dict(ms=ms, ms_eager=ms_eager, graph=graph_ms is not None, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
                 clocks=clocks, launches=launches, h2d=h2d, d2h=d2h)
 
 
-def cpu_baseline(w, seconds, dev=None):
+def decode_baseline(args, w, dev):
+    """The same workload with D = 0 (a plain decode step: one query row per
+    request, greedy top-1), graph-replayed like the verify step; gives the
+    verify/decode cost ratio."""
+    wd = w.with_(D=0, relaxed="none", relaxed_topk=0)
+    step = Step(wd, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            step.run(side)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    step.B.sync_status()
+    return t0.elapsed_time(t1) / args.steps
+
+
+def draft_oracle_request(w, inp, W, b):
+    """The oracle's D greedy draft steps of request b (argmax rows)."""
+    import oracle
+    toks = np.zeros((1, 1), np.int32)
+    mode = np.zeros(1, np.uint8)
+    out = []
+    for k in range(w.D):
+        h = synth.as_oracle_array(inp["hidden"][k, b:b + 1])
+        r = oracle.lmhead_accept(h, W, toks, mode, None, None, 0)
+        out.append(int(r["argmax"][0, 0]))
+    return out
+
+
+def cpu_baseline(w, seconds, dev=None, draft=False):
     """The oracle, as it stands, on a bounded sample of the same workload:
     whole requests (attention + LM head + acceptance + rollback), one thread."""
     import oracle
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
     gen_dev = dev if dev is not None else torch.device("cpu")
+    if draft:
+        inp = synth.make_draft_inputs(w, gen_dev)
+        W = synth.as_oracle_array(inp["lm_head"])
+        done, t0 = 0, time.perf_counter()
+        while True:
+            draft_oracle_request(w, inp, W, done % w.B)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or done >= w.B:
+                break
+        return dict(value=done / el, unit="requests/s", cores=1, kind="oracle",
+                    sample="%d request(s) of the %d-request batch (%d greedy draft steps each), single-threaded "
+                           "oracle, %.1f s" % (done, w.B, w.D, el))
     att = synth.make_attention_inputs(w, gen_dev)
     lm = synth.make_lmhead_inputs(w, gen_dev)
     W = synth.as_oracle_array(lm["lm_head"])
@@ -366,6 +485,24 @@ def run_reference(args, w, rank, world):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
     gen_dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if torch.cuda.is_available() else "cpu"
+    if is_draft(args.workload):
+        inp = synth.make_draft_inputs(w, gen_dev)
+        Wd = synth.as_oracle_array(inp["lm_head"])
+        for i in range(args.warmup):
+            draft_oracle_request(w, inp, Wd, i % w.B)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            draft_oracle_request(w, inp, Wd, (args.warmup + i) % w.B)
+        el = time.perf_counter() - t0
+        rps = args.steps / el
+        sample = "1 request per step of the %d-request batch (%d greedy draft steps), single-threaded oracle" % (
+            w.B, w.D)
+        json_line(impl="reference", metric=DRAFT_METRIC, value=rps, unit="requests/s", n_gpus=world,
+                  steps=args.steps, warmup=args.warmup, ms_per_step=el * 1e3 / args.steps, higher_is_better=True,
+                  scaling="weak", vs_baseline=None, dtype=w.dtype, data="synthetic", config=config_of(w, args),
+                  cpu_baseline=dict(value=rps, unit="requests/s", cores=1, kind="oracle", sample=sample),
+                  e2e=dict(value=rps, unit="requests/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+        return
     att = synth.make_attention_inputs(w, gen_dev)
     lm = synth.make_lmhead_inputs(w, gen_dev)
     W = synth.as_oracle_array(lm["lm_head"])
@@ -411,6 +548,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only (no CUDA-graph replay)")
+    ap.add_argument("--no-decode-baseline", action="store_true",
+                    help="skip timing the same workload at D = 0 (verify/decode cost ratio)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -427,33 +566,44 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
 
+    draft = is_draft(args.workload)
     r = run_gpu(args, w, rank, world, dev)
+    decode_ms = None
+    if not draft and w.D > 0 and not args.no_decode_baseline:
+        decode_ms = decode_baseline(args, w, dev)
     if rank != 0:
         torch.distributed.destroy_process_group() if world > 1 else None
         return
     peaks, src = load_peaks()
-    alg = algorithmic(w, r["ctx"])
+    alg = algorithmic(w, r["ctx"], draft)
     hbm = float(peaks["hbm_gbs"])
     tc_peak = float(peaks["bf16_tflops"])
     # Dominant kernel: the LM head (HBM-bound on W below M ~ 290 rows, tensor-bound above).
     ridge = tc_peak * 1e12 / (hbm * 1e9)
     lm_intensity = alg["lm_flops"] / alg["w_bytes"]
+    calls = alg["calls"]   # LM-head launches per step; the events time one of them
     if lm_intensity < ridge or w.dtype == "f32":
-        roof = dict(kernel="lm_head", bound="hbm", achieved=alg["w_bytes"] / (r["lm_ms"] * 1e-3) / 1e9, peak=hbm,
-                    unit="GB/s", peak_source=src + " (hbm_gbs)")
+        roof = dict(kernel="lm_head", bound="hbm", achieved=alg["w_bytes"] / calls / (r["lm_ms"] * 1e-3) / 1e9,
+                    peak=hbm, unit="GB/s", peak_source=src + " (hbm_gbs)")
     else:
-        roof = dict(kernel="lm_head", bound="tensor", achieved=alg["lm_flops"] / (r["lm_ms"] * 1e-3) / 1e12,
+        roof = dict(kernel="lm_head", bound="tensor",
+                    achieved=alg["lm_flops"] / calls / (r["lm_ms"] * 1e-3) / 1e12,
                     peak=tc_peak, unit="TFLOP/s", peak_source=src + " (bf16_tflops burst)")
     roof["frac"] = roof["achieved"] / roof["peak"]
     per_row = LMHEAD_TRAFFIC_PER_VOCAB_ROW.get(args.workload)
-    roof["traffic"] = per_row * w.V if per_row else None
+    roof["traffic"] = per_row * w.V if per_row and not draft else None
     roof["traffic_note"] = ("ncu capture of the same kernel at vocab 32768, scaled to the full vocabulary"
                             if per_row else "no capture for this workload")
     roof["avg_launch_ms"] = r["lm_ms"]
     step_bound_s = max((alg["kv_bytes"] + alg["w_bytes"]) / (hbm * 1e9),
                        (alg["lm_flops"] + alg["attn_flops"]) / (tc_peak * 1e12))
     value = world * w.B / (r["ms"] * 1e-3)
-    line = dict(metric=METRIC, value=value, unit="requests/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+    if draft:
+        kernels = dict(lm_head_ms_per_call=r["lm_ms"], calls_per_step=calls)
+    else:
+        kernels = dict(attention_ms=r["attn_ms"], attention_gbs=alg["kv_bytes"] / (r["attn_ms"] * 1e-3) / 1e9,
+                       attention_tflops=alg["attn_flops"] / (r["attn_ms"] * 1e-3) / 1e12, lm_head_ms=r["lm_ms"])
+    line = dict(metric=DRAFT_METRIC if draft else METRIC, value=value, unit="requests/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                 ms_per_step=r["ms"], ms_per_step_eager=r["ms_eager"], higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype,
                 data="synthetic (seeded; random-init weights of the named shapes)", config=config_of(w, args),
                 accepted_tokens_per_s=r["emitted"] / (r["ms"] * 1e-3),
@@ -462,15 +612,20 @@ def main():
                 step_roofline=dict(bound_ms=step_bound_s * 1e3, frac=step_bound_s * 1e3 / r["ms"],
                                    kv_gb=alg["kv_bytes"] / 1e9, w_gb=alg["w_bytes"] / 1e9,
                                    gflop=(alg["lm_flops"] + alg["attn_flops"]) / 1e9),
-                kernels=dict(attention_ms=r["attn_ms"],
-                             attention_gbs=alg["kv_bytes"] / (r["attn_ms"] * 1e-3) / 1e9,
-                             attention_tflops=alg["attn_flops"] / (r["attn_ms"] * 1e-3) / 1e12,
-                             lm_head_ms=r["lm_ms"]),
+                kernels=kernels,
                 e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
                          d2h_bytes_per_step=r["d2h"]),
                 gpu_launches=r["launches"], clocks=r["clocks"])
+    if draft:
+        for k in ("accepted_tokens_per_s", "mean_drafts_accepted"):
+            line.pop(k)
+        line["draft_tokens_per_s"] = r["emitted"] / (r["ms"] * 1e-3)
+    line["graph_speedup"] = r["ms_eager"] / r["ms"] if r["graph"] else None
+    if decode_ms is not None:
+        line["decode_baseline"] = dict(workload=w.name + ", D=0", ms_per_step=decode_ms,
+                                       verify_over_decode=r["ms"] / decode_ms)
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, dev)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, dev, draft)
     json_line(**line)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MTP_ABI_VERSION 2
+#define MTP_ABI_VERSION 3
 
 typedef enum {
   MTP_OK = 0,
@@ -244,6 +244,38 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* args, void* stream);
 int mtp_verify_logits_accept_noalloc(const mtp_lmhead_args* args, void* stream);
 size_t mtp_noalloc_scratch_bytes(void);
 
+/* 2c. Greedy draft step of MTP Eagle: the LM head with a top-1 pick.
+ *
+ * Defined by: "MTP principles" §一 (the MTP modules share the target's
+ * embedding and LM head and predict the D draft tokens one after another);
+ * "MTP in TensorRT-LLM on Blackwell", MTP Eagle (one MTP module is run D times,
+ * each run taking the draft token the previous run predicted). A draft step
+ * gives each of the B requests one token: the argmax of its logits
+ * l[b,v] = sum_k hidden[b,k] W[v,k] (lowest id on equal logits) over the
+ * shared LM head W. D draft tokens are D calls, each on the hidden states the
+ * MTP module produced for the previous token (the module itself is not part
+ * of this library).
+ *
+ * Layouts: hidden [B, H] dtype, lm_head [V, H] dtype; out_tokens [B] int32;
+ * lse_out [B] float (optional, log-sum-exp of the row, so that a caller can
+ * form the draft probability exp(l[b, d] - lse)). Same dtype and H rules,
+ * workspace rules (mtp_draft_workspace_size()), timing events (around the
+ * LM-head kernel) and errors as mtp_verify_logits_accept. B = 0 is a no-op. */
+typedef struct {
+  const void* hidden;
+  const void* lm_head;
+  int32_t* out_tokens;
+  float* lse_out;
+  int32_t B, H, V;
+  int32_t dtype;             /* mtp_dtype */
+  void* workspace;           /* device, >= mtp_draft_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+  void* timing_events[2];
+} mtp_draft_args;
+
+size_t mtp_draft_workspace_size(const mtp_draft_args* args);
+int mtp_draft_argmax(const mtp_draft_args* args, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* 3. KV-cache rollback.
  *
@@ -315,7 +347,8 @@ int mtp_sync_status(void* stream);
 int mtp_last_launch_count(void);
 
 /* ABI version (MTP_ABI_VERSION) and sizeof of the argument structs
- * (0 = mtp_attn_args, 1 = mtp_lmhead_args, 2 = mtp_rollback_args), for
+ * (0 = mtp_attn_args, 1 = mtp_lmhead_args, 2 = mtp_rollback_args,
+ * 3 = mtp_draft_args), for
  * bindings to check their struct layouts against. */
 int mtp_abi_version(void);
 size_t mtp_abi_struct_size(int which);

@@ -8,6 +8,7 @@ from ._binding import (  # noqa: F401
     MtpError,
     kv_rollback,
     lib,
+    mtp_draft_argmax,
     mtp_verify_attention,
     mtp_verify_logits_accept,
     mtp_verify_logits_accept_noalloc,

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libmtpverify.so")
 
 MTP_OK, MTP_INVALID_ARG, MTP_UNSUPPORTED, MTP_CUDA_ERROR, MTP_DEVICE_ERROR = range(5)
-ABI_VERSION = 2   # MTP_ABI_VERSION of the header the structs below mirror
+ABI_VERSION = 3   # MTP_ABI_VERSION of the header the structs below mirror
 MTP_F32, MTP_BF16 = 0, 1
 MAX_DRAFTS = 15
 BLOCK_SIZE = 64
@@ -39,6 +39,12 @@ class LmArgs(ctypes.Structure):
                 ("B", _I), ("D", _I), ("H", _I), ("V", _I), ("dtype", _I), ("any_sampling", _I),
                 ("relaxed_topk", _I), ("relaxed_delta", ctypes.c_float),
                 ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
+
+
+class DraftArgs(ctypes.Structure):
+    _fields_ = [("hidden", _P), ("lm_head", _P), ("out_tokens", _P), ("lse_out", _P), ("B", _I), ("H", _I),
+                ("V", _I), ("dtype", _I), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
+                ("timing_events", _P * 2)]
 
 
 class RollbackArgs(ctypes.Structure):
@@ -89,13 +95,17 @@ def lib():
         L.mtp_noalloc_scratch_bytes.restype = ctypes.c_size_t
         L.mtp_last_launch_count.argtypes = []
         L.mtp_last_launch_count.restype = ctypes.c_int
+        L.mtp_draft_workspace_size.argtypes = [ctypes.POINTER(DraftArgs)]
+        L.mtp_draft_workspace_size.restype = ctypes.c_size_t
+        L.mtp_draft_argmax.argtypes = [ctypes.POINTER(DraftArgs), _P]
+        L.mtp_draft_argmax.restype = ctypes.c_int
         L.mtp_abi_version.argtypes = []
         L.mtp_abi_version.restype = ctypes.c_int
         L.mtp_abi_struct_size.argtypes = [ctypes.c_int]
         L.mtp_abi_struct_size.restype = ctypes.c_size_t
         if L.mtp_abi_version() != ABI_VERSION:
             raise RuntimeError("library ABI version %d, binding expects %d" % (L.mtp_abi_version(), ABI_VERSION))
-        for which, st in enumerate((AttnArgs, LmArgs, RollbackArgs)):
+        for which, st in enumerate((AttnArgs, LmArgs, RollbackArgs, DraftArgs)):
             if L.mtp_abi_struct_size(which) != ctypes.sizeof(st):
                 raise RuntimeError("ABI mismatch for %s" % st.__name__)
         _lib = L
@@ -247,6 +257,35 @@ def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft
     a = lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
                 lse_out, argmax_out, logits_debug, workspace, relaxed_topk, relaxed_delta)
     _check(lib().mtp_verify_logits_accept(ctypes.byref(a), _stream_handle(stream)))
+
+
+def draft_args(hidden, lm_head, out_tokens, lse_out=None, workspace=None):
+    """Fill DraftArgs from tensors (see mtp_draft_argmax for shapes)."""
+    B, H = hidden.shape
+    V = lm_head.shape[0]
+    dt = lm_head.dtype
+    _dev(hidden, "hidden", dt, (B, H))
+    _dev(lm_head, "lm_head", dt, (V, H))
+    _dev(out_tokens, "out_tokens", torch.int32, (B,))
+    _dev(lse_out, "lse_out", torch.float32, (B,))
+    a = DraftArgs(_ptr(hidden), _ptr(lm_head), _ptr(out_tokens), _ptr(lse_out), B, H, V, _dtype_code(lm_head),
+                  None, 0)
+    n = lib().mtp_draft_workspace_size(ctypes.byref(a))
+    if n == 0:
+        _check(MTP_INVALID_ARG)
+    if workspace is None:
+        workspace = _workspace(n, hidden.device, "draft")
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def mtp_draft_argmax(hidden, lm_head, out_tokens, lse_out=None, workspace=None, stream=None):
+    """One greedy draft step over the shared LM head: out_tokens[b] = argmax_v hidden[b] . lm_head[v]
+    (lowest id on ties); hidden [B, H], lm_head [V, H] (float32 or bfloat16), out_tokens [B] int32,
+    optional lse_out [B] float32."""
+    a = draft_args(hidden, lm_head, out_tokens, lse_out, workspace)
+    _check(lib().mtp_draft_argmax(ctypes.byref(a), _stream_handle(stream)))
 
 
 def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens,

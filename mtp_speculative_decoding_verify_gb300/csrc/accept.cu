@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
   const int R = D + 1;
   const int M = B * R;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  const int md = mode[b];
+  const int md = mode ? mode[b] : 0;   // no mode array: a draft step (greedy, R = 1)
   const bool relaxed = md == 2 && relaxed_topk > 0;
 
   for (int j = warp; j < R; j += kWarps) {
@@ -106,10 +106,11 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
   __syncthreads();
   if (threadIdx.x != 0) return;
 
-  const int32_t* tok = tokens + (int64_t)b * R;
+  const int32_t* tok = tokens ? tokens + (int64_t)b * R : nullptr;   // read only while n < D
   int32_t* out = out_tokens + (int64_t)b * R;
   bool bad = false;
-  for (int j = 0; j < R; ++j) bad |= (tok[j] < 0 || tok[j] >= V);
+  if (tokens)
+    for (int j = 0; j < R; ++j) bad |= (tok[j] < 0 || tok[j] >= V);
   if (bad) raise_error(err, MTP_ERR_TOKEN_ID);
   if (md > 2 || (md == 2 && !relaxed)) raise_error(err, MTP_ERR_MODE);   // decided greedily
   const bool sampling = any_sampling && md == 1 && temperature[b] > 0.0f;
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
   }
   dec[b] = Decision{n, (sampling && !bad) ? 1 : 0, tie, 0};
   race_count[b] = 0;
-  num_accepted[b] = n;
-  tie_flags[b] = (uint8_t)tie;
+  if (num_accepted) num_accepted[b] = n;
+  if (tie_flags) tie_flags[b] = (uint8_t)tie;
 }
 
 // Block-wide merge of one race per thread; the result is valid in thread 0.

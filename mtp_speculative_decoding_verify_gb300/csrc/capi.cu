@@ -208,6 +208,7 @@ size_t mtp_abi_struct_size(int which) {
     case 0: return sizeof(mtp_attn_args);
     case 1: return sizeof(mtp_lmhead_args);
     case 2: return sizeof(mtp_rollback_args);
+    case 3: return sizeof(mtp_draft_args);
     default: return 0;
   }
 }

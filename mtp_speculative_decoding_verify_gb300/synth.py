@@ -221,6 +221,21 @@ def make_lmhead_inputs(w, device, chunk=16384):
                 relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta)
 
 
+def make_draft_inputs(w, device):
+    """Inputs of D sequential greedy draft steps over the shared LM head:
+    hidden [D, B, H] (draft step k's B rows, planted like the verify rows so
+    each row's argmax is its planted token), lm_head W [V, H], planted [D, B]."""
+    g = _gen(w, device, 8)
+    gc = _gen(w, "cpu", 9)
+    W = (torch.randn((w.V, w.H), generator=g, device=device, dtype=torch.float32) * 0.02)
+    planted = torch.randint(0, w.V, (w.D, w.B), generator=gc, dtype=torch.int64)
+    Wp = W[planted.reshape(-1).to(device)]
+    h = 4.0 * Wp / Wp.norm(dim=1, keepdim=True)
+    h = h + 0.01 * torch.randn((w.D * w.B, w.H), generator=g, device=device, dtype=torch.float32)
+    return dict(hidden=h.to(w.torch_dtype).reshape(w.D, w.B, w.H).contiguous(), lm_head=W.to(w.torch_dtype),
+                planted=planted.to(torch.int32))
+
+
 def as_oracle_array(t):
     """Host numpy view for the oracle: float32 as is, bf16 as uint16 bit patterns."""
     import numpy as np

@@ -44,8 +44,8 @@ def test_every_declared_symbol_is_exported(mtplib):
 
 def test_struct_layouts_match(mtplib):
     L = mtplib.lib()
-    assert L.mtp_abi_version() == mtplib.ABI_VERSION == 2
-    for which, st in enumerate((mtplib.AttnArgs, mtplib.LmArgs, mtplib.RollbackArgs)):
+    assert L.mtp_abi_version() == mtplib.ABI_VERSION == 3
+    for which, st in enumerate((mtplib.AttnArgs, mtplib.LmArgs, mtplib.RollbackArgs, mtplib.DraftArgs)):
         assert L.mtp_abi_struct_size(which) == ctypes.sizeof(st)
 
 
@@ -117,3 +117,28 @@ def test_binding_fails_loudly_without_library(monkeypatch, mtplib):
     monkeypatch.setattr(mtplib, "_lib", None)
     with pytest.raises(RuntimeError):
         mtplib.lib()
+
+
+def _draft_ok(mtplib, **kw):
+    a = mtplib.DraftArgs()
+    a.hidden = a.lm_head = a.out_tokens = 16
+    a.B, a.H, a.V, a.dtype = 4, 512, 8192, 0
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), 1), (dict(H=0), 1), (dict(V=0), 1), (dict(dtype=7), 1), (dict(dtype=1, H=100), 2),
+    (dict(dtype=0, H=6), 2), (dict(hidden=None), 1), (dict(out_tokens=None), 1),
+])
+def test_draft_rejects_bad_args_on_host(mtplib, kw, code):
+    L = mtplib.lib()
+    assert L.mtp_draft_argmax(ctypes.byref(_draft_ok(mtplib, **kw)), None) == code
+    assert L.mtp_last_error()
+    assert L.mtp_draft_workspace_size(ctypes.byref(_draft_ok(mtplib, **kw))) == 0
+
+
+def test_draft_empty_batch_is_a_no_op(mtplib):
+    L = mtplib.lib()
+    assert L.mtp_draft_argmax(ctypes.byref(_draft_ok(mtplib, B=0)), None) == 0

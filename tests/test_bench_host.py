@@ -54,3 +54,27 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT,
                        env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_draft_steps_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "draft_cfg0", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"].startswith("draft-step") and line["value"] > 0
+    assert "3 greedy draft steps" in line["cpu_baseline"]["sample"]
+
+
+def test_algorithmic_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+    import numpy as np
+    w = bench.workloads()["draft_cfg1_D3"]
+    a = bench.algorithmic(w, np.zeros(w.B, np.int64), draft=True)
+    assert a["w_bytes"] == 3 * 129280 * 7168 * 2 and a["calls"] == 3 and a["kv_bytes"] == 0
+    assert a["lm_flops"] == 2.0 * 32 * 7168 * 129280 * 3
+    v = bench.workloads()["cfg1_D3"]
+    ctx = np.array([512] * v.B, np.int64)
+    b = bench.algorithmic(v, ctx)
+    assert b["kv_bytes"] == v.B * (512 + 4) * 576 * 2 and b["calls"] == 1
