@@ -25,12 +25,14 @@ def lib():
         i32, u32, u64, f32 = ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox4x32_10.restype = None
-        L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 8
+        L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 9
         L.oracle_verify_attention.restype = i32
-        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7 + [i32, ctypes.c_float]
+        L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7 + [i32, ctypes.c_float, P, P]
         L.oracle_lmhead_accept.restype = i32
         L.oracle_kv_rollback.argtypes = [i32] * 4 + [P] * 5
         L.oracle_kv_rollback.restype = i32
+        L.oracle_tree_kv_compact.argtypes = [i32] * 10 + [P] * 6
+        L.oracle_tree_kv_compact.restype = i32
         L.oracle_accept_prefix.argtypes = [i32, P, P, P, P]
         L.oracle_relaxed_accept.argtypes = [i32, P, ctypes.c_float, i32, i32, ctypes.c_float, P]
         L.oracle_relaxed_accept.restype = i32
@@ -94,8 +96,9 @@ def race(w, E):
 
 
 def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *, D, Hq, Hkv,
-                     d_qk, d_v, block_size, is_mla, sm_scale):
-    """Append + verify attention. k_cache / v_cache are updated in place; returns out."""
+                     d_qk, d_v, block_size, is_mla, sm_scale, parents=None):
+    """Append + verify attention. k_cache / v_cache are updated in place; returns out.
+    parents [B, R] int32 (None: chains) gives tree drafts."""
     q, dt = _storage(q)
     k_new, _ = _storage(k_new)
     v_new = None if v_new is None else _storage(v_new)[0]
@@ -108,15 +111,18 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *
     num_blocks = k_cache.shape[0]
     rc = lib().oracle_verify_attention(B, D, Hq, Hkv, d_qk, d_v, block_size, bt.shape[1], num_blocks,
                                        int(is_mla), float(sm_scale), dt, _ptr(q), _ptr(k_new), _ptr(v_new),
-                                       _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(ctx), _ptr(out))
+                                       _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(ctx), _ptr(out),
+                                       _ptr(None if parents is None else _c(parents, np.int32)))
     if rc != 0:
         raise ValueError("oracle_verify_attention returned %d" % rc)
     return out
 
 
 def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, want_logits=False,
-                  request_index=None, relaxed_topk=0, relaxed_delta=0.0):
-    """LM head + row statistics + acceptance. Returns a dict of numpy arrays."""
+                  request_index=None, relaxed_topk=0, relaxed_delta=0.0, parents=None):
+    """LM head + row statistics + acceptance. Returns a dict of numpy arrays
+    (accepted_nodes: the accepted path's nodes, root first, then -1).
+    parents [B, R] int32 (None: chains) gives tree drafts (greedy requests)."""
     hidden, dt = _storage(hidden)
     lm_head, dt2 = _storage(lm_head)
     assert dt == dt2
@@ -134,13 +140,16 @@ def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, 
     amax = np.zeros((B, R), np.int32)
     logits = np.zeros((B * R, V), np.float32) if want_logits else None
     rid = None if request_index is None else _c(request_index, np.int32)
+    par = None if parents is None else _c(parents, np.int32)
+    nodes = np.full((B, R), -7, np.int32)
     rc = lib().oracle_lmhead_accept(B, D, H, V, dt, _ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode),
                                     _ptr(temperature), _ptr(q_draft), ctypes.c_uint64(seed), _ptr(rid), _ptr(out_tokens),
                                     _ptr(num_acc), _ptr(ties), _ptr(lse), _ptr(amax), _ptr(logits),
-                                    int(relaxed_topk), ctypes.c_float(relaxed_delta))
+                                    int(relaxed_topk), ctypes.c_float(relaxed_delta), _ptr(par), _ptr(nodes))
     if rc != 0:
         raise ValueError("oracle_lmhead_accept returned %d" % rc)
-    res = dict(out_tokens=out_tokens, num_accepted=num_acc, tie_flags=ties, lse=lse, argmax=amax)
+    res = dict(out_tokens=out_tokens, num_accepted=num_acc, tie_flags=ties, lse=lse, argmax=amax,
+               accepted_nodes=nodes)
     if want_logits:
         res["logits"] = logits
     return res
@@ -156,6 +165,22 @@ def kv_rollback(block_table, seq_lens, num_accepted, free_list, free_count, *, D
                                   _ptr(free_list), _ptr(free_count))
     if rc != 0:
         raise ValueError("oracle_kv_rollback returned %d" % rc)
+
+
+def tree_kv_compact(k_cache, v_cache, block_table, ctx_lens, accepted_nodes, num_accepted, *, D, Hkv, d_qk,
+                    d_v, block_size, is_mla):
+    """In place: the accepted path's K/V moved to slots ctx + 1 .. ctx + n (numpy caches)."""
+    assert k_cache.flags.c_contiguous and (v_cache is None or v_cache.flags.c_contiguous)
+    dt = {np.dtype(np.float32): F32, np.dtype(np.uint16): BF16}[k_cache.dtype]
+    bt = _c(block_table, np.int32)
+    ctx = _c(ctx_lens, np.int32)
+    nodes = _c(accepted_nodes, np.int32)
+    na = _c(num_accepted, np.int32)
+    rc = lib().oracle_tree_kv_compact(ctx.shape[0], D, Hkv, d_qk, d_v, block_size, bt.shape[1], k_cache.shape[0],
+                                      int(is_mla), dt, _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(ctx),
+                                      _ptr(nodes), _ptr(na))
+    if rc != 0:
+        raise ValueError("oracle_tree_kv_compact returned %d" % rc)
 
 
 def relaxed_accept(logits, lse, d, topk, delta):

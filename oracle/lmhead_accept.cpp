@@ -25,6 +25,15 @@
  *                 probability minus delta; d_{j+1} is accepted iff it is a
  *                 candidate. The first miss is replaced by the argmax and the
  *                 bonus is the argmax of row D, as for greedy requests.
+ *       tree:     ("MTP in TensorRT-LLM on Blackwell", future work: tree
+ *                 speculative sampling) node k >= 1 carries draft token
+ *                 tokens[k] continuing the path that ends at its parent.
+ *                 Node u is accepted when every node v on the path from the
+ *                 root to u carries the argmax of its parent's row (greedy
+ *                 rule per edge). The accepted node of greatest depth (lowest
+ *                 index among equally deep ones) ends the accepted path; the
+ *                 argmax of its row is the emitted correction/bonus token.
+ *                 The chain is the tree with parents[k] = k - 1.
  *     Every step emits n + 1 tokens, 1 .. D+1 ("MTP principles" stage 4).
  *  4. A categorical draw is an exponential race: argmax_v w_v / E_v with
  *     E_v ~ Exp(1) from the counter-based generator (philox.cpp); this picks
@@ -108,7 +117,8 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                                     int32_t* out_tokens, int32_t* num_accepted,
                                     uint8_t* tie_flags, float* lse_out,
                                     int32_t* argmax_out, float* logits_out,
-                                    int relaxed_topk, float relaxed_delta) {
+                                    int relaxed_topk, float relaxed_delta,
+                                    const int32_t* parents, int32_t* accepted_nodes) {
   if (B < 0 || D < 0 || H <= 0 || V <= 0 || (dtype != 0 && dtype != 1)) return ORACLE_BAD_ARG;
   if (relaxed_delta < 0.0f) return ORACLE_BAD_ARG;
   const int R = D + 1;
@@ -127,6 +137,12 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
     const bool relaxed = mode[b] == 2;
     if (sampling && q_draft == NULL) return ORACLE_BAD_ARG;
     if (relaxed && relaxed_topk < 1) return ORACLE_BAD_ARG;
+    if (parents && (sampling || relaxed)) return ORACLE_BAD_ARG;   /* trees are verified greedily */
+    std::vector<int> parent(R);
+    for (int k = 0; k < R; ++k) {
+      parent[k] = parents ? parents[(int64_t)b * R + k] : k - 1;
+      if (k == 0 ? parent[k] != -1 : (parent[k] < 0 || parent[k] >= k)) return ORACLE_BAD_ARG;
+    }
     const float inv_t = sampling ? 1.0f / temperature[b] : 1.0f;
 
     /* Steps 1-2 for the R rows of request b. */
@@ -164,7 +180,25 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
     for (int j = 0; j < R; ++j) out[j] = -1;
     uint8_t tie = 0;
     int n;
-    if (relaxed) {
+    std::vector<int> path;   /* accepted path, root first */
+    if (parents) {
+      int best_u = 0, best_depth = 0;
+      for (int u = 0; u < R; ++u) {
+        std::vector<int> up;   /* u, parent(u), ..., root */
+        for (int k = u; k >= 0; k = parent[k]) up.push_back(k);
+        bool ok = true;
+        for (size_t i = 0; i + 1 < up.size(); ++i) ok = ok && tok[up[i]] == amax[up[i + 1]];
+        const int depth = (int)up.size() - 1;
+        if (ok && depth > best_depth) {
+          best_depth = depth;
+          best_u = u;
+        }
+      }
+      for (int k = best_u; k >= 0; k = parent[k]) path.insert(path.begin(), k);
+      n = best_depth;
+      for (int i = 1; i <= n; ++i) out[i - 1] = tok[path[i]];
+      out[n] = amax[best_u];
+    } else if (relaxed) {
       n = 0;
       while (n < D && oracle_relaxed_accept(V, &logits[(size_t)n * V], lse[n], tok[n + 1], relaxed_topk,
                                             relaxed_delta, &tie))
@@ -208,6 +242,11 @@ extern "C" int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
     }
     num_accepted[b] = n;
     tie_flags[b] = tie;
+    if (accepted_nodes) {
+      if (!parents)
+        for (int i = 0; i <= n; ++i) path.push_back(i);
+      for (int i = 0; i < R; ++i) accepted_nodes[(int64_t)b * R + i] = i <= n ? path[i] : -1;
+    }
   }
   return ORACLE_OK;
 }

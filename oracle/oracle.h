@@ -58,6 +58,10 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
  *   v_cache  [num_blocks, block_size, Hkv, d_v]    updated in place (MLA NULL)
  *   block_table [B, max_blocks], ctx_lens [B]
  *   out      [B, R, Hq, d_v]  (dtype as q)
+ *   parents  [B, R] int32 or NULL (chain): tree drafts ([TRT] future work,
+ *            Fig. 9), parents[b][0] = -1 and 0 <= parents[b][k] < k; row j
+ *            then sees the context and the verify keys of the nodes on the
+ *            path from the root to node j (itself included)
  * Returns ORACLE_BAD_INDEX if a block id needed is outside [0, num_blocks). */
 int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
                             int block_size, int max_blocks, int num_blocks,
@@ -65,7 +69,7 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
                             const void* q, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache,
                             const int32_t* block_table, const int32_t* ctx_lens,
-                            void* out);
+                            void* out, const int32_t* parents);
 
 /* LM head + row statistics + acceptance ([K3] steps 4-6; [VLLM] §三 stages 3-4;
  * [SDMTP] §2.3, §4.4).
@@ -90,7 +94,13 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
  * at a decision, or for a relaxed decision |p_d - (p_1 - delta)| < 1e-3 or a
  * draft rank that moves across N when its logit moves by 1e-3 (1 + |l_d|);
  * bit1: top-2 race keys within 1e-5 relative), and optional lse_out [B, R],
- * argmax_out [B, R], logits_out [B*R, V] (fp32, / T). */
+ * argmax_out [B, R], logits_out [B*R, V] (fp32, / T).
+ * parents [B, R] (NULL: chains): tree drafts, greedy requests only (a tree
+ * with a sampling or relaxed request is BAD_ARG): node u is accepted when
+ * every node on its root path carries the argmax of its parent's row; the
+ * deepest accepted node (lowest index among equals) ends the path, and the
+ * argmax of its row is the last emitted token. accepted_nodes [B, R]
+ * (optional): the path's nodes, root (0) first, then -1. */
 int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                          const void* hidden, const void* lm_head,
                          const int32_t* tokens, const uint8_t* mode,
@@ -99,7 +109,8 @@ int oracle_lmhead_accept(int B, int D, int H, int V, int dtype,
                          int32_t* out_tokens, int32_t* num_accepted,
                          uint8_t* tie_flags, float* lse_out,
                          int32_t* argmax_out, float* logits_out,
-                         int relaxed_topk, float relaxed_delta);
+                         int relaxed_topk, float relaxed_delta,
+                         const int32_t* parents, int32_t* accepted_nodes);
 
 /* KV-cache rollback ([TRT] "MTP Vanilla"/"MTP Eagle": KV of discarded drafts
  * is cleared; [K3] "rollback keeps the correct prefix").
@@ -111,6 +122,16 @@ int oracle_kv_rollback(int B, int D, int block_size, int max_blocks,
                        int32_t* block_table, int32_t* seq_lens,
                        const int32_t* num_accepted,
                        int32_t* free_list, int32_t* free_count);
+
+/* KV compaction after a tree verify ([TRT] future work, Fig. 9): for
+ * i = 1 .. num_accepted[b], the K/V in slot ctx + accepted_nodes[b][i] is
+ * copied to slot ctx + i (in increasing i), so that the kept sequence is
+ * contiguous for oracle_kv_rollback. Same cache layout as
+ * oracle_verify_attention. */
+int oracle_tree_kv_compact(int B, int D, int Hkv, int d_qk, int d_v, int block_size, int max_blocks,
+                           int num_blocks, int is_mla, int dtype, void* k_cache, void* v_cache,
+                           const int32_t* block_table, const int32_t* ctx_lens,
+                           const int32_t* accepted_nodes, const int32_t* num_accepted);
 
 /* Pieces of the acceptance rule exposed for pinning with fixed inputs. */
 
