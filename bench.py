@@ -46,6 +46,13 @@ def workloads():
     return {
         "cfg1_D3": synth.CFG1,
         "cfg1_D1": synth.CFG1.with_(D=1),
+        # Tree drafts (full tree of 15 drafts: 3 at the root, 2 under each, then chains), greedy.
+        "tree_cfg0": synth.CFG0.with_(name="tiny fp32 MHA with random draft trees: B=4 D=7 ctx=128 H=512 V=8192",
+                                      D=7, tree="random"),
+        "tree_cfg1_D15": synth.CFG1.with_(name=synth.CFG1.name.replace("D=3", "tree of 15 drafts (3x2x1 fan-out)"),
+                                          D=15, tree="full"),
+        "tree_cfg3_D15": synth.CFG3.with_(name=synth.CFG3.name.replace("D=3", "tree of 15 drafts (3x2x1 fan-out)"),
+                                          D=15, tree="full", sampling="none"),
         # Relaxed acceptance (top-10, delta 0.6) on the DeepSeek-V3-shaped step.
         "cfg1_D3_relaxed": synth.CFG1.with_(name=synth.CFG1.name + ", relaxed acceptance N=10 delta=0.6",
                                             relaxed="all", relaxed_topk=10, relaxed_delta=0.6),
@@ -94,6 +101,18 @@ def elem_bytes(w):
     return 4 if w.dtype == "f32" else 2
 
 
+def path_lengths(w):
+    """[B, R] number of verify keys each row sees: j + 1 for chains, the root-path length for trees."""
+    par = synth.make_parents(w)
+    if par is None:
+        return np.tile(np.arange(1, w.R + 1), (w.B, 1))
+    par = par.numpy()
+    out = np.ones((w.B, w.R), np.int64)
+    for k in range(1, w.R):
+        out[:, k] = out[np.arange(w.B), par[:, k]] + 1
+    return out
+
+
 def algorithmic(w, ctx, draft=False):
     """Algorithmic bytes and flops of one step: KV read once (ctx + R keys per
     request and KV head), W read once; flops of the LM head and attention.
@@ -104,12 +123,13 @@ def algorithmic(w, ctx, draft=False):
                     lm_flops=2.0 * w.B * w.H * w.V * w.D, calls=w.D)
     R = w.R
     keys = float(np.sum(ctx + R))
+    visible = float(np.sum(ctx[:, None] + path_lengths(w)))   # (row, visible key) pairs per head
     if w.is_mla:
         kv_bytes = keys * w.d_qk * eb
-        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * float(np.sum([sum(c + j + 1 for j in range(R)) for c in ctx]))
+        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * visible
     else:
         kv_bytes = keys * w.Hkv * (w.d_qk + w.d_v) * eb
-        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * float(np.sum([sum(c + j + 1 for j in range(R)) for c in ctx]))
+        attn_flops = 2.0 * (w.d_qk + w.d_v) * w.Hq * visible
     w_bytes = float(w.V) * w.H * eb
     lm_flops = 2.0 * w.M * w.H * w.V
     return dict(kv_bytes=kv_bytes, w_bytes=w_bytes, attn_flops=attn_flops, lm_flops=lm_flops, calls=1)
@@ -182,11 +202,18 @@ class Step:
         self.seq = att["ctx_lens"].clone()
         self.free_list = torch.full((w.B * 2 + 8,), -1, dtype=torch.int32, device=dev)
         self.free_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.parents = lm.get("parents")
+        self.acc_nodes = torch.empty((w.B, w.R), dtype=torch.int32, device=dev)
         self.a_attn = B.attn_args(att["q"], att["k_new"], att["v_new"], att["k_cache"], att["v_cache"],
-                                  att["block_table"], att["ctx_lens"], self.out, sm_scale=w.sm_scale)
+                                  att["block_table"], att["ctx_lens"], self.out, sm_scale=w.sm_scale,
+                                  parents=self.parents)
         self.a_lm = B.lm_args(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
                               lm["q_draft"], lm["seed"], self.out_tokens, self.num_acc, self.ties,
-                              relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta)
+                              relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta, parents=self.parents,
+                              accepted_nodes=self.acc_nodes if self.parents is not None else None)
+        # Tree drafts: the accepted path's K/V moves to contiguous slots before the rollback.
+        self.a_cmp = None if self.parents is None else B.compact_args(
+            att["k_cache"], att["v_cache"], att["block_table"], att["ctx_lens"], self.acc_nodes, self.num_acc)
         self.a_rb = B.rollback_args(self.table_work, self.seq, self.num_acc, self.free_list, self.free_count, D=w.D)
         self.launches = 0
 
@@ -206,14 +233,20 @@ class Step:
         n = L.mtp_last_launch_count()
         chk(L.mtp_verify_logits_accept(ctypes.byref(self.a_lm), h))
         n += L.mtp_last_launch_count()
+        if self.a_cmp is not None:
+            chk(L.mtp_tree_kv_compact(ctypes.byref(self.a_cmp), h))
+            n += L.mtp_last_launch_count()
         chk(L.kv_rollback(ctypes.byref(self.a_rb), h))
         n += L.mtp_last_launch_count()
         self.launches = n
 
     def host_inputs(self):
         """Device tensors that carry a step's inputs (copied from host memory in the e2e timing)."""
-        return {"q": self.att["q"], "k_new": self.att["k_new"], "ctx_lens": self.att["ctx_lens"],
-                "hidden": self.lm["hidden"], "tokens": self.lm["tokens"]}
+        d = {"q": self.att["q"], "k_new": self.att["k_new"], "ctx_lens": self.att["ctx_lens"],
+             "hidden": self.lm["hidden"], "tokens": self.lm["tokens"]}
+        if self.parents is not None:
+            d["parents"] = self.parents
+        return d
 
     def results(self):
         return [self.out_tokens, self.num_acc]
@@ -389,7 +422,7 @@ def decode_baseline(args, w, dev):
     """The same workload with D = 0 (a plain decode step: one query row per
     request, greedy top-1), graph-replayed like the verify step; gives the
     verify/decode cost ratio."""
-    wd = w.with_(D=0, relaxed="none", relaxed_topk=0)
+    wd = w.with_(D=0, relaxed="none", relaxed_topk=0, tree="chain")
     step = Step(wd, dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -413,6 +446,23 @@ def decode_baseline(args, w, dev):
     torch.cuda.synchronize()
     step.B.sync_status()
     return t0.elapsed_time(t1) / args.steps
+
+
+def oracle_request(w, att, lm, W, table, ctx, b):
+    """The oracle's whole verify step for request b: append + attention, LM
+    head + acceptance, KV compaction (tree drafts) and rollback."""
+    import oracle
+    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
+    parents = lm.get("parents")
+    _, kc, vc, sub_table = oracle_attention(w, att, [b], parents, return_cache=True)
+    r = oracle_lmhead(w, lm, [b], W)
+    if parents is not None:
+        oracle.tree_kv_compact(kc, vc, sub_table, ctx[b:b + 1], r["accepted_nodes"], r["num_accepted"], D=w.D,
+                               Hkv=1 if w.is_mla else w.Hkv, d_qk=w.d_qk, d_v=w.d_v, block_size=64,
+                               is_mla=w.is_mla)
+    fl = np.zeros(w.D // 64 + 4, np.int32)
+    fc = np.zeros(1, np.int32)
+    oracle.kv_rollback(table[b:b + 1].copy(), ctx[b:b + 1].copy(), r["num_accepted"], fl, fc, D=w.D, block_size=64)
 
 
 def draft_oracle_request(w, inp, W, b):
@@ -455,14 +505,7 @@ def cpu_baseline(w, seconds, dev=None, draft=False):
     ctx = synth.as_oracle_array(att["ctx_lens"])
     done, t0 = 0, time.perf_counter()
     while True:
-        b = done % w.B
-        oracle_attention(w, att, [b])
-        r = oracle_lmhead(w, lm, [b], W)
-        t = table[b:b + 1].copy()
-        s = ctx[b:b + 1].copy()
-        fl = np.zeros(w.D // 64 + 4, np.int32)
-        fc = np.zeros(1, np.int32)
-        oracle.kv_rollback(t, s, r["num_accepted"], fl, fc, D=w.D, block_size=64)
+        oracle_request(w, att, lm, W, table, ctx, done % w.B)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds or done >= 4 * w.B:
@@ -510,12 +553,7 @@ def run_reference(args, w, rank, world):
     ctx = synth.as_oracle_array(att["ctx_lens"])
 
     def one(b):
-        oracle_attention(w, att, [b])
-        r = oracle_lmhead(w, lm, [b], W)
-        fl = np.zeros(8, np.int32)
-        fc = np.zeros(1, np.int32)
-        oracle.kv_rollback(table[b:b + 1].copy(), ctx[b:b + 1].copy(), r["num_accepted"], fl, fc, D=w.D,
-                           block_size=64)
+        oracle_request(w, att, lm, W, table, ctx, b)
     for i in range(args.warmup):
         one(i % w.B)
     t0 = time.perf_counter()

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MTP_ABI_VERSION 3
+#define MTP_ABI_VERSION 4
 
 typedef enum {
   MTP_OK = 0,
@@ -78,6 +78,7 @@ typedef enum { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
 #define MTP_ERR_FREE_LIST  0x10u /* free list capacity exceeded */
 #define MTP_ERR_TIMEOUT    0x20u /* a bounded wait inside a kernel gave up */
 #define MTP_ERR_MODE       0x40u /* mode > 2, or mode 2 while relaxed_topk is 0 (decided greedily) */
+#define MTP_ERR_TREE       0x80u /* malformed parents list (that request is treated as a chain) */
 
 /* ------------------------------------------------------------------------ */
 /* 1. Verify attention with KV append.
@@ -96,6 +97,14 @@ typedef enum { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
  * Absorbed MLA (is_mla = 1): one latent vector of width d_qk per token is
  * both the key and, through its first d_v entries, the value; Hkv = 1,
  * v_new and v_cache are NULL.
+ * Tree drafts ("MTP in TensorRT-LLM on Blackwell", future work: tree
+ * speculative sampling, Fig. 9), when `parents` is given: verify token j is
+ * node j of a tree, node 0 the input token and node k >= 1 a child of
+ * parents[b][k] (0 <= parents[b][k] < k, parents[b][0] = -1). Row j then
+ * attends slots 0 .. ctx-1 and ctx+k for every node k on the path from the
+ * root to node j (itself included). parents = NULL is the chain
+ * (parents[b][k] = k-1). A malformed list sets MTP_ERR_TREE and that request
+ * is computed as a chain.
  *
  * Layouts (dtype as given; MTP_F32 or MTP_BF16):
  *   q           [B, R, Hq, d_qk]
@@ -104,6 +113,7 @@ typedef enum { MTP_F32 = 0, MTP_BF16 = 1 } mtp_dtype;
  *   k_cache     [num_blocks, 64, Hkv, d_qk]   written at the verify slots
  *   v_cache     [num_blocks, 64, Hkv, d_v]    (MLA: NULL)
  *   block_table [B, max_blocks] int32;  ctx_lens [B] int32
+ *   parents     [B, R] int32 or NULL
  *   out         [B, R, Hq, d_v]
  * Requirements: R = D+1 <= 16; block_size == 64; Hq % Hkv == 0;
  *   GQA/MHA: d_qk == d_v, a multiple of 32, <= 256 (bf16: 64 or 128);
@@ -124,6 +134,7 @@ typedef struct {
   int32_t block_size, max_blocks, num_blocks, is_mla;
   float sm_scale;
   int32_t dtype;             /* mtp_dtype */
+  const int32_t* parents;    /* [B, R] tree drafts, NULL: chains */
   void* workspace;           /* device, >= mtp_attention_workspace_size() bytes */
   size_t workspace_bytes;
   void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just
@@ -163,6 +174,16 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  *     the first rejection j* and emit a draw from normalised
  *     max(0, p_j* - q_j*) (from p_j* if that is zero everywhere); if every
  *     draft is accepted emit a draw from p_D.
+ *   tree drafts (`parents` given; "MTP in TensorRT-LLM on Blackwell", future
+ *   work: tree speculative sampling): row j is node j of a tree as in
+ *   mtp_verify_attention, tokens[b][k] the draft token of node k >= 1.
+ *   Trees are verified greedily: node u is accepted when every node on the
+ *   path from the root to u carries the argmax of its parent's row; the
+ *   accepted node of greatest depth (lowest index among equally deep ones)
+ *   ends the path u_0 = 0, u_1 .. u_n; out_tokens[b] = [tokens[u_1] ..
+ *   tokens[u_n], argmax(row u_n)]. A tree request with mode 1 (temperature
+ *   > 0) or mode 2 sets MTP_ERR_MODE and is verified greedily; a malformed
+ *   parents list sets MTP_ERR_TREE and that request is verified as a chain.
  * Random numbers: Philox4x32-10 (Salmon et al., SC'11), key = seed (low,
  * high 32 bits), counter = (b, j, v, tag), output word 0:
  *   U_j   = (x >> 8) * 2^-24                                   tag 1, v = 0
@@ -175,8 +196,8 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  *   mode        [B] uint8 (0 greedy, 1 rejection sampling, 2 relaxed)
  *   temperature [B] float (NULL allowed when no request samples)
  *   q_draft     [B, D, V] float, the drafter's distributions (NULL allowed
- *               when no request samples); only rows of sampling requests
- *               are read.
+ *               when no request samples, or when D = 0); only rows of
+ *               sampling requests are read.
  * Outputs:
  *   out_tokens   [B, R] int32: n+1 emitted tokens then -1
  *   num_accepted [B] int32: n in [0, D] (tokens emitted = n + 1)
@@ -188,6 +209,9 @@ int mtp_verify_attention(const mtp_attn_args* args, void* stream);
  *   lse_out      [B*R] float (optional): log-sum-exp of row (scaled) logits
  *   argmax_out   [B*R] int32 (optional): argmax of row, lowest id on ties
  *   logits_debug [B*R, V] float (optional, validation only): scaled logits
+ *   accepted_nodes [B, R] int32 (optional): the accepted path's nodes u_0 = 0,
+ *                u_1 .. u_n, then -1 (for a chain: 0 .. n); the input of
+ *                mtp_tree_kv_compact
  * dtype MTP_F32 takes H a multiple of 4; MTP_BF16 takes H a multiple of 64.
  */
 typedef struct {
@@ -209,6 +233,8 @@ typedef struct {
   int32_t any_sampling;      /* 0: every request is greedy (q_draft/temperature unused) */
   int32_t relaxed_topk;      /* N of the relaxed rule (0: no request uses mode 2), <= V */
   float relaxed_delta;       /* delta of the relaxed rule, >= 0 */
+  const int32_t* parents;    /* [B, R] tree drafts, NULL: chains */
+  int32_t* accepted_nodes;   /* [B, R] optional output */
   void* workspace;           /* device, >= mtp_lmhead_workspace_size() bytes */
   size_t workspace_bytes;
   void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just
@@ -275,6 +301,37 @@ typedef struct {
 
 size_t mtp_draft_workspace_size(const mtp_draft_args* args);
 int mtp_draft_argmax(const mtp_draft_args* args, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* 2d. KV compaction after a tree verify.
+ *
+ * Defined by: "MTP in TensorRT-LLM on Blackwell", future work: tree
+ * speculative sampling, read with the rollback of the MTP Vanilla / Eagle
+ * sections (the K/V of every draft that was not accepted is removed). The
+ * verify call appended node k's K/V at slot ctx+k; the kept sequence is the
+ * input token and the accepted path, so for i = 1 .. num_accepted[b] the K/V
+ * of slot ctx + accepted_nodes[b][i] moves to slot ctx+i (in increasing i,
+ * which never overwrites a slot a later move still reads: path nodes
+ * increase). kv_rollback then trims the sequence to ctx + n + 1 and frees
+ * blocks as for a chain. A chain path (accepted_nodes[b][i] = i) moves
+ * nothing. Cache layouts as in mtp_verify_attention; ctx_lens is the
+ * context length before the step (kv_rollback's seq_lens on entry).
+ * Errors: num_accepted outside [0, D] sets MTP_ERR_ACCEPTED, a path that
+ * does not start at 0 or does not increase sets MTP_ERR_TREE, a block id
+ * outside [0, num_blocks) sets MTP_ERR_BLOCK_ID; that request is skipped. */
+typedef struct {
+  void* k_cache;
+  void* v_cache;                  /* NULL for MLA */
+  const int32_t* block_table;
+  const int32_t* ctx_lens;
+  const int32_t* accepted_nodes;  /* [B, D+1] */
+  const int32_t* num_accepted;    /* [B] */
+  int32_t B, D, Hkv, d_qk, d_v;
+  int32_t block_size, max_blocks, num_blocks, is_mla;
+  int32_t dtype;                  /* mtp_dtype */
+} mtp_kv_compact_args;
+
+int mtp_tree_kv_compact(const mtp_kv_compact_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* 3. KV-cache rollback.
@@ -348,7 +405,7 @@ int mtp_last_launch_count(void);
 
 /* ABI version (MTP_ABI_VERSION) and sizeof of the argument structs
  * (0 = mtp_attn_args, 1 = mtp_lmhead_args, 2 = mtp_rollback_args,
- * 3 = mtp_draft_args), for
+ * 3 = mtp_draft_args, 4 = mtp_kv_compact_args), for
  * bindings to check their struct layouts against. */
 int mtp_abi_version(void);
 size_t mtp_abi_struct_size(int which);

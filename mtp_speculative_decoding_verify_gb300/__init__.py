@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     kv_rollback,
     lib,
     mtp_draft_argmax,
+    mtp_tree_kv_compact,
     mtp_verify_attention,
     mtp_verify_logits_accept,
     mtp_verify_logits_accept_noalloc,

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libmtpverify.so")
 
 MTP_OK, MTP_INVALID_ARG, MTP_UNSUPPORTED, MTP_CUDA_ERROR, MTP_DEVICE_ERROR = range(5)
-ABI_VERSION = 3   # MTP_ABI_VERSION of the header the structs below mirror
+ABI_VERSION = 4   # MTP_ABI_VERSION of the header the structs below mirror
 MTP_F32, MTP_BF16 = 0, 1
 MAX_DRAFTS = 15
 BLOCK_SIZE = 64
@@ -28,8 +28,8 @@ class AttnArgs(ctypes.Structure):
                 ("block_table", _P), ("ctx_lens", _P), ("out", _P),
                 ("B", _I), ("D", _I), ("Hq", _I), ("Hkv", _I), ("d_qk", _I), ("d_v", _I),
                 ("block_size", _I), ("max_blocks", _I), ("num_blocks", _I), ("is_mla", _I),
-                ("sm_scale", ctypes.c_float), ("dtype", _I), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
-                ("timing_events", _P * 2)]
+                ("sm_scale", ctypes.c_float), ("dtype", _I), ("parents", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
 
 
 class LmArgs(ctypes.Structure):
@@ -37,7 +37,7 @@ class LmArgs(ctypes.Structure):
                 ("q_draft", _P), ("seed", ctypes.c_uint64), ("out_tokens", _P), ("num_accepted", _P),
                 ("tie_flags", _P), ("lse_out", _P), ("argmax_out", _P), ("logits_debug", _P),
                 ("B", _I), ("D", _I), ("H", _I), ("V", _I), ("dtype", _I), ("any_sampling", _I),
-                ("relaxed_topk", _I), ("relaxed_delta", ctypes.c_float),
+                ("relaxed_topk", _I), ("relaxed_delta", ctypes.c_float), ("parents", _P), ("accepted_nodes", _P),
                 ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
 
 
@@ -45,6 +45,12 @@ class DraftArgs(ctypes.Structure):
     _fields_ = [("hidden", _P), ("lm_head", _P), ("out_tokens", _P), ("lse_out", _P), ("B", _I), ("H", _I),
                 ("V", _I), ("dtype", _I), ("workspace", _P), ("workspace_bytes", ctypes.c_size_t),
                 ("timing_events", _P * 2)]
+
+
+class KvCompactArgs(ctypes.Structure):
+    _fields_ = [("k_cache", _P), ("v_cache", _P), ("block_table", _P), ("ctx_lens", _P), ("accepted_nodes", _P),
+                ("num_accepted", _P), ("B", _I), ("D", _I), ("Hkv", _I), ("d_qk", _I), ("d_v", _I),
+                ("block_size", _I), ("max_blocks", _I), ("num_blocks", _I), ("is_mla", _I), ("dtype", _I)]
 
 
 class RollbackArgs(ctypes.Structure):
@@ -99,13 +105,15 @@ def lib():
         L.mtp_draft_workspace_size.restype = ctypes.c_size_t
         L.mtp_draft_argmax.argtypes = [ctypes.POINTER(DraftArgs), _P]
         L.mtp_draft_argmax.restype = ctypes.c_int
+        L.mtp_tree_kv_compact.argtypes = [ctypes.POINTER(KvCompactArgs), _P]
+        L.mtp_tree_kv_compact.restype = ctypes.c_int
         L.mtp_abi_version.argtypes = []
         L.mtp_abi_version.restype = ctypes.c_int
         L.mtp_abi_struct_size.argtypes = [ctypes.c_int]
         L.mtp_abi_struct_size.restype = ctypes.c_size_t
         if L.mtp_abi_version() != ABI_VERSION:
             raise RuntimeError("library ABI version %d, binding expects %d" % (L.mtp_abi_version(), ABI_VERSION))
-        for which, st in enumerate((AttnArgs, LmArgs, RollbackArgs, DraftArgs)):
+        for which, st in enumerate((AttnArgs, LmArgs, RollbackArgs, DraftArgs, KvCompactArgs)):
             if L.mtp_abi_struct_size(which) != ctypes.sizeof(st):
                 raise RuntimeError("ABI mismatch for %s" % st.__name__)
         _lib = L
@@ -160,7 +168,8 @@ def _workspace(nbytes, device, key):
     return buf
 
 
-def attn_args(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, *, sm_scale=None, workspace=None):
+def attn_args(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, *, sm_scale=None, workspace=None,
+              parents=None):
     """Fill AttnArgs from tensors (see mtp_verify_attention for shapes)."""
     is_mla = v_cache is None
     B, R, Hq, d_qk = q.shape
@@ -181,12 +190,13 @@ def attn_args(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, *, 
     _dev(out, "out", dt, (B, R, Hq, d_v))
     _dev(block_table, "block_table", torch.int32)
     _dev(ctx_lens, "ctx_lens", torch.int32, (B,))
+    _dev(parents, "parents", torch.int32, (B, R))
     if dk != d_qk:
         raise ValueError("k_cache head dim %d != q head dim %d" % (dk, d_qk))
     a = AttnArgs(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                  _ptr(ctx_lens), _ptr(out), B, D, Hq, Hkv, d_qk, d_v, bs, block_table.shape[1], num_blocks,
                  int(is_mla), float(sm_scale if sm_scale is not None else d_qk ** -0.5), _dtype_code(q),
-                 None, 0)
+                 _ptr(parents), None, 0)
     n = lib().mtp_attention_workspace_size(ctypes.byref(a))
     if n == 0:
         _check(MTP_INVALID_ARG)
@@ -198,20 +208,22 @@ def attn_args(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, *, 
 
 
 def mtp_verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, *, sm_scale=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, parents=None):
     """Append the verify tokens' K/V to the paged cache and run verify attention into `out`.
 
     q [B, R, Hq, d_qk]; GQA/MHA: k_new [B, R, Hkv, d], v_new [B, R, Hkv, d], caches [blocks, 64, Hkv, d];
     absorbed MLA: k_new [B, R, 576], v_new = v_cache = None, k_cache [blocks, 64, 1, 576];
-    block_table [B, max_blocks] int32, ctx_lens [B] int32, out [B, R, Hq, d_v].
+    block_table [B, max_blocks] int32, ctx_lens [B] int32, out [B, R, Hq, d_v];
+    parents [B, R] int32 (tree drafts) or None (chains).
     """
     a = attn_args(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, out, sm_scale=sm_scale,
-                  workspace=workspace)
+                  workspace=workspace, parents=parents)
     _check(lib().mtp_verify_attention(ctypes.byref(a), _stream_handle(stream)))
 
 
 def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
-            lse_out=None, argmax_out=None, logits_debug=None, workspace=None, relaxed_topk=0, relaxed_delta=0.0):
+            lse_out=None, argmax_out=None, logits_debug=None, workspace=None, relaxed_topk=0, relaxed_delta=0.0,
+            parents=None, accepted_nodes=None):
     """Fill LmArgs from tensors (see mtp_verify_logits_accept for shapes)."""
     B, R = tokens.shape
     D = R - 1
@@ -230,10 +242,12 @@ def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_token
     _dev(lse_out, "lse_out", torch.float32, (B, R))
     _dev(argmax_out, "argmax_out", torch.int32, (B, R))
     _dev(logits_debug, "logits_debug", torch.float32, (B * R, V))
+    _dev(parents, "parents", torch.int32, (B, R))
+    _dev(accepted_nodes, "accepted_nodes", torch.int32, (B, R))
     a = LmArgs(_ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(mode), _ptr(temperature), _ptr(q_draft),
                int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_tokens), _ptr(num_accepted), _ptr(tie_flags), _ptr(lse_out),
                _ptr(argmax_out), _ptr(logits_debug), B, D, H, V, _dtype_code(lm_head), int(any_sampling),
-               int(relaxed_topk), float(relaxed_delta), None, 0)
+               int(relaxed_topk), float(relaxed_delta), _ptr(parents), _ptr(accepted_nodes), None, 0)
     n = lib().mtp_lmhead_workspace_size(ctypes.byref(a))
     if n == 0:
         _check(MTP_INVALID_ARG)
@@ -246,16 +260,17 @@ def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_token
 
 def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted,
                              tie_flags, lse_out=None, argmax_out=None, logits_debug=None, workspace=None,
-                             stream=None, relaxed_topk=0, relaxed_delta=0.0):
+                             stream=None, relaxed_topk=0, relaxed_delta=0.0, parents=None, accepted_nodes=None):
     """LM head + streaming softmax statistics + greedy / rejection-sampling / relaxed acceptance.
 
     hidden [B*R, H], lm_head [V, H] (float32 or bfloat16), tokens [B, R] int32, mode [B] uint8,
     temperature [B] float32 or None, q_draft [B, D, V] float32 or None (None: every request greedy),
     outputs out_tokens [B, R] int32, num_accepted [B] int32, tie_flags [B] uint8, optional lse_out / argmax_out
     [B, R] and logits_debug [B*R, V]. relaxed_topk / relaxed_delta: the relaxed rule of mode-2 requests.
+    parents [B, R] int32: tree drafts (greedy); accepted_nodes [B, R] int32: optional output, the accepted path.
     """
     a = lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
-                lse_out, argmax_out, logits_debug, workspace, relaxed_topk, relaxed_delta)
+                lse_out, argmax_out, logits_debug, workspace, relaxed_topk, relaxed_delta, parents, accepted_nodes)
     _check(lib().mtp_verify_logits_accept(ctypes.byref(a), _stream_handle(stream)))
 
 
@@ -290,7 +305,8 @@ def mtp_draft_argmax(hidden, lm_head, out_tokens, lse_out=None, workspace=None, 
 
 def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens,
                                      num_accepted, tie_flags, lse_out=None, argmax_out=None, logits_debug=None,
-                                     stream=None, relaxed_topk=0, relaxed_delta=0.0):
+                                     stream=None, relaxed_topk=0, relaxed_delta=0.0, parents=None,
+                                     accepted_nodes=None):
     """mtp_verify_logits_accept for callers that cannot allocate device memory:
     the scratch lives in a fixed array owned by the library (no workspace is
     allocated or passed). Raises MtpError if the batch needs more scratch
@@ -299,13 +315,39 @@ def mtp_verify_logits_accept_noalloc(hidden, lm_head, tokens, mode, temperature,
                int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out_tokens), _ptr(num_accepted), _ptr(tie_flags), _ptr(lse_out),
                _ptr(argmax_out), _ptr(logits_debug), tokens.shape[0], tokens.shape[1] - 1, lm_head.shape[1],
                lm_head.shape[0], _dtype_code(lm_head), int(q_draft is not None), int(relaxed_topk),
-               float(relaxed_delta), None, 0)
+               float(relaxed_delta), _ptr(parents), _ptr(accepted_nodes), None, 0)
     for t, n in ((hidden, "hidden"), (lm_head, "lm_head"), (tokens, "tokens"), (mode, "mode"),
                  (temperature, "temperature"), (q_draft, "q_draft"), (out_tokens, "out_tokens"),
                  (num_accepted, "num_accepted"), (tie_flags, "tie_flags"), (lse_out, "lse_out"),
-                 (argmax_out, "argmax_out"), (logits_debug, "logits_debug")):
+                 (argmax_out, "argmax_out"), (logits_debug, "logits_debug"), (parents, "parents"),
+                 (accepted_nodes, "accepted_nodes")):
         _dev(t, n)
     _check(lib().mtp_verify_logits_accept_noalloc(ctypes.byref(a), _stream_handle(stream)))
+
+
+def compact_args(k_cache, v_cache, block_table, ctx_lens, accepted_nodes, num_accepted):
+    """Fill KvCompactArgs from tensors (see mtp_tree_kv_compact)."""
+    B, R = accepted_nodes.shape
+    is_mla = v_cache is None
+    num_blocks, bs, Hkv, d_qk = k_cache.shape
+    d_v = d_qk if is_mla else v_cache.shape[-1]
+    dt = k_cache.dtype
+    _dev(k_cache, "k_cache", dt)
+    _dev(v_cache, "v_cache", dt, (num_blocks, bs, Hkv, d_v))
+    _dev(block_table, "block_table", torch.int32)
+    _dev(ctx_lens, "ctx_lens", torch.int32, (B,))
+    _dev(accepted_nodes, "accepted_nodes", torch.int32, (B, R))
+    _dev(num_accepted, "num_accepted", torch.int32, (B,))
+    return KvCompactArgs(_ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), _ptr(accepted_nodes),
+                         _ptr(num_accepted), B, R - 1, Hkv, d_qk, d_v, bs, block_table.shape[1], num_blocks,
+                         int(is_mla), _dtype_code(k_cache))
+
+
+def mtp_tree_kv_compact(k_cache, v_cache, block_table, ctx_lens, accepted_nodes, num_accepted, stream=None):
+    """Move each request's accepted tree path K/V (accepted_nodes [B, R], num_accepted [B]) to slots
+    ctx+1 .. ctx+n of the paged cache (ctx_lens = context lengths before the step); v_cache None for MLA."""
+    a = compact_args(k_cache, v_cache, block_table, ctx_lens, accepted_nodes, num_accepted)
+    _check(lib().mtp_tree_kv_compact(ctypes.byref(a), _stream_handle(stream)))
 
 
 def rollback_args(block_table, seq_lens, num_accepted, free_list, free_count, *, D):

@@ -15,6 +15,10 @@
 // TensorRT-LLM on Blackwell", MTP optimization: relaxed acceptance): a draft
 // is accepted while it ranks among the row's relaxed_topk largest logits and
 // p(d) >= p(top-1) - relaxed_delta; the first miss is replaced by the argmax.
+// Tree drafts ("MTP in TensorRT-LLM on Blackwell", future work: tree
+// speculative sampling) are verified greedily edge by edge: a node is
+// accepted when its whole root path matches the parents' argmaxes, and the
+// deepest accepted node (lowest index on equal depth) ends the emitted path.
 //
 // The redraw uses the residual max(0, p - q) (normalised) so that the
 // emitted tokens follow p exactly; a categorical draw is an exponential race
@@ -51,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
     Decision* __restrict__ dec, int* __restrict__ race_count, int32_t* __restrict__ out_tokens,
     int32_t* __restrict__ num_accepted, uint8_t* __restrict__ tie_flags, float* __restrict__ lse_out,
     int32_t* __restrict__ argmax_out, const int* __restrict__ rcnt, int relaxed_topk, float relaxed_delta,
-    unsigned* err) {
+    const int32_t* __restrict__ parents, int32_t* __restrict__ accepted_nodes, unsigned* err) {
   __shared__ float s_lse[kMaxRows];
   __shared__ float s_top[kMaxRows];
   __shared__ int s_amax[kMaxRows];
@@ -113,9 +117,50 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
     for (int j = 0; j < R; ++j) bad |= (tok[j] < 0 || tok[j] >= V);
   if (bad) raise_error(err, MTP_ERR_TOKEN_ID);
   if (md > 2 || (md == 2 && !relaxed)) raise_error(err, MTP_ERR_MODE);   // decided greedily
-  const bool sampling = any_sampling && md == 1 && temperature[b] > 0.0f;
+  bool sampling = any_sampling && md == 1 && temperature[b] > 0.0f;
   int n = 0, tie = 0;
-  if (relaxed && !bad) {
+  // Tree requests: validate the parents list and find the deepest accepted node.
+  int tree_end = -1;          // >= 0: the accepted path ends at this node
+  int par[kMaxRows];
+  if (parents && !bad) {
+    if (sampling || md == 2) raise_error(err, MTP_ERR_MODE);   // trees are verified greedily
+    sampling = false;
+    const int32_t* pb = parents + (int64_t)b * R;
+    bool ok = pb[0] == -1;
+    int depth[kMaxRows];
+    bool acc[kMaxRows];
+    depth[0] = 0;
+    acc[0] = true;
+    int best = 0;
+    for (int k = 1; ok && k < R; ++k) {
+      const int pk = pb[k];
+      ok = pk >= 0 && pk < k;
+      if (!ok) break;
+      par[k] = pk;
+      acc[k] = acc[pk] && tok[k] == s_amax[pk];
+      depth[k] = depth[pk] + 1;
+      if (acc[k] && depth[k] > depth[best]) best = k;
+    }
+    if (ok) tree_end = best;
+    else raise_error(err, MTP_ERR_TREE);   // verified as a chain
+  }
+  if (tree_end >= 0) {
+    n = 0;
+    for (int k = tree_end; k > 0; k = par[k]) ++n;
+    // walk back from the end: path node i sits at depth i
+    int k = tree_end;
+    for (int i = n; i >= 1; --i) {
+      out[i - 1] = tok[k];
+      if (accepted_nodes) accepted_nodes[(int64_t)b * R + i] = k;
+      k = par[k];
+    }
+    out[n] = s_amax[tree_end];
+    for (int j = n + 1; j < R; ++j) out[j] = -1;
+    if (accepted_nodes) {
+      accepted_nodes[(int64_t)b * R] = 0;
+      for (int j = n + 1; j < R; ++j) accepted_nodes[(int64_t)b * R + j] = -1;
+    }
+  } else if (relaxed && !bad) {
     for (; n < D; ++n) {
       const int d = tok[n + 1];
       const int before = s_cnt[n][0], sure = s_cnt[n][1], maybe = s_cnt[n][2];
@@ -141,6 +186,8 @@ __global__ void __launch_bounds__(kThreads) accept_decide_kernel(
     }
     for (int j = 0; j < R; ++j) out[j] = j < n ? tok[j + 1] : -1;  // out[n] comes from the race
   }
+  if (accepted_nodes && tree_end < 0)
+    for (int j = 0; j < R; ++j) accepted_nodes[(int64_t)b * R + j] = j <= n ? j : -1;
   dec[b] = Decision{n, (sampling && !bad) ? 1 : 0, tie, 0};
   race_count[b] = 0;
   if (num_accepted) num_accepted[b] = n;
@@ -232,7 +279,7 @@ cudaError_t launch_accept(const mtp_lmhead_args& a, const LmPlan& p, unsigned* e
       a.q_draft, a.any_sampling, a.seed, a.B, a.D, a.V, (float*)(ws + p.off_lse), (int*)(ws + p.off_amax),
       (Decision*)(ws + p.off_dec), (int*)(ws + p.off_count), a.out_tokens, a.num_accepted, a.tie_flags, a.lse_out,
       a.argmax_out, a.relaxed_topk > 0 ? (const int*)(ws + p.off_rcnt) : nullptr, a.relaxed_topk, a.relaxed_delta,
-      err);
+      a.parents, a.accepted_nodes, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !a.any_sampling) return e;
   dim3 grid(a.B, p.race_slices);

@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(
     const T* __restrict__ q, const T* __restrict__ k_cache, const T* __restrict__ v_cache,
     const int32_t* __restrict__ block_table, const int32_t* __restrict__ ctx_lens, T* __restrict__ out,
     float* __restrict__ part_o, float* __restrict__ part_lse, int R, int Hq, int Hkv, int group, int max_blocks,
-    int num_blocks, int split_len, int n_splits, int is_mla, float sm_scale, unsigned* err) {
+    int num_blocks, int split_len, int n_splits, int is_mla, float sm_scale, const int32_t* __restrict__ parents,
+    unsigned* err) {
   constexpr int DQ = EQ * kWarp, DV = EV * kWarp;
   const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
   const int split = blockIdx.x;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(
   const int t0 = split * split_len;
   if (t0 >= L) return;
   const int t1 = min(L, t0 + split_len);
+  const uint32_t path = tree_path_mask(parents, b, R, j, err);   // visible verify keys of this row
 
   const int64_t row = ((int64_t)b * R + j) * Hq + h;
   float qv[EQ];
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(256) attention_simt_kernel(
   const int kv_heads = is_mla ? 1 : Hkv;
   const int32_t* tbl = block_table + (int64_t)b * max_blocks;
   for (int t = t0; t < t1; ++t) {
+    if (tree_hidden(t, ctx, path)) continue;
     const int blk = tbl[t / kBlock];
     if (blk < 0 || blk >= num_blocks) {
       if (lane == 0) raise_error(err, MTP_ERR_BLOCK_ID);
@@ -198,7 +201,8 @@ static void run_simt(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, c
   float* pl = p.n_splits > 1 ? (float*)((char*)a.workspace + p.ws_partial_lse) : nullptr;
   attention_simt_kernel<T, EQ, EV><<<grid, 256, 0, s>>>(
       (const T*)a.q, (const T*)a.k_cache, (const T*)a.v_cache, a.block_table, a.ctx_lens, (T*)a.out, po, pl, R,
-      a.Hq, kv_heads, group, a.max_blocks, a.num_blocks, p.split_len, p.n_splits, a.is_mla, a.sm_scale, err);
+      a.Hq, kv_heads, group, a.max_blocks, a.num_blocks, p.split_len, p.n_splits, a.is_mla, a.sm_scale, a.parents,
+      err);
 }
 
 cudaError_t launch_attention_simt(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s) {

@@ -80,7 +80,7 @@ constexpr int kMaxCluster = MTP_MLA_MAX_CLUSTER;   // CTAs (row blocks) sharing 
 constexpr int kQOff = 0;                                    // 9 x 8 KB
 constexpr int kSlotOff = kQOff + kQChunks * 8192;           // 73728
 constexpr int kRedOff = kSlotOff + kSlots * kSlotBytes;     // red_max[4][64], red_sum[4][64]
-constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;           // m_run, l_run, m_ref, scale [64] floats, lim [64] int, shift [64]
+constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;           // m_run, l_run, m_ref, scale [64] floats, path [64] u32, shift [64]
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
 constexpr int kNumBars = 2 * kSlots + 1 + 2 * kSBufs + 1 + 1 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;            // tmem base, abort, rescale flag
@@ -97,6 +97,7 @@ struct Params {
   const int32_t* block_table;
   const int32_t* ctx_lens;
   const int32_t* order;   // work items, longest first (mla_schedule_kernel)
+  const int32_t* parents; // [B, R] tree drafts, nullptr: chains
   unsigned* err;
   int B, R, Hq, max_blocks, num_blocks, split_len, n_splits;
   int groups;           // row-block clusters per request
@@ -269,6 +270,9 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// kTree: rows see the verify keys of their root path (tree drafts); the chain
+// instantiation keeps each row's plain key limit ctx + j in the same array.
+template <bool kTree>
 __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                   const __grid_constant__ CUtensorMap tm_kv,
                                                                   const Params p) {
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   float* l_run = m_run + 64;
   float* m_ref = m_run + 128;
   float* rscale = m_run + 192;
-  int* lim = reinterpret_cast<int*>(m_run + 256);
+  uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 256);   // per row: path mask (tree) or key limit (chain)
   float* m_shift = m_run + 320;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kSlots]: slot c holds this tile's chunk c
   uint64_t* empty = full + kSlots;                                  // [kSlots]: every cluster CTA is done with it
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   }
   if (threadIdx.x < kRows) {
     const int rr = min(row_base + (int)threadIdx.x, rows - 1);
-    lim[threadIdx.x] = ctx + rr / p.Hq;
+    path[threadIdx.x] = kTree ? tree_path_mask(p.parents, b, p.R, rr / p.Hq, p.err) : (uint32_t)(ctx + rr / p.Hq);
     m_run[threadIdx.x] = -INFINITY;
     m_ref[threadIdx.x] = 0.0f;   // reference max the softmax warps start from
     l_run[threadIdx.x] = 0.0f;
@@ -361,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
     float acc[16];
 #pragma unroll
     for (int x = 0; x < 16; ++x) acc[x] = 0.0f;
-    const int lim_min = ctx + row_base / p.Hq;   // smallest key limit of the block's rows
+    // first key some row of the block may not see: after the first row's own key for a chain, the
+    // first verify key for a tree
+    const int mask_from = kTree ? ctx : ctx + row_base / p.Hq + 1;
     // Every softmax warp runs the same sequence of named barriers for every
     // tile; after an abort the tensor-memory work is skipped but the barrier
     // sequence is kept, so no warp is left waiting on the others.
@@ -388,10 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
         for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
       }
       const int tile0 = t0 + i * kKeys;
-      if (tile0 + kKeys - 1 > lim_min || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
+      if (tile0 + kKeys - 1 >= mask_from || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
         const int key = tile0 + 32 * qq + lane;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) d[x] = (key > lim[cq * 16 + x] || key >= t_end) ? -INFINITY : d[x];
+        for (int x = 0; x < 16; ++x)
+          d[x] = (key >= t_end || (kTree ? tree_hidden(key, ctx, path[cq * 16 + x]) : key > (int)path[cq * 16 + x]))
+                     ? -INFINITY
+                     : d[x];
       }
       // The reference only moves when a score exceeds it by more than
       // kLazyRescale: then (and on the first tile) the tile's row maxima are
@@ -681,7 +690,7 @@ constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]
 constexpr int kVOff = kKOff + 9 * 8192;           // 8 x [64 keys x 64 dv]: slot (h * 2 + kb) * 2 + j
 constexpr int kPOff = kVOff + 8 * 8192;           // P [64 rows x 128 keys]: keys 0..63, then 64..127
 constexpr int kRedOff = kPOff + 8192;             // red_max[8][64], red_sum[8][64] alias P keys 64..127
-constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, lim [64] i32
+constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, path [64] u32
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
 constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull uses 3 of its 9)
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
@@ -690,6 +699,7 @@ constexpr uint32_t kColO = 0;                     // O of product h at columns 1
 constexpr uint32_t kColS = 256;                   // S buffer b at 256 + 64 b
 }  // namespace pr
 
+template <bool kTree>
 __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                     const __grid_constant__ CUtensorMap tm_kv,
                                                                     const Params p) {
@@ -702,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   float* rscale = m_run + 128;
   float* m_shift = m_run + 192;
   float* l_run = m_run + 256;
-  int* lim = reinterpret_cast<int*>(m_run + 320);
+  uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 320);   // per row: path mask (tree) or key limit (chain)
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // leader: both CTAs' 9 K chunks landed
   uint64_t* kempty = kfull + 9;                                         // both: the K slots are free
   uint64_t* vfull = kempty + 9;                                         // leader: both CTAs' 8 V boxes landed
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   }
   if (threadIdx.x < kRows) {
     const int rr = min(row_base + (int)threadIdx.x, rows - 1);
-    lim[threadIdx.x] = ctx + rr / p.Hq;
+    path[threadIdx.x] = kTree ? tree_path_mask(p.parents, b, p.R, rr / p.Hq, p.err) : (uint32_t)(ctx + rr / p.Hq);
     m_run[threadIdx.x] = -INFINITY;
     m_ref[threadIdx.x] = 0.0f;
   }
@@ -777,8 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
     const int part = khalf * 4 + sub;                 // which of the row's 8 partials this thread holds
     const int st = sw * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    const int lim_r = lim[r];
-    const int lim_min = ctx + row_base / p.Hq;
+    const uint32_t path_r = path[r];
+    const int mask_from = kTree ? ctx : ctx + row_base / p.Hq + 1;   // first key some row may not see
     float acc = 0.0f;                                 // partial row sum over this thread's keys
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
@@ -799,10 +809,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
       }
       const int tile0 = t0 + i * kKeys;
-      if (tile0 + kKeys - 1 > lim_min || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
+      if (tile0 + kKeys - 1 >= mask_from || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
         const int key0 = tile0 + 64 * khalf + 16 * sub;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) d[x] = (key0 + x > lim_r || key0 + x >= t_end) ? -INFINITY : d[x];
+        for (int x = 0; x < 16; ++x)
+          d[x] = (key0 + x >= t_end || (kTree ? tree_hidden(key0 + x, ctx, path_r) : key0 + x > (int)path_r))
+                     ? -INFINITY
+                     : d[x];
       }
       bool exceed = (i == 0);
 #pragma unroll
@@ -1134,6 +1147,7 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   p.block_table = a.block_table;
   p.ctx_lens = a.ctx_lens;
   p.order = (const int32_t*)((const char*)a.workspace + pl.ws_order);
+  p.parents = a.parents;
   p.err = err;
   p.B = a.B;
   p.R = R;
@@ -1157,8 +1171,10 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int smem_bytes = paired ? pr::kSmemBytes : kSmemBytes;
-  e = paired ? cudaFuncSetAttribute(attn_mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)
-             : cudaFuncSetAttribute(attn_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  const bool tree = a.parents != nullptr;
+  auto kern = paired ? (tree ? attn_mla_pair_kernel<true> : attn_mla_pair_kernel<false>)
+                     : (tree ? attn_mla_tc_kernel<true> : attn_mla_tc_kernel<false>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_items * C, 1, 1);
@@ -1172,8 +1188,7 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = paired ? cudaLaunchKernelEx(&cfg, attn_mla_pair_kernel, tq, tkv, p)
-             : cudaLaunchKernelEx(&cfg, attn_mla_tc_kernel, tq, tkv, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tq, tkv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -43,6 +43,7 @@ struct AttnKParams {
   float* part_lse;
   const int32_t* block_table;
   const int32_t* ctx_lens;
+  const int32_t* parents;        // [B, R] tree drafts, nullptr: chains
   unsigned* err;
   int R, Hq, Hkv, group, rows;  // rows = query rows per (request, KV head)
   int max_blocks, num_blocks, split_len, n_splits, stages;
@@ -60,7 +61,9 @@ struct GqaCfg {
   static constexpr int kStageBytes = 2 * kKBytes;              // K and V
 };
 
-template <int D>
+// kTree: rows see the verify keys of their root path (tree drafts) instead of
+// a causal prefix; the chain instantiation keeps the plain limit test.
+template <int D, bool kTree>
 __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                        const __grid_constant__ CUtensorMap tm_v,
                                                        const AttnKParams p) {
@@ -152,6 +155,9 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
   const int j_lo = rl / p.group, j_hi = rh / p.group;
   const int h_lo = kvh * p.group + rl % p.group, h_hi = kvh * p.group + rh % p.group;
   const int lim_lo = ctx + j_lo, lim_hi = ctx + j_hi;
+  const uint32_t path_lo = kTree ? tree_path_mask(p.parents, b, p.R, j_lo, p.err) : 0u;   // visible verify keys
+  const uint32_t path_hi = kTree ? tree_path_mask(p.parents, b, p.R, j_hi, p.err) : 0u;
+  const int mask_from = kTree ? ctx : min(lim_lo, lim_hi) + 1;   // first key a row may not see
   const int64_t qrow_lo = ((int64_t)b * p.R + j_lo) * p.Hq + h_lo;
   const int64_t qrow_hi = ((int64_t)b * p.R + j_hi) * p.Hq + h_hi;
 
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
       }
       // Scale, causal mask, online softmax (rows r_lo / r_hi).
       const int tk = (page0 + i) * C::kTileKeys;
-      const bool need_mask = tk + C::kTileKeys - 1 > min(lim_lo, lim_hi);
+      const bool need_mask = tk + C::kTileKeys - 1 >= mask_from;
       float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
@@ -214,7 +220,9 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
           float v = s[n][e] * p.scale_log2;
           if (need_mask) {
             const int key = tk + n * 8 + 2 * t + (e & 1);
-            if (key > ((e < 2) ? lim_lo : lim_hi)) v = -INFINITY;
+            const bool hidden = kTree ? tree_hidden(key, ctx, (e < 2) ? path_lo : path_hi)
+                                      : key > ((e < 2) ? lim_lo : lim_hi);
+            if (hidden) v = -INFINITY;
           }
           s[n][e] = v;
         }
@@ -329,6 +337,7 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
   p.part_lse = pl.n_splits > 1 ? (float*)((char*)a.workspace + pl.ws_partial_lse) : nullptr;
   p.block_table = a.block_table;
   p.ctx_lens = a.ctx_lens;
+  p.parents = a.parents;
   p.err = err;
   p.R = R;
   p.Hq = a.Hq;
@@ -343,10 +352,11 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
   p.scale_log2 = a.sm_scale * kLog2e;
   const int warps = std::min(kGqaRowsPerCta / 16, (rows + 15) / 16);
   const int smem = gqa_smem_bytes<D>(stages);
-  cudaError_t e = cudaFuncSetAttribute(attn_gqa_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = a.parents ? attn_gqa_kernel<D, true> : attn_gqa_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(pl.n_splits, a.B * a.Hkv, (rows + kGqaRowsPerCta - 1) / kGqaRowsPerCta);
-  attn_gqa_kernel<D><<<grid, 32 * (warps + 1), smem, s>>>(tk, tv, p);
+  kern<<<grid, 32 * (warps + 1), smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 

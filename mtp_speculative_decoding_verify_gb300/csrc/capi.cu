@@ -122,8 +122,8 @@ int check_lm(const mtp_lmhead_args* a) {
   if (a->B > 0 && (!a->hidden || !a->lm_head || !a->tokens || !a->mode || !a->out_tokens || !a->num_accepted ||
                    !a->tie_flags))
     return fail(MTP_INVALID_ARG, "a required pointer is NULL");
-  if (a->any_sampling && a->B > 0 && (!a->q_draft || !a->temperature))
-    return fail(MTP_INVALID_ARG, "any_sampling = 1 needs q_draft and temperature");
+  if (a->any_sampling && a->B > 0 && (!a->temperature || (a->D > 0 && !a->q_draft)))
+    return fail(MTP_INVALID_ARG, "any_sampling = 1 needs temperature, and q_draft when D > 0");
   if (a->relaxed_topk < 0 || a->relaxed_topk > a->V)
     return fail(MTP_INVALID_ARG, "relaxed_topk = %d outside [0, V]", a->relaxed_topk);
   if (a->relaxed_topk > 0 && !(a->relaxed_delta >= 0.0f && a->relaxed_delta <= 1e30f))
@@ -209,6 +209,7 @@ size_t mtp_abi_struct_size(int which) {
     case 1: return sizeof(mtp_lmhead_args);
     case 2: return sizeof(mtp_rollback_args);
     case 3: return sizeof(mtp_draft_args);
+    case 4: return sizeof(mtp_kv_compact_args);
     default: return 0;
   }
 }
@@ -322,11 +323,11 @@ int mtp_sync_status(void* stream) {
   if (word == 0) return MTP_OK;
   e = cudaMemset(c->err, 0, sizeof word);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
-  return fail(MTP_DEVICE_ERROR, "device range check failed: 0x%x%s%s%s%s%s%s%s", word,
+  return fail(MTP_DEVICE_ERROR, "device range check failed: 0x%x%s%s%s%s%s%s%s%s", word,
               (word & MTP_ERR_BLOCK_ID) ? " block-id" : "", (word & MTP_ERR_TOKEN_ID) ? " token-id" : "",
               (word & MTP_ERR_LENGTH) ? " length" : "", (word & MTP_ERR_ACCEPTED) ? " num-accepted" : "",
               (word & MTP_ERR_FREE_LIST) ? " free-list" : "", (word & MTP_ERR_TIMEOUT) ? " timeout" : "",
-              (word & MTP_ERR_MODE) ? " mode" : "");
+              (word & MTP_ERR_MODE) ? " mode" : "", (word & MTP_ERR_TREE) ? " tree" : "");
 }
 
 }  // extern "C"

@@ -78,6 +78,35 @@ __device__ __forceinline__ RowStat warp_merge(RowStat v) {
   return v;
 }
 
+// Tree drafts ("MTP in TensorRT-LLM on Blackwell", future work: tree
+// speculative sampling, Fig. 9): node 0 of a request is the input token and
+// node k >= 1 hangs under parents[k] < k. Bit k of a row's path mask is set
+// iff node k is on the path from the root to the row's node (itself
+// included); a chain (parents == nullptr) gives bits 0..j. A malformed list
+// (parents[0] != -1, or some parents[k] outside [0, k)) raises MTP_ERR_TREE
+// and yields the chain mask for every row of the request. R <= 16.
+__device__ __forceinline__ uint32_t tree_path_mask(const int32_t* parents, int b, int R, int j, unsigned* err) {
+  const uint32_t chain = (2u << j) - 1u;
+  if (!parents) return chain;
+  const int32_t* par = parents + (int64_t)b * R;
+  bool ok = par[0] == -1;
+  for (int k = 1; k < R; ++k) ok = ok && par[k] >= 0 && par[k] < k;
+  if (!ok) {
+    raise_error(err, MTP_ERR_TREE);
+    return chain;
+  }
+  uint32_t m = 0;
+  for (int k = j; k >= 0; k = par[k]) m |= 1u << k;   // parents decrease: at most j + 1 steps
+  return m;
+}
+
+// Key t of a request with ctx cached keys is hidden from a row whose path
+// mask is m: t is a verify key (t >= ctx) of a node off the row's root path.
+__device__ __forceinline__ bool tree_hidden(int t, int ctx, uint32_t m) {
+  const int rel = t - ctx;
+  return rel >= 0 && (rel >= 32 || ((m >> rel) & 1u) == 0u);
+}
+
 // Relaxed acceptance ("MTP in TensorRT-LLM on Blackwell", MTP optimization:
 // relaxed acceptance): rank counts of draft d (logit lp) over the logits l of the
 // vocabulary entries v a CTA sees: cnt[0] entries ordered before d (larger

@@ -18,6 +18,11 @@ Workload recipe (what the five standard workloads contain):
   * for rejection-sampling requests the draft distribution of row j is
     q_j = softmax(logits_j / T + N(0, 0.5)) (logits = h W^T, a plain float32
     matmul used only to shape the input) and draft d_{j+1} ~ q_j;
+  * tree drafts: "full" trees fan out 3 ways at the root, 2 ways below, then
+    continue as chains (D = 15: 3 + 6 + 6 nodes, depth 3); "random" trees
+    give node k a uniform parent in [0, k). Node k's draft copies the
+    planted token of its parent's row with the agreement probability, else a
+    uniform token, so several branches of a node can match;
   * relaxed requests (mode 2) get sharper rows with a planted runner-up:
     h = L1 W[t] / ||W[t]||^2 + L2 W[s] / ||W[s]||^2 + N(0, 0.01) with
     L1 ~ U(ln V - 1, ln V + 3) and L2 = L1 - U(0, 3), so that token t leads
@@ -56,6 +61,7 @@ class Workload:
     relaxed: str = "none"       # "none" | "all" | "half" (first half of the batch), mode 2 over the sampling mask
     relaxed_topk: int = 0       # N of the relaxed rule
     relaxed_delta: float = 0.0  # delta of the relaxed rule
+    tree: str = "chain"         # "chain" | "full" | "random" draft trees (greedy verification)
 
     @property
     def R(self):
@@ -116,6 +122,39 @@ def _sampling_mask(w):
     m = torch.zeros(w.B, dtype=torch.bool)
     m[w.B // 2:] = True
     return m
+
+
+def full_tree_parents(R):
+    """Parents of a full tree in breadth-first order: 3 children at the root,
+    2 under each of those, then single chains under the leaves, until R nodes."""
+    parents = [-1]
+    frontier = [0]
+    fan = [3, 2]
+    level = 0
+    while len(parents) < R:
+        nxt = []
+        for u in frontier:
+            for _ in range(fan[level] if level < len(fan) else 1):
+                if len(parents) < R:
+                    parents.append(u)
+                    nxt.append(len(parents) - 1)
+        frontier = nxt if nxt else frontier
+        level += 1
+    return parents
+
+
+def make_parents(w):
+    """[B, R] int32 parents of each request's draft tree (None for chains)."""
+    if w.tree == "chain":
+        return None
+    if w.tree == "full":
+        return torch.tensor([full_tree_parents(w.R)] * w.B, dtype=torch.int32)
+    g = _gen(w, "cpu", 10)
+    par = torch.empty((w.B, w.R), dtype=torch.int32)
+    par[:, 0] = -1
+    for k in range(1, w.R):
+        par[:, k] = torch.randint(0, k, (w.B,), generator=g, dtype=torch.int32)
+    return par
 
 
 def _relaxed_mask(w):
@@ -194,6 +233,10 @@ def make_lmhead_inputs(w, device, chunk=16384):
     agree = torch.rand((w.B, w.D), generator=gc) < w.agreement
     rand_tok = torch.randint(0, w.V, (w.B, w.D), generator=gc)
     tokens[:, 1:] = torch.where(agree, planted[:, :w.D], rand_tok)
+    parents = make_parents(w)
+    if parents is not None:   # node k continues its parent's row: copy that row's planted token
+        par = parents[:, 1:].to(torch.int64)
+        tokens[:, 1:] = torch.where(agree, torch.gather(planted, 1, par), rand_tok)
     if runner is not None:
         pick = torch.rand((w.B, w.D), generator=_gen(w, "cpu", 7))
         rtok = torch.where(pick < 0.5, runner[:, :w.D], torch.where(pick < 0.75, planted[:, :w.D], rand_tok))
@@ -218,7 +261,8 @@ def make_lmhead_inputs(w, device, chunk=16384):
             tokens[b, 1:] = draws[i]
     return dict(hidden=h, lm_head=W, tokens=tokens.to(torch.int32).to(device), mode=mode.to(device),
                 temperature=temperature.to(device), q_draft=q_draft, planted=planted.to(torch.int32), seed=w.seed,
-                relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta)
+                relaxed_topk=w.relaxed_topk, relaxed_delta=w.relaxed_delta,
+                parents=None if parents is None else parents.to(device))
 
 
 def make_draft_inputs(w, device):

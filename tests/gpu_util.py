@@ -19,10 +19,10 @@ TOL_ATTN = {"f32": 1e-4, "bf16": 1e-2}
 TOL_LSE_REL = 1e-5
 
 
-def gpu_attention(w, att):
+def gpu_attention(w, att, parents=None):
     out = torch.empty((w.B, w.R, w.Hq, w.d_v), dtype=w.torch_dtype, device=att["q"].device)
     mv.mtp_verify_attention(att["q"], att["k_new"], att["v_new"], att["k_cache"], att["v_cache"],
-                            att["block_table"], att["ctx_lens"], out, sm_scale=w.sm_scale)
+                            att["block_table"], att["ctx_lens"], out, sm_scale=w.sm_scale, parents=parents)
     return out
 
 
@@ -32,13 +32,15 @@ def gpu_lmhead(w, lm, debug_logits=False):
                num_accepted=torch.full((w.B,), -9, dtype=torch.int32, device=dev),
                tie_flags=torch.full((w.B,), 255, dtype=torch.uint8, device=dev),
                lse=torch.empty((w.B, w.R), dtype=torch.float32, device=dev),
-               argmax=torch.empty((w.B, w.R), dtype=torch.int32, device=dev))
+               argmax=torch.empty((w.B, w.R), dtype=torch.int32, device=dev),
+               accepted_nodes=torch.full((w.B, w.R), -9, dtype=torch.int32, device=dev))
     if debug_logits:
         res["logits"] = torch.empty((w.M, w.V), dtype=torch.float32, device=dev)
     mv.mtp_verify_logits_accept(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
                                 lm["q_draft"], lm["seed"], res["out_tokens"], res["num_accepted"], res["tie_flags"],
                                 res["lse"], res["argmax"], res.get("logits"), relaxed_topk=lm.get("relaxed_topk", 0),
-                                relaxed_delta=lm.get("relaxed_delta", 0.0))
+                                relaxed_delta=lm.get("relaxed_delta", 0.0), parents=lm.get("parents"),
+                                accepted_nodes=res["accepted_nodes"])
     return res
 
 
@@ -58,10 +60,11 @@ def request_pages(w, table_h, ctx_h, b):
     return table_h[b, :n]
 
 
-def oracle_attention(w, att, reqs):
+def oracle_attention(w, att, reqs, parents=None, return_cache=False):
     """Oracle output [len(reqs), R, Hq, d_v] for the given requests. Each
     request's pages are gathered from the (device) cache into a compact
-    host cache; the oracle re-does the append into it."""
+    host cache; the oracle re-does the append into it. return_cache: also
+    return that host cache (k, v) and its block table."""
     table_h = A(att["block_table"])
     ctx_h = A(att["ctx_lens"])
     pages = [request_pages(w, table_h, ctx_h, b) for b in reqs]
@@ -75,9 +78,11 @@ def oracle_attention(w, att, reqs):
         pos += len(p)
     idx = torch.tensor(list(reqs), dtype=torch.int64, device=att["q"].device)
     sel = lambda t: None if t is None else A(t.index_select(0, idx))
-    return oracle.verify_attention(sel(att["q"]), sel(att["k_new"]), sel(att["v_new"]), kc, vc, sub_table,
-                                   ctx_h[list(reqs)], D=w.D, Hq=w.Hq, Hkv=1 if w.is_mla else w.Hkv, d_qk=w.d_qk,
-                                   d_v=w.d_v, block_size=BLOCK, is_mla=w.is_mla, sm_scale=w.sm_scale)
+    out = oracle.verify_attention(sel(att["q"]), sel(att["k_new"]), sel(att["v_new"]), kc, vc, sub_table,
+                                  ctx_h[list(reqs)], D=w.D, Hq=w.Hq, Hkv=1 if w.is_mla else w.Hkv, d_qk=w.d_qk,
+                                  d_v=w.d_v, block_size=BLOCK, is_mla=w.is_mla, sm_scale=w.sm_scale,
+                                  parents=None if parents is None else A(parents.index_select(0, idx)))
+    return (out, kc, vc, sub_table) if return_cache else out
 
 
 def oracle_lmhead(w, lm, reqs, W_host=None, want_logits=False):
@@ -87,10 +92,12 @@ def oracle_lmhead(w, lm, reqs, W_host=None, want_logits=False):
     idx = torch.tensor(reqs, dtype=torch.int64, device=dev)
     W = W_host if W_host is not None else A(lm["lm_head"])
     q = None if lm["q_draft"] is None else A(lm["q_draft"].index_select(0, idx))
+    par = lm.get("parents")
     return oracle.lmhead_accept(A(lm["hidden"].index_select(0, rows)), W, A(lm["tokens"].index_select(0, idx)),
                                 A(lm["mode"].index_select(0, idx)), A(lm["temperature"].index_select(0, idx)), q,
                                 lm["seed"], want_logits=want_logits, request_index=np.array(reqs, np.int32),
-                                relaxed_topk=lm.get("relaxed_topk", 0), relaxed_delta=lm.get("relaxed_delta", 0.0))
+                                relaxed_topk=lm.get("relaxed_topk", 0), relaxed_delta=lm.get("relaxed_delta", 0.0),
+                                parents=None if par is None else A(par.index_select(0, idx)))
 
 
 def compare_accept(gpu, ref, reqs):
@@ -107,6 +114,9 @@ def compare_accept(gpu, ref, reqs):
             continue
         assert g_n[b] == ref["num_accepted"][i], (b, g_n[b], ref["num_accepted"][i])
         assert (g_tok[b] == ref["out_tokens"][i]).all(), (b, g_tok[b], ref["out_tokens"][i])
+        if "accepted_nodes" in gpu and "accepted_nodes" in ref:
+            g_nodes = gpu["accepted_nodes"][b].cpu().numpy()
+            assert (g_nodes == ref["accepted_nodes"][i]).all(), (b, g_nodes, ref["accepted_nodes"][i])
     return flagged
 
 

@@ -78,3 +78,22 @@ def test_algorithmic_counts():
     ctx = np.array([512] * v.B, np.int64)
     b = bench.algorithmic(v, ctx)
     assert b["kv_bytes"] == v.B * (512 + 4) * 576 * 2 and b["calls"] == 1
+
+
+def test_reference_arm_tree_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tree_cfg0", "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+
+
+def test_tree_path_lengths():
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.workloads()["tree_cfg1_D15"]
+    pl = bench.path_lengths(w)
+    assert list(pl[0]) == [1, 2, 2, 2, 3, 3, 3, 3, 3, 3, 4, 4, 4, 4, 4, 4]
+    v = bench.workloads()["cfg1_D3"]
+    assert (bench.path_lengths(v) == [1, 2, 3, 4]).all()

@@ -182,6 +182,7 @@ def test_sweep_points_sampled(B, D):
 
 EDGE = {
     "D0": synth.CFG0.with_(name="D=0", D=0, dtype="bf16", H=64, V=300),
+    "D0_sampling": synth.CFG0.with_(name="D=0 sampling", D=0, dtype="bf16", H=64, V=300, sampling="all"),
     "D15": synth.CFG0.with_(name="D=15", D=15, dtype="bf16", H=64, V=300, ctx=(50, 130), sampling="half"),
     "ctx0_fp32": synth.CFG0.with_(name="empty context", ctx=(0, 0), V=50, H=16),
     "tiny_vocab_sampling": synth.CFG0.with_(name="V=7 sampling", V=7, H=8, sampling="all", B=16),
