@@ -143,3 +143,28 @@ def test_draft_rejects_bad_args_on_host(mtplib, kw, code):
 def test_draft_empty_batch_is_a_no_op(mtplib):
     L = mtplib.lib()
     assert L.mtp_draft_argmax(ctypes.byref(_draft_ok(mtplib, B=0)), None) == 0
+
+
+def _cmp_ok(mtplib, **kw):
+    a = mtplib.KvCompactArgs()
+    a.k_cache = a.v_cache = a.block_table = a.ctx_lens = a.accepted_nodes = a.num_accepted = 16
+    a.B, a.D, a.Hkv, a.d_qk, a.d_v = 2, 7, 2, 128, 128
+    a.block_size, a.max_blocks, a.num_blocks, a.is_mla, a.dtype = 64, 4, 8, 0, 1
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=-1), dict(D=16), dict(D=-1), dict(block_size=32), dict(Hkv=0), dict(dtype=3), dict(k_cache=None),
+    dict(v_cache=None), dict(accepted_nodes=None), dict(num_accepted=None), dict(is_mla=1, Hkv=1),
+])
+def test_tree_kv_compact_rejects_bad_args_on_host(mtplib, kw):
+    L = mtplib.lib()
+    assert L.mtp_tree_kv_compact(ctypes.byref(_cmp_ok(mtplib, **kw)), None) == 1
+    assert L.mtp_last_error()
+
+
+def test_tree_kv_compact_empty_batch_is_a_no_op(mtplib):
+    L = mtplib.lib()
+    assert L.mtp_tree_kv_compact(ctypes.byref(_cmp_ok(mtplib, B=0)), None) == 0
