@@ -404,19 +404,41 @@ def run_gpu(args, w, rank, world, dev):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    e2e_t0 = time.perf_counter()
-    for _ in range(K):
+    def e2e_step(st):
         for k, t in host.items():
             dev_t[k].copy_(t, non_blocking=True)
-        step.run(stream)
+        step.run(st)
         for th, td in zip(res_host, res_dev):
             th.copy_(td, non_blocking=True)
+
+    # With graphs on, the copies from and to pinned host memory and the calls
+    # are captured together once and replayed, as a serving loop would.
+    g_e2e = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e, stream=side):
+                e2e_step(side)
+        torch.cuda.synchronize()
+        for _ in range(max(1, args.warmup // 2)):
+            g_e2e.replay()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e2e_t0 = time.perf_counter()
+    for _ in range(K):
+        if g_e2e is not None:
+            g_e2e.replay()
+        else:
+            e2e_step(stream)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - e2e_t0) * 1e3 / K
 
     ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, emitted, world, dev)
     ms_eager, _, _ = combine_ranks(ms_eager, 0.0, 0.0, world, dev)
-    return dict(ms=ms, ms_eager=ms_eager, graph=graph_ms is not None, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
+    return dict(ms=ms, ms_eager=ms_eager, graph=graph_ms is not None, e2e_graph=g_e2e is not None, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
                 clocks=clocks, launches=launches, h2d=h2d, d2h=d2h)
 
 
@@ -480,41 +502,59 @@ def draft_oracle_request(w, inp, W, b):
     return out
 
 
+def _timed_requests(fn, n_items, seconds, threads):
+    """Run fn(i) for i = 0, 1, ... (at most n_items) on `threads` threads until
+    `seconds` have passed (each thread finishes the request it is in); returns
+    (requests done, elapsed seconds)."""
+    import concurrent.futures as cf
+    import itertools
+    t0 = time.perf_counter()
+    stop = t0 + seconds
+    counter = itertools.count()
+
+    def worker():
+        n = 0
+        while time.perf_counter() < stop:
+            i = next(counter)
+            if i >= n_items:
+                break
+            fn(i)
+            n += 1
+        return n
+    with cf.ThreadPoolExecutor(threads) as ex:
+        done = sum(f.result() for f in [ex.submit(worker) for _ in range(threads)])
+    return done, time.perf_counter() - t0
+
+
 def cpu_baseline(w, seconds, dev=None, draft=False):
     """The oracle, as it stands, on a bounded sample of the same workload:
-    whole requests (attention + LM head + acceptance + rollback), one thread."""
-    import oracle
+    whole requests (attention + LM head + acceptance + KV compaction for trees
+    + rollback, or the D draft steps), first on one thread, then on every host
+    core (one unmodified single-threaded oracle call per request and thread;
+    the calls release the interpreter lock)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
     gen_dev = dev if dev is not None else torch.device("cpu")
     if draft:
         inp = synth.make_draft_inputs(w, gen_dev)
         W = synth.as_oracle_array(inp["lm_head"])
-        done, t0 = 0, time.perf_counter()
-        while True:
-            draft_oracle_request(w, inp, W, done % w.B)
-            done += 1
-            el = time.perf_counter() - t0
-            if el >= seconds or done >= w.B:
-                break
-        return dict(value=done / el, unit="requests/s", cores=1, kind="oracle",
-                    sample="%d request(s) of the %d-request batch (%d greedy draft steps each), single-threaded "
-                           "oracle, %.1f s" % (done, w.B, w.D, el))
-    att = synth.make_attention_inputs(w, gen_dev)
-    lm = synth.make_lmhead_inputs(w, gen_dev)
-    W = synth.as_oracle_array(lm["lm_head"])
-    table = synth.as_oracle_array(att["block_table"])
-    ctx = synth.as_oracle_array(att["ctx_lens"])
-    done, t0 = 0, time.perf_counter()
-    while True:
-        oracle_request(w, att, lm, W, table, ctx, done % w.B)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or done >= 4 * w.B:
-            break
-    return dict(value=done / el, unit="requests/s", cores=1, kind="oracle",
-                sample="%d request(s) of the %d-request batch (attention + LM head + acceptance + rollback), "
-                       "single-threaded oracle, %.1f s" % (done, w.B, el))
+        fn = lambda i: draft_oracle_request(w, inp, W, i % w.B)  # noqa: E731
+        what = "%d greedy draft steps each" % w.D
+    else:
+        att = synth.make_attention_inputs(w, gen_dev)
+        lm = synth.make_lmhead_inputs(w, gen_dev)
+        W = synth.as_oracle_array(lm["lm_head"])
+        table = synth.as_oracle_array(att["block_table"])
+        ctx = synth.as_oracle_array(att["ctx_lens"])
+        fn = lambda i: oracle_request(w, att, lm, W, table, ctx, i % w.B)  # noqa: E731
+        what = "attention + LM head + acceptance + rollback"
+    n1, el1 = _timed_requests(fn, 4 * w.B, seconds, 1)
+    cores = os.cpu_count() or 1
+    nc, elc = _timed_requests(fn, 4 * w.B, seconds, cores)
+    return dict(value=nc / elc, unit="requests/s", cores=cores, kind="oracle",
+                sample="%d request(s) of the %d-request batch (%s), the single-threaded oracle on %d threads, one "
+                       "request per thread at a time, %.1f s" % (nc, w.B, what, cores, elc),
+                single_thread=dict(value=n1 / el1, unit="requests/s", cores=1,
+                                   sample="%d request(s), one thread, %.1f s" % (n1, el1)))
 
 
 def json_line(**kw):
@@ -522,53 +562,46 @@ def json_line(**kw):
 
 
 def run_reference(args, w, rank, world):
-    """Reference arm: the CPU oracle on the host cores, timed per step on a
-    bounded sample (one request per step) of the same workload."""
+    """Reference arm: the CPU oracle on the host cores. Each step is a bounded
+    sample of the same workload: one whole request per host core, each on its
+    own thread running the unmodified single-threaded oracle."""
     if rank != 0:
         return
-    import oracle
+    import concurrent.futures as cf
     sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
     gen_dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if torch.cuda.is_available() else "cpu"
-    if is_draft(args.workload):
+    draft = is_draft(args.workload)
+    if draft:
         inp = synth.make_draft_inputs(w, gen_dev)
         Wd = synth.as_oracle_array(inp["lm_head"])
-        for i in range(args.warmup):
-            draft_oracle_request(w, inp, Wd, i % w.B)
+        one = lambda b: draft_oracle_request(w, inp, Wd, b)  # noqa: E731
+        what = "%d greedy draft steps" % w.D
+    else:
+        att = synth.make_attention_inputs(w, gen_dev)
+        lm = synth.make_lmhead_inputs(w, gen_dev)
+        W = synth.as_oracle_array(lm["lm_head"])
+        table = synth.as_oracle_array(att["block_table"])
+        ctx = synth.as_oracle_array(att["ctx_lens"])
+        one = lambda b: oracle_request(w, att, lm, W, table, ctx, b)  # noqa: E731
+        what = "attention + LM head + acceptance + rollback"
+    cores = os.cpu_count() or 1
+    with cf.ThreadPoolExecutor(cores) as ex:
+        def step(k):
+            list(ex.map(one, [(k * cores + c) % w.B for c in range(cores)]))
+        for k in range(args.warmup):
+            step(k)
         t0 = time.perf_counter()
-        for i in range(args.steps):
-            draft_oracle_request(w, inp, Wd, (args.warmup + i) % w.B)
+        for k in range(args.steps):
+            step(args.warmup + k)
         el = time.perf_counter() - t0
-        rps = args.steps / el
-        sample = "1 request per step of the %d-request batch (%d greedy draft steps), single-threaded oracle" % (
-            w.B, w.D)
-        json_line(impl="reference", metric=DRAFT_METRIC, value=rps, unit="requests/s", n_gpus=world,
-                  steps=args.steps, warmup=args.warmup, ms_per_step=el * 1e3 / args.steps, higher_is_better=True,
-                  scaling="weak", vs_baseline=None, dtype=w.dtype, data="synthetic", config=config_of(w, args),
-                  cpu_baseline=dict(value=rps, unit="requests/s", cores=1, kind="oracle", sample=sample),
-                  e2e=dict(value=rps, unit="requests/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
-        return
-    att = synth.make_attention_inputs(w, gen_dev)
-    lm = synth.make_lmhead_inputs(w, gen_dev)
-    W = synth.as_oracle_array(lm["lm_head"])
-    table = synth.as_oracle_array(att["block_table"])
-    ctx = synth.as_oracle_array(att["ctx_lens"])
-
-    def one(b):
-        oracle_request(w, att, lm, W, table, ctx, b)
-    for i in range(args.warmup):
-        one(i % w.B)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        one((args.warmup + i) % w.B)
-    el = time.perf_counter() - t0
-    rps = args.steps / el
-    sample = "1 request per step of the %d-request batch (attention + LM head + acceptance + rollback), " \
-             "single-threaded oracle" % w.B
-    json_line(impl="reference", metric=METRIC, value=rps, unit="requests/s", n_gpus=world, steps=args.steps,
-              warmup=args.warmup, ms_per_step=el * 1e3 / args.steps, higher_is_better=True, scaling="weak",
-              vs_baseline=None, dtype=w.dtype, data="synthetic", config=config_of(w, args),
-              cpu_baseline=dict(value=rps, unit="requests/s", cores=1, kind="oracle", sample=sample),
+    rps = args.steps * cores / el
+    sample = "%d requests per step (one per host core) of the %d-request batch (%s), the single-threaded " \
+             "oracle on each of %d threads" % (cores, w.B, what, cores)
+    json_line(impl="reference", metric=DRAFT_METRIC if draft else METRIC, value=rps, unit="requests/s",
+              n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=el * 1e3 / args.steps,
+              higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype, data="synthetic",
+              config=config_of(w, args),
+              cpu_baseline=dict(value=rps, unit="requests/s", cores=cores, kind="oracle", sample=sample),
               e2e=dict(value=rps, unit="requests/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
@@ -654,7 +687,10 @@ def main():
                                    gflop=(alg["lm_flops"] + alg["attn_flops"]) / 1e9),
                 kernels=kernels,
                 e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
-                         d2h_bytes_per_step=r["d2h"]),
+                         d2h_bytes_per_step=r["d2h"], ms_per_step=r["e2e_ms"],
+                         path="pinned host inputs -> device, the library calls, results -> pinned host, "
+                              + ("captured once as a CUDA graph and replayed" if r["e2e_graph"] else "eager")
+                              + ", host wall clock per step including the synchronize"),
                 gpu_launches=r["launches"], clocks=r["clocks"])
     if draft:
         for k in ("accepted_tokens_per_s", "mean_drafts_accepted"):
