@@ -229,15 +229,40 @@ __global__ void __launch_bounds__(kThreads) accept_race_kernel(
   const uint32_t tag = n < D ? kTagResidual : kTagBonus;
   const float* lrow = samp_logits + row * V;
   const float* qrow = n < D ? q_draft + ((int64_t)b * D + n) * V : nullptr;
-  const int per = (V + nsl - 1) / nsl;
+  const int per = ((V + nsl - 1) / nsl + 3) & ~3;   // slices start on 16-byte boundaries of a row
   const int v0 = sl_id * per;
   const int v1 = min(V, v0 + per);
 
   Race resid = race_empty();
-  for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
-    const float p = expf(lrow[v] - lse);
-    const float w = p - (qrow ? qrow[v] : 0.0f);
+  auto visit = [&](float l, float q, int v) {
+    const float w = expf(l - lse) - q;
     if (w > 0.0f) race_add(resid, w / race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag), v);
+  };
+  if ((V & 3) == 0) {
+    // Rows start 16-byte aligned: each thread takes 4 consecutive entries per
+    // step (ascending within the thread, as race_add expects) and keeps two
+    // steps' loads in flight.
+    const float4* l4 = reinterpret_cast<const float4*>(lrow);
+    const float4* q4 = reinterpret_cast<const float4*>(qrow);
+    const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int g = v0 / 4 + threadIdx.x; g < v1 / 4; g += 2 * kThreads) {
+      const int g2 = g + kThreads;
+      const bool two = g2 < v1 / 4;
+      const float4 la = __ldg(l4 + g), qa = qrow ? __ldg(q4 + g) : zero;
+      const float4 lb = two ? __ldg(l4 + g2) : zero, qb = (two && qrow) ? __ldg(q4 + g2) : zero;
+      visit(la.x, qa.x, 4 * g);
+      visit(la.y, qa.y, 4 * g + 1);
+      visit(la.z, qa.z, 4 * g + 2);
+      visit(la.w, qa.w, 4 * g + 3);
+      if (two) {
+        visit(lb.x, qb.x, 4 * g2);
+        visit(lb.y, qb.y, 4 * g2 + 1);
+        visit(lb.z, qb.z, 4 * g2 + 2);
+        visit(lb.w, qb.w, 4 * g2 + 3);
+      }
+    }
+  } else {
+    for (int v = v0 + threadIdx.x; v < v1; v += kThreads) visit(lrow[v], qrow ? qrow[v] : 0.0f, v);
   }
   resid = block_race_merge(resid, s_part);
   if (threadIdx.x == 0) {

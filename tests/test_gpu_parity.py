@@ -45,6 +45,9 @@ SMALL = {
                                                 ctx=(40, 90), H=256, V=5003),
     "lm_pair_two_groups_mixed": synth.CFG3.with_(name="LM head pairs, 2 groups", B=100, D=3, Hq=8, Hkv=2,
                                                  ctx=(64, 200), H=128, V=7001),
+    # vocabulary a multiple of 4: the race kernel's 16-byte row scan, ragged last slice
+    "sampling_aligned_vocab": synth.CFG2.with_(name="sampling, V % 4 == 0", B=12, D=3, Hq=8, Hkv=2, ctx=(40, 90),
+                                               H=128, V=4100),
 }
 
 
