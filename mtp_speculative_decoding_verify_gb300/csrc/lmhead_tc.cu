@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
               for (int x = 0; x < 32; x += 4) {
                 const float4 v4 = make_float4(rowv[x], rowv[x + 1], rowv[x + 2], rowv[x + 3]);
-                if (dst_s) *reinterpret_cast<float4*>(dst_s + x) = v4;
+                // streaming stores: the rows are read once, later, by the race
+                // kernel; W tiles shared by the row groups stay in L2
+                if (dst_s) __stcs(reinterpret_cast<float4*>(dst_s + x), v4);
                 if (dst_d) *reinterpret_cast<float4*>(dst_d + x) = v4;
               }
             } else {
