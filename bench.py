@@ -96,7 +96,7 @@ def load_peaks():
 # a reduced vocabulary (32768) of the same kernel and shapes; traffic grows in
 # proportion to the vocabulary, so it is scaled to the full one. Only valid
 # while the kernel is unchanged since the capture (profiles/ names the file).
-LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.698688e6 + 3.054336e6) / 32768}
+LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.696896e6 + 2.870272e6) / 32768}
 
 
 def elem_bytes(w):

@@ -94,6 +94,32 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
     // partial write and the combine pass. Keys per split <= 8192.
     n = base >= sm_count ? 1 : (int)((sm_count + base - 1) / std::max<long long>(base, 1));
     n = std::max(n, (max_len + 8191) / 8192);
+  } else if (a.dtype == MTP_BF16 && attention_mma_supported(a)) {
+    // GQA/MHA tensor-core CTAs run one per SM: take the split count with the
+    // shortest estimated time for requests of max_len keys, i.e. waves of
+    // CTAs x (keys per split + a CTA's start-up, about 256 keys' worth), plus,
+    // once split, the partial outputs' round trip (2 R group n fp32 rows of
+    // d_v against the KV bytes, about 2 R group n / max_len of them) and the
+    // combine pass (about 256 keys' worth). At least enough splits to give
+    // every SM two CTAs when the batch alone does not; splits hold at most
+    // 16384 keys so that long requests in a mixed batch leave a short tail.
+    const int kMaxSplitLen = 16384, kStartKeys = 256;
+    const int fill = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));
+    const int c0 = std::max(fill, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
+    const int c1 = std::max(c0, std::min(64, (max_len + kMinSplitLen - 1) / kMinSplitLen));
+    double best = 0.0;
+    n = c0;
+    for (int c = c0; c <= c1; ++c) {
+      const int sl = ((max_len + c - 1) / c + kBlock - 1) / kBlock * kBlock;
+      const int ce = (max_len + sl - 1) / sl;
+      const long long waves = (base * ce + sm_count - 1) / sm_count;
+      double cost = (double)waves * (sl + kStartKeys);
+      if (ce > 1) cost = cost * (1.0 + 2.0 * R * group * ce / max_len) + 256.0;
+      if (c == c0 || cost < best) {
+        best = cost;
+        n = ce;
+      }
+    }
   } else {
     const int kMaxSplitLen = 4096;
     n = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));

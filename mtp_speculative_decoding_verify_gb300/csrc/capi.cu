@@ -16,7 +16,6 @@ namespace mtp {
 int lmhead_simt_slices(int V, int sm_count);
 int lmhead_tc_slices(int V, int M, int sm_count);
 bool lmhead_tc_supported(const mtp_lmhead_args& a);
-bool attention_mma_supported(const mtp_attn_args& a);
 size_t accept_decision_bytes();
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned* err, cudaStream_t s);
 size_t accept_race_part_bytes();
