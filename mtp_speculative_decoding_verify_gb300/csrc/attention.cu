@@ -249,12 +249,34 @@ cudaError_t launch_attention_simt(const mtp_attn_args& a, const AttnPlan& p, uns
 
 // ------------------------------------------------------------------ combine
 // One warp per (request, row, head): merge the non-empty splits with
-// weights exp(lse_s - LSE).
+// weights exp(lse_s - LSE). The warp first turns the splits' log-sum-exps
+// into weights (one split per lane), then each lane sums its 4 output
+// elements over the splits with 16-byte loads, several splits in flight.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxSplits = 64;   // weights kept in shared memory up to this many splits
+
 template <typename T>
-__global__ void attention_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-                                         const int32_t* __restrict__ ctx_lens, T* __restrict__ out, int B, int R,
-                                         int Hq, int d_v, int split_len, int n_splits, int max_len) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp, lane = threadIdx.x % kWarp;
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_lse, const int32_t* __restrict__ ctx_lens,
+    T* __restrict__ out, int B, int R, int Hq, int d_v, int split_len, int n_splits, int max_len) {
+  __shared__ float s_w[kCombineThreads / kWarp][kCombineMaxSplits];
+  const int wl = threadIdx.x / kWarp;
+  const int warp = blockIdx.x * (kCombineThreads / kWarp) + wl, lane = threadIdx.x % kWarp;
   const int rows = B * R * Hq;
   if (warp >= rows) return;
   const int b = warp / (R * Hq), j = (warp / Hq) % R;
@@ -264,14 +286,41 @@ __global__ void attention_combine_kernel(const float* __restrict__ part_o, const
   const int ns = min(n_splits, (L + split_len - 1) / split_len);
   const float* lse = part_lse + (int64_t)warp * n_splits;
   float mx = -INFINITY;
-  for (int sp = 0; sp < ns; ++sp) mx = fmaxf(mx, lse[sp]);
+  for (int sp = lane; sp < ns; sp += kWarp) mx = fmaxf(mx, lse[sp]);
+#pragma unroll
+  for (int o = kWarp / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float denom = 0.0f;
-  for (int sp = 0; sp < ns; ++sp) denom += expf(lse[sp] - mx);
+  for (int sp = lane; sp < ns; sp += kWarp) {
+    const float w = expf(lse[sp] - mx);
+    if (sp < kCombineMaxSplits) s_w[wl][sp] = w;
+    denom += w;
+  }
+#pragma unroll
+  for (int o = kWarp / 2; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+  __syncwarp();
   const float inv = 1.0f / denom;
-  for (int e = lane; e < d_v; e += kWarp) {
-    float acc = 0.0f;
-    for (int sp = 0; sp < ns; ++sp) acc += expf(lse[sp] - mx) * part_o[((int64_t)warp * n_splits + sp) * d_v + e];
-    out[(int64_t)warp * d_v + e] = Num<T>::from_f(acc * inv);
+  const float* po = part_o + (int64_t)warp * n_splits * d_v;
+  T* dst = out + (int64_t)warp * d_v;
+  if ((d_v & 3) == 0 && ns <= kCombineMaxSplits) {
+    for (int e = 4 * lane; e < d_v; e += 4 * kWarp) {
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 8
+      for (int sp = 0; sp < ns; ++sp) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(po + (int64_t)sp * d_v + e));
+        const float w = s_w[wl][sp];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+      store4<T>(dst + e, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    }
+  } else {   // many splits or an odd width: weights recomputed per split
+    for (int e = lane; e < d_v; e += kWarp) {
+      float acc = 0.0f;
+      for (int sp = 0; sp < ns; ++sp) acc += expf(lse[sp] - mx) * po[(int64_t)sp * d_v + e];
+      dst[e] = Num<T>::from_f(acc * inv);
+    }
   }
 }
 
@@ -279,7 +328,7 @@ cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, 
   if (p.n_splits == 1 || a.B == 0) return cudaSuccess;
   const int R = a.D + 1;
   const int rows = a.B * R * a.Hq;
-  const int threads = 256;
+  const int threads = kCombineThreads;
   const int blocks = (rows * kWarp + threads - 1) / threads;
   const float* po = (const float*)((const char*)a.workspace + p.ws_partial_o);
   const float* pl = (const float*)((const char*)a.workspace + p.ws_partial_lse);
