@@ -80,6 +80,7 @@ static int rows_per_cta(const mtp_attn_args& a) {
 
 AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
   AttnPlan p{};
+  p.sm_count = sm_count;
   const int R = a.D + 1;
   const int group = a.Hq / a.Hkv;
   p.rows_per_kv = group * R;

@@ -46,12 +46,18 @@ struct AttnKParams {
   const int32_t* parents;        // [B, R] tree drafts, nullptr: chains
   unsigned* err;
   int R, Hq, Hkv, group, rows;  // rows = query rows per (request, KV head)
+  int row_warps, key_parts;     // consumer warps = row_warps x key_parts (warps sharing rows split the tiles)
   int max_blocks, num_blocks, split_len, n_splits, stages;
   float scale_log2;              // sm_scale * log2(e)
 };
 
 // ------------------------------------------------------------------ GQA
-constexpr int kGqaRowsPerCta = 112;   // 7 consumer warps x 16 rows (+1 producer warp = 256 threads)
+constexpr int kGqaRowsPerCta = 112;   // up to 7 row warps x 16 rows
+// Consumers (row warps x key parts) + 1 producer warp: 7 consumers keep the
+// 8 warps at 2 per SM sub-partition (up to 255 registers a thread); the wide
+// form with 8 consumers (4 row warps x 2 key parts) puts 3 warps on one
+// sub-partition and so has at most 168 registers a thread.
+constexpr int kGqaConsumers = 7, kGqaConsumersWide = 8;
 
 template <int D>
 struct GqaCfg {
@@ -63,8 +69,11 @@ struct GqaCfg {
 
 // kTree: rows see the verify keys of their root path (tree drafts) instead of
 // a causal prefix; the chain instantiation keeps the plain limit test.
-template <int D, bool kTree>
-__global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
+// kForm: 0 one warp per 16 rows, each reading every tile (the loop keeps a
+// running stage / phase); 1 key parts on up to 7 consumers; 2 the wide form,
+// 8 consumers.
+template <int D, bool kTree, int kForm>
+__global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaConsumers) + 1), 1) attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                        const __grid_constant__ CUtensorMap tm_v,
                                                        const AttnKParams p) {
   using C = GqaCfg<D>;
@@ -94,7 +103,7 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       sm100::mbar_init(&full[s], 1);
-      sm100::mbar_init(&empty[s], n_cons);
+      sm100::mbar_init(&empty[s], p.row_warps);   // every tile is read by one warp per row block
     }
     *abort = 0;
     sm100::fence_barrier_init();
@@ -148,9 +157,12 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
   }
 
   // ---------------------------------------------------------- consumers
+  // Consumer cw takes rows 16 rw .. 16 rw + 15 of the CTA and the tiles i
+  // with i % key_parts == kp; the key parts of a row block merge at the end.
   const int cw = warp - 1;
+  const int rw = kForm == 0 ? cw : cw % p.row_warps, kp = kForm == 0 ? 0 : cw / p.row_warps;
   const int g = lane >> 2, t = lane & 3;
-  const int r_lo = row_base + cw * 16 + g, r_hi = r_lo + 8;
+  const int r_lo = row_base + rw * 16 + g, r_hi = r_lo + 8;
   const int rl = min(r_lo, p.rows - 1), rh = min(r_hi, p.rows - 1);   // padding rows compute on the last row
   const int j_lo = rl / p.group, j_hi = rh / p.group;
   const int h_lo = kvh * p.group + rl % p.group, h_hi = kvh * p.group + rh % p.group;
@@ -179,15 +191,15 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.0f, l_hi = 0.0f;
 
-  int stage = 0;
-  uint32_t phase = 0;
-  for (int i = 0; i < n_tiles; ++i) {
+  // One tile: wait for its stage, S = Q K^T, online softmax, O += P V,
+  // release the stage. False when the wait gave up.
+  auto consume = [&](int i, int stage, uint32_t phase) -> bool {
     if (!__all_sync(0xffffffffu, sm100::mbar_wait(&full[stage], phase, abort) ? 1 : 0)) {
       if (lane == 0) {
         *abort = 1;
         raise_error(p.err, MTP_ERR_TIMEOUT);
       }
-      break;
+      return false;
     }
     if (stage_valid[stage]) {
       const uint32_t kbase = sm100::smem_u32(smem + stage * C::kStageBytes);
@@ -274,9 +286,65 @@ __global__ void __launch_bounds__(256, 1) attn_gqa_kernel(const __grid_constant_
     }
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(&empty[stage]);
-    if (++stage == p.stages) {
-      stage = 0;
-      phase ^= 1u;
+    return true;
+  };
+  if constexpr (kForm == 0) {
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (!consume(i, stage, phase)) break;
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else {
+    for (int i = kp; i < n_tiles; i += p.key_parts)
+      if (!consume(i, i % p.stages, (uint32_t)(i / p.stages) & 1u)) break;
+  }
+
+  if constexpr (kForm != 0) {
+    // Merge the key parts of each row block. Every consumer is past its last
+    // tile at the first barrier, so the stage ring is free: parts kp > 0
+    // leave their (o, m, l) there, one slot per (warp, lane) (the fragment
+    // layout is the same in every part), and part 0 folds them in.
+    constexpr int kVals = D / 2 + 4;
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    if (kp > 0) {
+      float* xs = reinterpret_cast<float*>(smem) + ((size_t)cw * 32 + lane) * kVals;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        xs[4 * n] = o[n][0];
+        xs[4 * n + 1] = o[n][1];
+        xs[4 * n + 2] = o[n][2];
+        xs[4 * n + 3] = o[n][3];
+      }
+      xs[D / 2] = m_lo;
+      xs[D / 2 + 1] = m_hi;
+      xs[D / 2 + 2] = l_lo;
+      xs[D / 2 + 3] = l_hi;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    if (kp > 0) return;
+    for (int q = 1; q < p.key_parts; ++q) {
+      const float* ys = reinterpret_cast<const float*>(smem) + ((size_t)(q * p.row_warps + rw) * 32 + lane) * kVals;
+      const float mb_lo = ys[D / 2], mb_hi = ys[D / 2 + 1];
+      const float mx_lo = fmaxf(m_lo, mb_lo), mx_hi = fmaxf(m_hi, mb_hi);
+      const float fa_lo = m_lo == -INFINITY ? 0.0f : exp2f(m_lo - mx_lo);
+      const float fb_lo = mb_lo == -INFINITY ? 0.0f : exp2f(mb_lo - mx_lo);
+      const float fa_hi = m_hi == -INFINITY ? 0.0f : exp2f(m_hi - mx_hi);
+      const float fb_hi = mb_hi == -INFINITY ? 0.0f : exp2f(mb_hi - mx_hi);
+      l_lo = l_lo * fa_lo + ys[D / 2 + 2] * fb_lo;
+      l_hi = l_hi * fa_hi + ys[D / 2 + 3] * fb_hi;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] = o[n][0] * fa_lo + ys[4 * n] * fb_lo;
+        o[n][1] = o[n][1] * fa_lo + ys[4 * n + 1] * fb_lo;
+        o[n][2] = o[n][2] * fa_hi + ys[4 * n + 2] * fb_hi;
+        o[n][3] = o[n][3] * fa_hi + ys[4 * n + 3] * fb_hi;
+      }
+      m_lo = mx_lo;
+      m_hi = mx_hi;
     }
   }
 
@@ -320,16 +388,82 @@ int gqa_smem_bytes(int stages) {
   return stages * GqaCfg<D>::kStageBytes + stages * 20 + 64 + 1024;
 }
 
+constexpr int kGqaMaxSmem = 232448;   // 227 KB opt-in per CTA
+
+template <int D>
+using GqaKernel = void (*)(const CUtensorMap, const CUtensorMap, const AttnKParams);
+
+template <int D>
+GqaKernel<D> gqa_kernel(bool tree, int form) {
+  if (form == 2) return tree ? attn_gqa_kernel<D, true, 2> : attn_gqa_kernel<D, false, 2>;
+  if (form == 1) return tree ? attn_gqa_kernel<D, true, 1> : attn_gqa_kernel<D, false, 1>;
+  return tree ? attn_gqa_kernel<D, true, 0> : attn_gqa_kernel<D, false, 0>;
+}
+
+// CTAs of one form that fit on an SM at once (the occupancy the runtime
+// reports for its threads and shared memory), cached per form.
+template <int D>
+int gqa_occupancy(bool tree, int form, int warps, int stages) {
+  static int cache[2][3][kGqaConsumersWide + 1][9] = {};
+  int& c = cache[tree][form][warps][stages];
+  if (c == 0) {
+    const GqaKernel<D> kern = gqa_kernel<D>(tree, form);
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGqaMaxSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (warps + 1), gqa_smem_bytes<D>(stages)) !=
+            cudaSuccess)
+      n = 1;
+    c = std::max(1, n);
+  }
+  return c;
+}
+
 template <int D>
 cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, cudaStream_t s) {
-  const int stages = D == 128 ? 3 : 4;
+  // Consumer layout: one warp per 16 rows of the CTA. When a KV head has few
+  // rows, spare warps can take alternate tiles of the same rows (key parts)
+  // and merge at the end. Tile i sits in stage i % stages and goes to part
+  // i % key_parts; stages is a multiple of key_parts, so each stage serves
+  // one part, which meets that stage's phases in order (a part that skipped
+  // ahead to a stage of another part could take a phase that has not
+  // completed for a completed one: the parity wait cannot tell them apart).
+  // Key parts are used only when they put more consumer warps on an SM than
+  // single-part CTAs do at their occupancy (two of those often share an SM),
+  // the grid fills at least two waves of single-part CTAs, and each part gets
+  // at least 4 tiles. The wide form (8 consumers) only serves 4 row warps,
+  // which 7 consumers cannot split.
+  const int R = a.D + 1, group = a.Hq / a.Hkv, rows = group * R;
+  const bool tree = a.parents != nullptr;
+  constexpr int kMaxStages = 8;   // the producer tracks at most 8 stages
+  const int s_max = std::min(kMaxStages, (kGqaMaxSmem - 2048) / GqaCfg<D>::kStageBytes);
+  const int row_warps = std::min(kGqaRowsPerCta / 16, (rows + 15) / 16);
+  const int max_tiles = (pl.split_len + kBlock - 1) / kBlock;
+  const long long grid_ctas =
+      (long long)pl.n_splits * a.B * a.Hkv * ((rows + kGqaRowsPerCta - 1) / kGqaRowsPerCta);
+  int key_parts = 1, stages = D == 128 ? 3 : 4, form = 0;
+  const int occ1 = gqa_occupancy<D>(tree, 0, row_warps, stages);
+  if (grid_ctas >= 2LL * occ1 * pl.sm_count) {
+    int best = occ1 * row_warps;
+    for (int k = 2; k <= s_max && 4 * k <= max_tiles; ++k) {
+      const bool w = row_warps * k > kGqaConsumers;
+      if (w && !(row_warps == 4 && k == 2)) continue;
+      const int S = k * (s_max / k);
+      const int cons = gqa_occupancy<D>(tree, w ? 2 : 1, row_warps * k, S) * row_warps * k;
+      if (cons > best) {
+        best = cons;
+        key_parts = k;
+        stages = S;
+        form = w ? 2 : 1;
+      }
+    }
+  }
+  const int warps = row_warps * key_parts;
   CUtensorMap tk, tv;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)kBlock, (cuuint64_t)a.num_blocks};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hkv * D * 2, (cuuint64_t)kBlock * a.Hkv * D * 2};
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBlock, 1};
   if (!make_bf16_map(&tk, a.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
   if (!make_bf16_map(&tv, a.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
-  const int R = a.D + 1, group = a.Hq / a.Hkv, rows = group * R;
   AttnKParams p;
   p.q = (const __nv_bfloat16*)a.q;
   p.out = (__nv_bfloat16*)a.out;
@@ -350,9 +484,13 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
   p.n_splits = pl.n_splits;
   p.stages = stages;
   p.scale_log2 = a.sm_scale * kLog2e;
-  const int warps = std::min(kGqaRowsPerCta / 16, (rows + 15) / 16);
+  p.row_warps = row_warps;
+  p.key_parts = key_parts;
+  // the merge of the key parts stages every consumer's (o, m, l) in the stage ring
+  if ((size_t)warps * 32 * (D / 2 + 4) * sizeof(float) > (size_t)stages * GqaCfg<D>::kStageBytes)
+    return cudaErrorInvalidValue;
   const int smem = gqa_smem_bytes<D>(stages);
-  auto kern = a.parents ? attn_gqa_kernel<D, true> : attn_gqa_kernel<D, false>;
+  const GqaKernel<D> kern = gqa_kernel<D>(tree, form);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(pl.n_splits, a.B * a.Hkv, (rows + kGqaRowsPerCta - 1) / kGqaRowsPerCta);

@@ -19,6 +19,7 @@ struct AttnPlan {
   size_t ws_partial_lse;
   size_t ws_order;     // MLA tensor-core path: work-item order (int32 per item)
   size_t ws_bytes;
+  int sm_count;        // SMs of the device the plan is for
 };
 
 AttnPlan plan_attention(const mtp_attn_args& a, int sm_count);

@@ -45,6 +45,10 @@ SMALL = {
                                                 ctx=(40, 90), H=256, V=5003),
     "lm_pair_two_groups_mixed": synth.CFG3.with_(name="LM head pairs, 2 groups", B=100, D=3, Hq=8, Hkv=2,
                                                  ctx=(64, 200), H=128, V=7001),
+    # GQA with 16 rows per KV head over a grid of several waves: spare warps split each
+    # CTA's tiles (key parts) and merge at the end
+    "gqa_key_parts": synth.CFG3.with_(name="GQA key parts", B=80, D=3, Hq=32, Hkv=8, ctx=(1800, 2100), H=128,
+                                      V=3001),
     # vocabulary a multiple of 4: the race kernel's 16-byte row scan, ragged last slice
     "sampling_aligned_vocab": synth.CFG2.with_(name="sampling, V % 4 == 0", B=12, D=3, Hq=8, Hkv=2, ctx=(40, 90),
                                                H=128, V=4100),

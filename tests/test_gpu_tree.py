@@ -241,3 +241,26 @@ def test_tree_single_node_and_chain_shaped_trees():
         ref = oracle_attention(w, att, range(w.B), parents)
         assert attention_excess(_out_np(w, out), _ref_np(ref), w.dtype) <= 0.0
         assert compare_accept(gpu, oracle_lmhead(w, lm, range(w.B)), range(w.B)) == 0
+
+
+@pytest.mark.parametrize("name,w", [
+    # 4 row warps per CTA (16 nodes x 4 heads per KV head): the 8-consumer form with 2 key parts
+    ("wide_two_parts", synth.CFG3.with_(name="tree GQA 64 rows", B=40, D=15, Hq=32, Hkv=8, ctx=(600, 900), H=128,
+                                        V=3001, sampling="none", tree="full", stream=46)),
+    # 2 row warps per CTA (8 nodes x 4 heads): key parts on 7 consumers
+    ("two_row_warps", synth.CFG3.with_(name="tree GQA 32 rows", B=80, D=7, Hq=32, Hkv=8, ctx=(800, 1000), H=128,
+                                       V=3001, sampling="none", tree="random", stream=47)),
+])
+def test_tree_gqa_key_parts_all_requests(name, w):
+    """Tree attention on grids large enough that spare warps split the tiles
+    of each CTA, every request against the oracle (run in threads)."""
+    import concurrent.futures as cf
+    att = synth.make_attention_inputs(w, DEV)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    parents = lm["parents"]
+    out = gpu_attention(w, att, parents)
+    mv.sync_status()
+    with cf.ThreadPoolExecutor(8) as ex:
+        refs = list(ex.map(lambda b: oracle_attention(w, att, [b], parents), range(w.B)))
+    ref = np.concatenate(refs)
+    assert attention_excess(_out_np(w, out), _ref_np(ref), w.dtype) <= 0.0
