@@ -64,6 +64,8 @@ def workloads():
         "profile_mla_V32k": synth.CFG1.with_(name="profiling case: DeepSeek-V3-shaped MLA B=32 D=3, vocab 32768",
                                              V=32768),
         "profile_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, B=16", B=16),
+        "profile_gqa_B32_keyparts": synth.CFG3.with_(
+            name="profiling case: large-batch mixed GQA, B=32 (grid large enough for key parts)", B=32),
         "profile_tree_mla_V32k": synth.CFG1.with_(name="profiling case: DeepSeek-V3-shaped MLA, trees of 15 drafts, "
                                                        "B=32, vocab 32768", D=15, tree="full", V=32768),
         "profile_sampling_V32k": synth.CFG2.with_(
