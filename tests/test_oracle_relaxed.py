@@ -156,3 +156,18 @@ def test_relaxed_needs_topk():
     with pytest.raises(ValueError):
         oracle.lmhead_accept(np.ones((2, 4), np.float32), np.eye(4, dtype=np.float32), np.zeros((1, 2), np.int32),
                              np.array([2], np.uint8), None, None, 0, relaxed_topk=0)
+
+
+def test_equal_logits_rank_lower_token_id_first():
+    """Logits [3, 2, 2, 1] with N = 2 and a delta that admits every token:
+    token 1 (lower id of the tied pair) is the second candidate, token 2 is
+    third and so outside the top 2. The tie sits on the boundary, so the
+    decision is flagged as a near-tie, but the rule itself is fixed."""
+    lg = np.array([3.0, 2.0, 2.0, 1.0], np.float32)
+    lse = np.float32(_lse(lg))
+    acc1, tie1 = oracle.relaxed_accept(lg, lse, 1, 2, 1.0)
+    acc2, tie2 = oracle.relaxed_accept(lg, lse, 2, 2, 1.0)
+    assert acc1 == 1 and acc2 == 0
+    assert tie1 & 1 and tie2 & 1
+    # With N = 3 both tied tokens are candidates.
+    assert oracle.relaxed_accept(lg, lse, 2, 3, 1.0)[0] == 1
