@@ -9,10 +9,13 @@
 // TensorRT-LLM", attention for MTP: K+1 chained queries need only a causal
 // mask. Row of verify token j (request context ctx) attends slots 0..ctx+j.
 //
-// attn_gqa_kernel<D>: GQA/MHA, d_qk = d_v = D (64 or 128). CTA = (split,
-// request x KV head, row block): the g*R query rows that share one KV head
-// (up to 112: one consumer warp per 16 rows), 64-key tiles = one cache
-// block. (Absorbed MLA runs on tcgen05: attention_mla_tc.cu.)
+// attn_gqa_kernel<D, tree, form>: GQA/MHA, d_qk = d_v = D (64 or 128). CTA =
+// (split, request x KV head, row block): the g*R query rows that share one
+// KV head (up to 112: one row warp per 16 rows), 64-key tiles = one cache
+// block. Forms 1 and 2 add key parts: warps sharing rows take alternate tiles
+// and merge their softmax state at the end (see run_gqa). Tree drafts use a
+// per-row root-path mask instead of the causal limit. (Absorbed MLA runs on
+// tcgen05: attention_mla_tc.cu.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
