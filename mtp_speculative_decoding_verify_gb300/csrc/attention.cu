@@ -5,7 +5,9 @@
 // every verify token's new K/V is written to the cache for the tokens after
 // it. "MTP in TensorRT-LLM", attention for MTP: with K+1 chained input
 // tokens a causal mask is all the attention kernel needs. Row j of a request
-// with ctx cached tokens therefore attends slots 0 .. ctx+j.
+// with ctx cached tokens therefore attends slots 0 .. ctx+j. With tree drafts
+// ("MTP in TensorRT-LLM on Blackwell", future work) row j attends the context
+// and the slots of the nodes on its root path instead (tree_path_mask).
 #include <math.h>
 
 #include <algorithm>

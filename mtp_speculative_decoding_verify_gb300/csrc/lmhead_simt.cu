@@ -9,6 +9,8 @@
 // the argmax; the accept kernel merges the per-CTA partials. Full logits go
 // to memory only for rejection-sampling rows (their residual draw needs the
 // whole row once the log-sum-exp is known) and for the optional debug copy.
+// Relaxed rows also count the entries that rank before their draft ("MTP in
+// TensorRT-LLM on Blackwell", relaxed acceptance; relaxed_count).
 #include <math.h>
 
 #include <algorithm>

@@ -7,7 +7,9 @@
 // full logits are never stored for greedy rows: the epilogue keeps, per row,
 // a running max, sum of exp(l - max) and argmax over the vocabulary this CTA
 // sees; rejection-sampling rows also get their fp32 logit rows written once
-// (their residual draw needs the whole row after the log-sum-exp is known).
+// (their residual draw needs the whole row after the log-sum-exp is known),
+// and relaxed rows count the entries that rank before their draft ("MTP in
+// TensorRT-LLM on Blackwell", relaxed acceptance; relaxed_count).
 //
 // Mapping (swap-AB): the MMA's M dimension is 128 vocabulary rows of W (the
 // big streamed operand), its N dimension is a group of N verify rows of
