@@ -68,6 +68,9 @@ def workloads():
             name="profiling case: large-batch mixed GQA, B=32 (grid large enough for key parts)", B=32),
         "profile_tree_mla_V32k": synth.CFG1.with_(name="profiling case: DeepSeek-V3-shaped MLA, trees of 15 drafts, "
                                                        "B=32, vocab 32768", D=15, tree="full", V=32768),
+        "profile_tree_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, trees of 15 drafts, "
+                                                      "B=16, vocab 32768", B=16, D=15, tree="full", sampling="none",
+                                                 V=32768),
         "profile_sampling_V32k": synth.CFG2.with_(
             name="profiling case: Llama-70B-shaped rejection sampling B=64 D=5, vocab 32768", V=32768),
         # MTP-Eagle draft steps: D sequential greedy top-1 calls over the shared LM head, B rows each.

@@ -98,16 +98,18 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
     n = base >= sm_count ? 1 : (int)((sm_count + base - 1) / std::max<long long>(base, 1));
     n = std::max(n, (max_len + 8191) / 8192);
   } else if (a.dtype == MTP_BF16 && attention_mma_supported(a)) {
-    // GQA/MHA tensor-core CTAs run one per SM: take the split count with the
+    // GQA/MHA tensor-core CTAs (mma.sync, or tcgen05 for 33..64 rows per KV
+    // head, one CTA per SM in both): take the split count with the
     // shortest estimated time for requests of max_len keys, i.e. waves of
     // CTAs x (keys per split + a CTA's start-up, about 256 keys' worth), plus,
     // once split, the partial outputs' round trip (2 R group n fp32 rows of
     // d_v against the KV bytes, about 2 R group n / max_len of them) and the
     // combine pass (about 256 keys' worth). At least enough splits to give
-    // every SM two CTAs when the batch alone does not; splits hold at most
+    // every SM two CTAs (mma.sync; one for tcgen05) when the batch alone does not; splits hold at most
     // 16384 keys so that long requests in a mixed batch leave a short tail.
     const int kMaxSplitLen = 16384, kStartKeys = 256;
-    const int fill = (int)std::max<long long>(1, (2LL * sm_count + base - 1) / std::max<long long>(base, 1));
+    const int per_sm = attention_uses_gqa_tc(a) ? 1 : 2;
+    const int fill = (int)std::max<long long>(1, (per_sm * sm_count + base - 1) / std::max<long long>(base, 1));
     const int c0 = std::max(fill, (max_len + kMaxSplitLen - 1) / kMaxSplitLen);
     const int c1 = std::max(c0, std::min(64, (max_len + kMinSplitLen - 1) / kMinSplitLen));
     double best = 0.0;
@@ -130,7 +132,8 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
   }
   n = std::min(n, std::max(1, (max_len + kMinSplitLen - 1) / kMinSplitLen));
   int split_len = (max_len + n - 1) / n;
-  const int gran = (a.is_mla && a.dtype == MTP_BF16) ? 128 : kBlock;   // MLA tensor-core tiles are 128 keys
+  // tcgen05 MLA and GQA tiles are 128 keys
+  const int gran = (a.is_mla && a.dtype == MTP_BF16) || attention_uses_gqa_tc(a) ? 128 : kBlock;
   split_len = (split_len + gran - 1) / gran * gran;
   p.split_len = split_len;
   p.n_splits = (max_len + split_len - 1) / split_len;
@@ -142,9 +145,10 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
     p.ws_bytes = p.ws_partial_lse + rows * p.n_splits * sizeof(float);
     p.ws_bytes = (p.ws_bytes + 255) / 256 * 256;
   }
-  if (attention_uses_mla_tc(a)) {   // one int per (split, request, row block) at most
+  if (attention_uses_mla_tc(a) || attention_uses_gqa_tc(a)) {   // one int per work item at most
     p.ws_order = p.ws_bytes;
-    p.ws_bytes += ((size_t)p.n_splits * a.B * row_tiles * sizeof(int32_t) + 255) / 256 * 256;
+    const size_t items = (size_t)p.n_splits * a.B * row_tiles * (a.is_mla ? 1 : a.Hkv);
+    p.ws_bytes += (items * sizeof(int32_t) + 255) / 256 * 256;
   }
   return p;
 }

@@ -235,13 +235,14 @@ int mtp_verify_attention(const mtp_attn_args* a, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "kv append launch");
   if ((e = record(a->timing_events[0], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   if (mtp::attention_uses_mla_tc(*a)) e = mtp::launch_attention_mla(*a, p, c->err, s);
+  else if (mtp::attention_uses_gqa_tc(*a)) e = mtp::launch_attention_gqa_tc(*a, p, c->err, s);
   else if (a->dtype == MTP_BF16 && mtp::attention_mma_supported(*a)) e = mtp::launch_attention_mma(*a, p, c->err, s);
   else e = mtp::launch_attention_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_attention_combine(*a, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention combine launch");
-  g_launches = 2 + (p.n_splits > 1 ? 1 : 0) + (mtp::attention_uses_mla_tc(*a) ? 1 : 0);
+  g_launches = 2 + (p.n_splits > 1 ? 1 : 0) + (mtp::attention_uses_mla_tc(*a) || mtp::attention_uses_gqa_tc(*a) ? 1 : 0);
   return MTP_OK;
 }
 

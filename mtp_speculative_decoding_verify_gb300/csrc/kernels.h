@@ -17,7 +17,7 @@ struct AttnPlan {
   int split_len;       // keys per split (multiple of 64)
   size_t ws_partial_o; // byte offset of the split partial outputs in the workspace
   size_t ws_partial_lse;
-  size_t ws_order;     // MLA tensor-core path: work-item order (int32 per item)
+  size_t ws_order;     // tensor-core MLA / GQA paths: work-item order (int32 per item)
   size_t ws_bytes;
   int sm_count;        // SMs of the device the plan is for
 };
@@ -30,6 +30,9 @@ cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsi
 cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 bool attention_mma_supported(const mtp_attn_args& a);   // bf16 GQA/MHA (d 64, 128) or MLA on tensor cores
 bool attention_uses_mla_tc(const mtp_attn_args& a);
+// bf16 GQA/MHA, head dim 128, 33..64 query rows per KV head: tcgen05 kernel
+bool attention_uses_gqa_tc(const mtp_attn_args& a);
+cudaError_t launch_attention_gqa_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ LM head

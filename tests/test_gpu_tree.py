@@ -244,9 +244,13 @@ def test_tree_single_node_and_chain_shaped_trees():
 
 
 @pytest.mark.parametrize("name,w", [
-    # 4 row warps per CTA (16 nodes x 4 heads per KV head): the 8-consumer form with 2 key parts
+    # 16 nodes x 4 heads = 64 rows per KV head: the tcgen05 GQA kernel at head dim 128
     ("wide_two_parts", synth.CFG3.with_(name="tree GQA 64 rows", B=40, D=15, Hq=32, Hkv=8, ctx=(600, 900), H=128,
                                         V=3001, sampling="none", tree="full", stream=46)),
+    # the same at head dim 64, on mma.sync: 4 row warps per CTA, the 8-consumer form with 2 key parts
+    ("wide_two_parts_d64", synth.CFG3.with_(name="tree GQA 64 rows d64", B=80, D=15, Hq=32, Hkv=8, d_qk=64, d_v=64,
+                                            ctx=(600, 900), H=128, V=3001, sampling="none", tree="full",
+                                            stream=48)),
     # 2 row warps per CTA (8 nodes x 4 heads): key parts on 7 consumers
     ("two_row_warps", synth.CFG3.with_(name="tree GQA 32 rows", B=80, D=7, Hq=32, Hkv=8, ctx=(800, 1000), H=128,
                                        V=3001, sampling="none", tree="random", stream=47)),
