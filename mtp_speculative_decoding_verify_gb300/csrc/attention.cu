@@ -98,7 +98,7 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
     n = base >= sm_count ? 1 : (int)((sm_count + base - 1) / std::max<long long>(base, 1));
     n = std::max(n, (max_len + 8191) / 8192);
   } else if (a.dtype == MTP_BF16 && attention_mma_supported(a)) {
-    // GQA/MHA tensor-core CTAs (mma.sync, or tcgen05 for 33..64 rows per KV
+    // GQA/MHA tensor-core CTAs (mma.sync, or tcgen05 for 49..64 rows per KV
     // head, one CTA per SM in both): take the split count with the
     // shortest estimated time for requests of max_len keys, i.e. waves of
     // CTAs x (keys per split + a CTA's start-up, about 256 keys' worth), plus,

@@ -1,7 +1,7 @@
 // GQA/MHA verify attention on the 5th-generation tensor cores, for KV heads
-// that carry 33..64 query rows (group x R: e.g. 8 heads x 6 verify tokens, or
-// 4 heads x 16 tree nodes), where the mma.sync kernel falls short of the
-// cache read rate.
+// that carry 49..64 query rows (group x R: e.g. 4 heads x 16 tree nodes, 8
+// heads x 7 verify tokens), where the mma.sync kernel falls short of the
+// cache read rate (it reads the cache at the copy rate up to 48 rows).
 //
 // "Multi Token Prediction" note, K=3 flow step 2 (stacked queries against the
 // reused cache, causal within the verify chain); tree drafts ("MTP in
@@ -12,8 +12,8 @@
 // Transposed formulation (keys on the TMEM lanes, rows on the columns):
 //   S^T [128 keys x N rows]  = K_tile [128 x 128 dims] . Q^T      M = 128 keys
 //   O^T [128 dv   x N rows] += V^T [128 dv x 128 keys] . P^T       M = 128 dv
-// N = the KV head's rows padded to a multiple of 16 (32, 48 or 64). TMEM:
-// O^T in columns 0..N-1, two S^T buffers at 64 and 128.
+// N = 64 (the KV head's rows, padding rows zero). TMEM: O^T in columns
+// 0..63, two S^T buffers at 64 and 128.
 //
 // Shared memory: Q (two 64-dim chunks of [N rows x 128 B]) and three stages
 // of one 128-key tile each: K slots (dims 0..63, 64..127) and V slots (dv
@@ -61,7 +61,7 @@ namespace {
 
 constexpr int kKeys = 128;             // keys per tile (MMA M of S^T)
 constexpr int kD = 128;                // head dim of K and V
-constexpr int kTcMaxRows = 64;           // query rows per KV head handled here
+constexpr int kTcMinRows = 49, kTcMaxRows = 64;   // query rows per KV head handled here
 constexpr int kSlotBytes = 16384;      // [128 keys x 64 dims] bf16
 constexpr int kStageBytes = 4 * kSlotBytes;   // K0, K1, V0, V1
 constexpr int kStages = 3;
@@ -73,7 +73,8 @@ constexpr int kQOff = 0;                                   // 2 x [N rows x 128 
 constexpr int kStageOff = 16384;
 constexpr int kRedOff = kStageOff + kStages * kStageBytes; // red_max[4][64], red_sum[4][64]
 constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;          // m_run, l_run, m_ref, rscale, path, m_shift [64]
-constexpr int kBarOff = kRowOff + 6 * 64 * 4;
+constexpr int kRowOffOut = kRowOff + 6 * 64 * 4;           // int64 [64]: output element offset of each row
+constexpr int kBarOff = kRowOffOut + 64 * 8;
 constexpr int kRing = 8;                                   // work items published ahead by the scheduler warp
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 2 * kRing;
 constexpr int kRingOff = kBarOff + kNumBars * 8;           // kRing work items (RingItem)
@@ -90,7 +91,7 @@ struct Shape {
   static constexpr int kSoftThreads = 32 * kSoftWarps;
   static constexpr int kThreads = 128 + kSoftThreads;
   static constexpr int kQChunk = kN * 128;               // one 64-dim chunk of Q; also one 64-key block of P^T
-  static_assert(kN % 16 == 0 && kN >= 32 && kN <= kTcMaxRows, "row count");
+  static_assert(kN % 16 == 0 && kN <= 64, "row count");
 };
 
 struct Params {
@@ -122,29 +123,31 @@ __device__ __forceinline__ Item decode_item(int i, int B, int Hkv) {
 constexpr int kMaxItemTiles = 128;   // split_len <= 16384 keys
 
 // Orders the work items by tile count, longest first (counting sort, one
-// CTA): CTAs start in index order, so long items start first and short ones
-// fill the tail of the last wave.
+// CTA) in groups of the Hkv items of one (split, request), which have the
+// same keys: a request's KV heads share the cache blocks (the heads of a
+// token are interleaved), so CTAs that start them together read the same
+// DRAM pages at about the same time. CTAs take positions in index order, so
+// long items start first and short ones fill the tail of the last round.
 __global__ void __launch_bounds__(1024) gqa_schedule_kernel(const int32_t* __restrict__ ctx_lens, int B, int R,
                                                            int Hkv, int split_len, int n_splits, int max_len,
                                                            int32_t* __restrict__ order, unsigned* err) {
   __shared__ int hist[kMaxItemTiles + 1];
-  const int n = n_splits * B * Hkv;
-  auto tiles_of = [&](int i) -> int {
-    const Item it = decode_item(i, B, Hkv);
-    const int ctx = ctx_lens[it.b];
+  const int n = n_splits * B;   // groups (split, request); group q = split * B + b holds items q * Hkv + h
+  auto tiles_of = [&](int q) -> int {
+    const int ctx = ctx_lens[q % B];
     if (ctx < 0 || ctx + R > max_len) {   // the attention kernel skips the request
       raise_error(err, MTP_ERR_LENGTH);
       return 0;
     }
-    const int t0 = it.split * split_len;
+    const int t0 = (q / B) * split_len;
     const int t_end = min(t0 + split_len, ctx + R);
     return t0 < t_end ? min((t_end - t0 + kKeys - 1) / kKeys, kMaxItemTiles) : 0;
   };
   for (int k = threadIdx.x; k <= kMaxItemTiles; k += blockDim.x) hist[k] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[tiles_of(i)], 1);
+  for (int q = threadIdx.x; q < n; q += blockDim.x) atomicAdd(&hist[tiles_of(q)], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {   // hist[k] becomes the first position of tile count k
+  if (threadIdx.x == 0) {   // hist[k] becomes the first group position of tile count k
     int acc = 0;
     for (int k = kMaxItemTiles; k >= 0; --k) {
       const int h = hist[k];
@@ -153,7 +156,10 @@ __global__ void __launch_bounds__(1024) gqa_schedule_kernel(const int32_t* __res
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) order[atomicAdd(&hist[tiles_of(i)], 1)] = i;
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const int pos = atomicAdd(&hist[tiles_of(q)], 1);
+    for (int h = 0; h < Hkv; ++h) order[pos * Hkv + h] = q * Hkv + h;
+  }
 }
 
 // MN-major operand with 128-byte swizzling: 64-element MN blocks `lbo` bytes
@@ -314,6 +320,7 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
   float* rscale = m_run + 192;
   uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 256);   // per row: path mask (tree) or key limit (chain)
   float* m_shift = m_run + 320;
+  int64_t* row_out = reinterpret_cast<int64_t*>(smem + kRowOffOut);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kStages]: the stage holds its tile
   uint64_t* empty = full + kStages;                                 // [kStages]: PV of the stage's tile is done
   uint64_t* qbar = empty + kStages;                                 // Q of the next item has landed
@@ -518,7 +525,17 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
         if (lane < 16) red_sum[qq * 64 + cq * 16 + lane] = sm;
       }
       softmax_barrier<S::kSoftThreads>();
-      if (st < kN) l_run[st] = red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
+      if (st < rows) {
+        // Per row, once: 1/l (into rscale, free until the next item's first
+        // tile), the offset of the row's output, and the split's log-sum-exp.
+        const float l = red_sum[st] + red_sum[64 + st] + red_sum[128 + st] + red_sum[192 + st];
+        rscale[st] = l > 0.0f ? 1.0f / l : 0.0f;
+        const int j = st / p.group, gg = st - j * p.group;
+        const int64_t orow = ((int64_t)b * p.R + j) * p.Hq + h * p.group + gg;
+        row_out[st] = (p.n_splits == 1 ? orow : orow * p.n_splits + split) * kD;
+        if (p.n_splits > 1 && ok)
+          p.part_lse[orow * p.n_splits + split] = l > 0.0f ? (m_run[st] + log2f(l)) * kLn2 : -INFINITY;
+      }
       // ------------------------------------------------------ epilogue
       // Wait for PV of the item's last tile (global tile g-1; with it every
       // earlier MMA). The next item's first PV waits for P, which these warps
@@ -536,18 +553,10 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
         for (int x = 0; x < 16; ++x) {
           const int rloc = cq * 16 + x;
           if (rloc >= rows) continue;
-          const float l = l_run[rloc];
-          const float o = l > 0.0f ? __uint_as_float(r[x]) / l : 0.0f;
-          const int j = rloc / p.group, gg = rloc - j * p.group;
-          const int64_t orow = ((int64_t)b * p.R + j) * p.Hq + h * p.group + gg;
-          if (p.n_splits == 1) p.out[orow * kD + dv] = __float2bfloat16_rn(o);
-          else p.part_o[(orow * p.n_splits + split) * kD + dv] = o;
-        }
-        if (p.n_splits > 1 && st < rows) {
-          const float l = l_run[st];
-          const int j = st / p.group, gg = st - j * p.group;
-          const int64_t orow = ((int64_t)b * p.R + j) * p.Hq + h * p.group + gg;
-          p.part_lse[orow * p.n_splits + split] = l > 0.0f ? (m_run[st] + log2f(l)) * kLn2 : -INFINITY;
+          const float o = __uint_as_float(r[x]) * rscale[rloc];
+          const int64_t e = row_out[rloc] + dv;
+          if (p.n_splits == 1) p.out[e] = __float2bfloat16_rn(o);
+          else p.part_o[e] = o;
         }
         sm100::tc_fence_before();
       }
@@ -610,6 +619,7 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
       sm100::tma_prefetch_desc(&tm_k);
       sm100::tma_prefetch_desc(&tm_v);
       constexpr int kNoBlock = INT_MIN;
+      constexpr int kAhead = 4;   // L2 prefetch distance in tiles
       int g = 0;
       for (int k = 0; ok; ++k) {
         RingItem it;
@@ -625,13 +635,32 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
           }
           return v;
         };
-        int nb0 = raw_block(it.t0), nb1 = raw_block(it.t0 + 64);
-        for (int i = 0; i < it.n_tiles; ++i, ++g) {
-          const int b0 = nb0, b1 = nb1;
-          if (i + 1 < it.n_tiles) {
-            nb0 = raw_block(it.t0 + (i + 1) * kKeys);
-            nb1 = raw_block(it.t0 + (i + 1) * kKeys + 64);
+        // Block ids of tiles i .. i+kAhead (two per tile), read kAhead+1
+        // tiles ahead; tile i+kAhead is prefetched into L2 when tile i is
+        // loaded, so its later load finds it there.
+        int f0[kAhead + 1], f1[kAhead + 1];
+#pragma unroll
+        for (int j = 0; j <= kAhead; ++j) {
+          f0[j] = raw_block(it.t0 + j * kKeys);
+          f1[j] = raw_block(it.t0 + j * kKeys + 64);
+        }
+        auto prefetch = [&](int v) {   // the tile's boxes of one cache block (K and V, both dim halves)
+          if (v == kNoBlock || v < 0 || v >= p.num_blocks) return;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            sm100::tma_prefetch_4d(&tm_k, c * 64, it.h, 0, v);
+            sm100::tma_prefetch_4d(&tm_v, c * 64, it.h, 0, v);
           }
+        };
+        for (int i = 0; i < it.n_tiles; ++i, ++g) {
+          const int b0 = f0[0], b1 = f1[0];
+#pragma unroll
+          for (int j = 0; j < kAhead; ++j) {
+            f0[j] = f0[j + 1];
+            f1[j] = f1[j + 1];
+          }
+          f0[kAhead] = raw_block(it.t0 + (i + kAhead + 1) * kKeys);
+          f1[kAhead] = raw_block(it.t0 + (i + kAhead + 1) * kKeys + 64);
           const int s = g % kStages;
           ok = sm100::mbar_wait(&empty[s], (uint32_t)(((g / kStages) & 1) ^ 1), abort);
           if (!ok) break;
@@ -647,6 +676,15 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
                                  pol);
             }
           }
+          if (i == 0) {   // an item's first tiles: nothing prefetched them
+#pragma unroll
+            for (int j = 0; j + 1 < kAhead; ++j) {
+              prefetch(f0[j]);
+              prefetch(f1[j]);
+            }
+          }
+          prefetch(f0[kAhead - 1]);   // tile i + kAhead
+          prefetch(f1[kAhead - 1]);
         }
       }
       // Every copy must land before the CTA may exit: wait (time-limited)
@@ -803,7 +841,7 @@ bool attention_uses_gqa_tc(const mtp_attn_args& a) {
   if (a.is_mla || a.dtype != MTP_BF16 || a.d_qk != kD || a.d_v != kD) return false;
   if (a.Hkv <= 0 || a.Hq % a.Hkv != 0 || tensor_map_encoder() == nullptr) return false;
   const int rows = (a.Hq / a.Hkv) * (a.D + 1);
-  return rows > 32 && rows <= kTcMaxRows;
+  return rows >= kTcMinRows && rows <= kTcMaxRows;
 }
 
 int gqa_tc_split_granularity() { return kKeys; }
@@ -811,7 +849,7 @@ int gqa_tc_split_granularity() { return kKeys; }
 cudaError_t launch_attention_gqa_tc(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, cudaStream_t s) {
   if (a.B == 0) return cudaSuccess;
   const int R = a.D + 1, group = a.Hq / a.Hkv, rows = group * R;
-  if (pl.split_len % kKeys || rows > kTcMaxRows || rows < 1) return cudaErrorInvalidValue;
+  if (pl.split_len % kKeys || rows > kTcMaxRows || rows < kTcMinRows) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)a.Hq, (cuuint64_t)a.B * R};
@@ -853,10 +891,7 @@ cudaError_t launch_attention_gqa_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const bool tree = a.parents != nullptr;
-  const int sms = std::max(1, pl.sm_count);
-  if (rows <= 32) return launch_n<32>(tree, tq, tk, tv, p, n_items, sms, s);
-  if (rows <= 48) return launch_n<48>(tree, tq, tk, tv, p, n_items, sms, s);
-  return launch_n<64>(tree, tq, tk, tv, p, n_items, sms, s);
+  return launch_n<64>(tree, tq, tk, tv, p, n_items, std::max(1, pl.sm_count), s);
 }
 
 }  // namespace mtp

@@ -30,7 +30,7 @@ cudaError_t launch_attention_mla(const mtp_attn_args& a, const AttnPlan& p, unsi
 cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 bool attention_mma_supported(const mtp_attn_args& a);   // bf16 GQA/MHA (d 64, 128) or MLA on tensor cores
 bool attention_uses_mla_tc(const mtp_attn_args& a);
-// bf16 GQA/MHA, head dim 128, 33..64 query rows per KV head: tcgen05 kernel
+// bf16 GQA/MHA, head dim 128, 49..64 query rows per KV head: tcgen05 kernel
 bool attention_uses_gqa_tc(const mtp_attn_args& a);
 cudaError_t launch_attention_gqa_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s);

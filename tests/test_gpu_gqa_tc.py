@@ -1,11 +1,11 @@
-"""GPU parity of the tcgen05 GQA attention kernel (bf16, head dim 128, 33..64
+"""GPU parity of the tcgen05 GQA attention kernel (bf16, head dim 128, 49..64
 query rows per KV head) against the CPU oracle, every request of each case:
-ragged row counts (33, 36 rows: the Q box is not a whole number of 8-row
-swizzle groups, padding rows are zero), 48 and 64 rows, contexts that start
+ragged row counts (50, 52, 60 rows: the Q box is not a whole number of 8-row
+swizzle groups, padding rows are zero), 56 and 64 rows, contexts that start
 empty or end inside a cache block, KV splits with the combine pass, tree
-masks, a batch of several items per CTA with mixed lengths (the
-longest-first work order), and one with enough items per persistent CTA that
-the ring of published work items wraps. Cache pages are shuffled, so every tile reads two
+masks, a batch of several items per CTA with mixed lengths (the longest-first
+work order), and one with enough items per persistent CTA that the ring of
+published work items wraps. Cache pages are shuffled, so every tile reads two
 unrelated blocks."""
 import concurrent.futures as cf
 
@@ -27,26 +27,26 @@ DEV = torch.device("cuda:0")
 _G = synth.CFG3.with_(sampling="none", H=128, V=1000)
 
 CASES = {
-    # 3 heads x 11 verify tokens = 33 rows (N = 48), contexts from empty
-    "rows33_ctx_from_0": _G.with_(name="GQA tc 33 rows", B=5, D=10, Hq=6, Hkv=2, ctx=(0, 300), stream=61),
-    # 4 heads x 9 tokens = 36 rows; long contexts: KV splits and the combine
-    "rows36_splits": _G.with_(name="GQA tc 36 rows, splits", B=2, D=8, Hq=8, Hkv=2, ctx=(3000, 9000), stream=62),
-    # 16 heads x 3 tokens = 48 rows (N = 48, no padding)
-    "rows48_group16": _G.with_(name="GQA tc 48 rows", B=6, D=2, Hq=32, Hkv=2, ctx=(100, 1000), stream=63),
-    # 8 heads x 6 tokens = 48 rows: the Llama-70B grouping
-    "rows48_llama_grouping": _G.with_(name="GQA tc 8x6", B=4, D=5, Hq=64, Hkv=8, ctx=(1, 700), stream=64),
+    # 4 heads x 13 verify tokens = 52 rows, contexts from empty
+    "rows52_ctx_from_0": _G.with_(name="GQA tc 52 rows", B=5, D=12, Hq=8, Hkv=2, ctx=(0, 300), stream=61),
+    # 5 heads x 10 tokens = 50 rows; long contexts: KV splits and the combine
+    "rows50_splits": _G.with_(name="GQA tc 50 rows, splits", B=2, D=9, Hq=10, Hkv=2, ctx=(3000, 9000), stream=62),
+    # 16 heads x 4 tokens = 64 rows
+    "rows64_group16": _G.with_(name="GQA tc 16x4", B=6, D=3, Hq=32, Hkv=2, ctx=(100, 1000), stream=63),
+    # 8 heads x 7 tokens = 56 rows: the Llama-70B grouping at D = 6
+    "rows56_llama_grouping": _G.with_(name="GQA tc 8x7", B=4, D=6, Hq=64, Hkv=8, ctx=(1, 700), stream=64),
     # 8 heads x 8 tokens = 64 rows, contexts that end inside a block
     "rows64_chain": _G.with_(name="GQA tc 64 rows", B=5, D=7, Hq=16, Hkv=2, ctx=(63, 390), stream=65),
     # 4 heads x 16 tree nodes = 64 rows, random trees
     "rows64_tree_random": _G.with_(name="GQA tc tree 64 rows", B=6, D=15, Hq=8, Hkv=2, ctx=(1, 500),
                                    tree="random", stream=66),
-    # 4 heads x 12 nodes = 48 rows, random trees, long requests (splits)
-    "rows48_tree_splits": _G.with_(name="GQA tc tree, splits", B=2, D=11, Hq=4, Hkv=1, ctx=(5000, 6000),
+    # 4 heads x 15 nodes = 60 rows, random trees, long requests (splits)
+    "rows60_tree_splits": _G.with_(name="GQA tc tree, splits", B=2, D=14, Hq=4, Hkv=1, ctx=(5000, 6000),
                                    tree="random", stream=67),
-    # several waves of CTAs (B * Hkv = 480), mixed lengths: longest-first order
-    "rows40_waves_mixed": _G.with_(name="GQA tc waves", B=120, D=9, Hq=16, Hkv=4, ctx=(10, 1500), stream=68),
+    # several items per CTA (B * Hkv = 480), mixed lengths: longest-first order
+    "rows56_waves_mixed": _G.with_(name="GQA tc waves", B=120, D=13, Hq=16, Hkv=4, ctx=(10, 1500), stream=68),
     # about ten items per persistent CTA: the scheduler's ring of 8 work items wraps
-    "rows40_ring_wrap": _G.with_(name="GQA tc ring wrap", B=400, D=9, Hq=16, Hkv=4, ctx=(0, 300), stream=69),
+    "rows56_ring_wrap": _G.with_(name="GQA tc ring wrap", B=400, D=13, Hq=16, Hkv=4, ctx=(0, 300), stream=69),
 }
 
 
@@ -70,7 +70,7 @@ def _run(w):
 def test_gqa_tc_all_requests(name):
     w = CASES[name]
     rows = (w.Hq // w.Hkv) * w.R
-    assert 32 < rows <= 64 and w.d_qk == 128 and w.dtype == "bf16"
+    assert 48 < rows <= 64 and w.d_qk == 128 and w.dtype == "bf16"
     got, ref = _run(w)
     assert np.isfinite(got).all()
     assert attention_excess(got, ref, w.dtype) <= 0.0
