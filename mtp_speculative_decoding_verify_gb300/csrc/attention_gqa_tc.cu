@@ -1,7 +1,8 @@
 // GQA/MHA verify attention on the 5th-generation tensor cores, for KV heads
 // that carry 49..64 query rows (group x R: e.g. 4 heads x 16 tree nodes, 8
 // heads x 7 verify tokens), where the mma.sync kernel falls short of the
-// cache read rate (it reads the cache at the copy rate up to 48 rows).
+// cache read rate (up to 48 rows it reads the cache at 86-109 % of the
+// measured copy rate).
 //
 // "Multi Token Prediction" note, K=3 flow step 2 (stacked queries against the
 // reused cache, causal within the verify chain); tree drafts ("MTP in
@@ -32,9 +33,9 @@
 // into the next item's tiles while the softmax warps finish the current one,
 // so the stream from HBM does not stop at item boundaries.
 //
-// Warps: 0 MMA issuer, 1 K/V producer, 2 Q producer, 3 scheduler; 4.. softmax /
-// epilogue, N/4 of them: warp w owns TMEM lanes 32*(w%4)..+31 (keys of S^T,
-// dv of O^T) and the 16 row columns 16*((w-4)/4)..+15.
+// Warps: 0 MMA issuer, 1 K/V producer, 2 Q producer, 3 scheduler; 4..19
+// softmax / epilogue: warp w owns TMEM lanes 32*(w%4)..+31 (keys of S^T, dv
+// of O^T) and the 16 row columns 16*((w-4)/4)..+15.
 //
 // Online softmax with a lazy rescale (the reference row max only moves when a
 // score exceeds it by more than 8 in log2 units; P and the row sums use the
