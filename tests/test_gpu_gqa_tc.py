@@ -54,6 +54,11 @@ def _np(t):
     return t.float().cpu().numpy()
 
 
+def _ref_float(ref):
+    """Oracle output (bf16 bit patterns) as float32."""
+    return torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
 def _run(w):
     att = synth.make_attention_inputs(w, DEV)
     parents = synth.make_parents(w)
@@ -62,8 +67,7 @@ def _run(w):
     mv.sync_status()
     with cf.ThreadPoolExecutor(8) as ex:
         refs = list(ex.map(lambda b: oracle_attention(w, att, [b], parents), range(w.B)))
-    ref = np.concatenate(refs)   # bf16 bit patterns
-    return _np(out), torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy()
+    return _np(out), _ref_float(np.concatenate(refs))
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -87,3 +91,23 @@ def test_gqa_tc_chain_as_tree_matches_chain():
     tree = gpu_attention(w, att2, parents)
     mv.sync_status()
     assert torch.equal(chain, tree)
+
+
+def test_gqa_tc_range_checks_report_and_spare_other_requests():
+    """One request's first block id lies beyond the cache and another's context
+    exceeds its block table: both are reported (the block reads as zeros, the
+    long request is skipped), the other requests still match the oracle, and
+    the next call runs normally."""
+    w = CASES["rows64_chain"]
+    att = synth.make_attention_inputs(w, DEV)
+    keep = [0, 2, 4]
+    ref = _ref_float(np.concatenate([oracle_attention(w, att, [b]) for b in keep]))
+    att["block_table"][1, 0] = 10 ** 6
+    att["ctx_lens"][3] = w.max_blocks * 64
+    out = gpu_attention(w, att)
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert ei.value.code == 4 and "block-id" in str(ei.value) and "length" in str(ei.value)
+    assert attention_excess(_np(out)[keep], ref, w.dtype) <= 0.0
+    got, ref2 = _run(CASES["rows64_tree_random"])
+    assert attention_excess(got, ref2, "bf16") <= 0.0
