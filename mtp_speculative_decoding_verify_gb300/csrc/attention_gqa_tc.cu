@@ -73,8 +73,8 @@ constexpr float kLazyRescale = 8.0f;   // log2 units
 constexpr int kQOff = 0;                                   // 2 x [N rows x 128 B], at most 16 KB
 constexpr int kStageOff = 16384;
 constexpr int kRedOff = kStageOff + kStages * kStageBytes; // red_max[4][64], red_sum[4][64]
-constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;          // m_run, l_run, m_ref, rscale, path, m_shift [64]
-constexpr int kRowOffOut = kRowOff + 6 * 64 * 4;           // int64 [64]: output element offset of each row
+constexpr int kRowOff = kRedOff + 2 * 4 * 64 * 4;          // m_run, m_ref, rscale, path, m_shift [64]
+constexpr int kRowOffOut = kRowOff + 5 * 64 * 4;           // int64 [64]: output element offset of each row
 constexpr int kBarOff = kRowOffOut + 64 * 8;
 constexpr int kRing = 8;                                   // work items published ahead by the scheduler warp
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1 + 2 * kRing;
@@ -316,11 +316,10 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
   float* red_max = reinterpret_cast<float*>(smem + kRedOff);
   float* red_sum = red_max + 4 * 64;
   float* m_run = reinterpret_cast<float*>(smem + kRowOff);
-  float* l_run = m_run + 64;
-  float* m_ref = m_run + 128;
-  float* rscale = m_run + 192;
-  uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 256);   // per row: path mask (tree) or key limit (chain)
-  float* m_shift = m_run + 320;
+  float* m_ref = m_run + 64;
+  float* rscale = m_run + 128;
+  uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 192);   // per row: path mask (tree) or key limit (chain)
+  float* m_shift = m_run + 256;
   int64_t* row_out = reinterpret_cast<int64_t*>(smem + kRowOffOut);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kStages]: the stage holds its tile
   uint64_t* empty = full + kStages;                                 // [kStages]: PV of the stage's tile is done
@@ -410,7 +409,6 @@ __global__ void __launch_bounds__(Shape<kN>::kThreads, 1) attn_gqa_tc_kernel(con
         path[st] = kTree ? tree_path_mask(p.parents, b, p.R, j, p.err) : (uint32_t)(ctx + j);
         m_run[st] = -INFINITY;
         m_ref[st] = 0.0f;
-        l_run[st] = 0.0f;
       }
       softmax_barrier<S::kSoftThreads>();
       float acc[16];
