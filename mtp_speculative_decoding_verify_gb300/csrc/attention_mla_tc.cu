@@ -18,10 +18,8 @@
 // Slots are released as PV stops needing them and refilled with the next
 // tile (prefetched into L2 one tile ahead), so loads overlap PV.
 //
-// The row blocks of one request may form a thread-block cluster (up to
-// MTP_MLA_MAX_CLUSTER CTAs): every slot fill is fetched from L2 once per
-// cluster with a TMA multicast (fills spread round-robin over the CTAs) and
-// released by a multicast tcgen05.commit from each CTA's MMA thread.
+// This single-CTA form serves requests whose 64-row blocks do not pair up
+// (an odd count); each CTA fetches its own copy of every key tile.
 //
 // Warps (5 warpgroups): 0 MMA issuer, 1-3 TMA producers (lanes 0 and 1 of
 // each issue one 8 KB box at a time, so six copies stay in flight), 4..19
@@ -44,10 +42,6 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
-
-#ifndef MTP_MLA_MAX_CLUSTER
-#define MTP_MLA_MAX_CLUSTER 2
-#endif
 
 namespace mtp {
 
@@ -75,7 +69,6 @@ static_assert(128 * kRegsLight + 4 * 128 * kRegsSoftmax <= kThreads * kLaunchReg
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazyRescale = 8.0f;  // log2 units
-constexpr int kMaxCluster = MTP_MLA_MAX_CLUSTER;   // CTAs (row blocks) sharing each KV tile by TMA multicast
 
 constexpr int kQOff = 0;                                    // 9 x 8 KB
 constexpr int kSlotOff = kQOff + kQChunks * 8192;           // 73728
@@ -100,8 +93,8 @@ struct Params {
   const int32_t* parents; // [B, R] tree drafts, nullptr: chains
   unsigned* err;
   int B, R, Hq, max_blocks, num_blocks, split_len, n_splits;
-  int groups;           // row-block clusters per request
-  int cluster;          // CTAs per cluster (row blocks of one request sharing each KV tile by multicast)
+  int groups;           // work groups per request: row blocks (single CTA) or row-block pairs (CTA pairs)
+  int cluster;          // CTAs per work group: 1, or 2 for the CTA-pair kernel
   float scale_log2;
 };
 
@@ -176,9 +169,9 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
   return v[0];
 }
 
-// A work item is (split, request, cluster g of C row blocks): item index
-// i = (split * B + b) * groups + g. Every CTA of the cluster walks the keys
-// [t0, t_end) visible to the cluster's last row.
+// A work item is (split, request, group g of C row blocks): item index
+// i = (split * B + b) * groups + g. Every CTA of the group walks the keys
+// [t0, t_end) visible to the group's last row.
 struct Item {
   int split, b, g;
 };
@@ -287,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 256);   // per row: path mask (tree) or key limit (chain)
   float* m_shift = m_run + 320;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);   // [kSlots]: slot c holds this tile's chunk c
-  uint64_t* empty = full + kSlots;                                  // [kSlots]: every cluster CTA is done with it
+  uint64_t* empty = full + kSlots;                                  // [kSlots]: the MMAs are done with it
   uint64_t* qbar = empty + kSlots;
   uint64_t* s_full = qbar + 1;
   uint64_t* s_empty = s_full + kSBufs;
@@ -298,20 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int C = p.cluster;
-  const uint32_t rank = C > 1 ? sm100::cluster_ctarank() : 0u;
-  const Item item = decode_item(p.order[blockIdx.x / C], p.B, p.groups);
+  constexpr int C = 1;   // one row block per work item
+  const Item item = decode_item(p.order[blockIdx.x], p.B, p.groups);
   const int split = item.split, b = item.b;
   const int rows = p.R * p.Hq;
-  const int row_base = (item.g * C + (int)rank) * kRows;
-  const uint16_t peers = (uint16_t)((1u << C) - 1u);
+  const int row_base = item.g * kRows;
   const int ctx = p.ctx_lens[b];
-  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {   // uniform over the cluster (same request)
+  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {
     if (threadIdx.x == 0 && split == 0 && row_base == 0) raise_error(p.err, MTP_ERR_LENGTH);
     return;
   }
-  // Every CTA of a cluster walks the same keys (those visible to the cluster's
-  // last row); rows that see fewer keys mask the rest.
+  // The CTA walks the keys visible to its last row; rows that see fewer keys
+  // mask the rest.
   const int t0 = split * p.split_len;
   const int t_end = item_key_end(item, ctx, p.R, p.Hq, rows, C, p.split_len);
   if (t0 >= t_end) return;  // no key of this split is visible to these rows: the combine skips it
@@ -320,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int c = 0; c < kSlots; ++c) {
       sm100::mbar_init(&full[c], 2);   // one arrival per box
-      sm100::mbar_init(&empty[c], C);
+      sm100::mbar_init(&empty[c], 1);
     }
     sm100::mbar_init(qbar, 1);
     for (int i = 0; i < kSBufs; ++i) {
@@ -346,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
   }
   sm100::tc_fence_before();
   __syncthreads();
-  if (C > 1) sm100::cluster_sync();   // peers' barriers exist before any multicast lands
   sm100::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t smem_base = sm100::smem_u32(smem);
@@ -535,10 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       // A tile is 18 boxes of [64 keys x 64 dims] (8 KB): box x = slot x/2,
       // keys 64*(x%2).. of the tile. Producer pw owns boxes pw, pw+6, pw+12
       // (slots in the order the MMA consumes them) and refills a box as soon
-      // as every cluster CTA released its slot from the previous tile. Each
+      // as the MMAs released its slot from the previous tile. Each
       // box issue is followed by an L2 prefetch of the same box of the next
       // tile, so that the refill after the release hits L2.
-      const uint64_t pol_kv = sm100::l2_policy_evict_last();   // the cluster's other row blocks re-read it
+      const uint64_t pol_kv = sm100::l2_policy_evict_last();   // the request's other row blocks re-read it
       if (pw == 0) {
         sm100::tma_prefetch_desc(&tm_q);
         sm100::tma_prefetch_desc(&tm_kv);
@@ -565,15 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
           ok = sm100::mbar_wait(&empty[c], (uint32_t)((i & 1) ^ 1), abort);
           if (!ok) break;
           sm100::mbar_arrive_expect_tx(&full[c], kSlotBytes / 2);
-          if ((i * 2 * kSlots + x) % C == (int)rank) {
-            const int blk = block_of(t0 + i * kKeys + half * 64);
-            uint8_t* dst = smem + kSlotOff + c * kSlotBytes + half * (kSlotBytes / 2);
-            if (C > 1) sm100::tma_load_3d_mc(dst, &tm_kv, &full[c], c * 64, 0, blk, peers, pol_kv);
-            else sm100::tma_load_3d(dst, &tm_kv, &full[c], c * 64, 0, blk, pol_kv);
-            if (i + 1 < n_tiles) {
-              const int nblk = block_of(t0 + (i + 1) * kKeys + half * 64);
-              if (nblk >= 0) sm100::tma_prefetch_3d(&tm_kv, c * 64, 0, nblk);
-            }
+          const int blk = block_of(t0 + i * kKeys + half * 64);
+          uint8_t* dst = smem + kSlotOff + c * kSlotBytes + half * (kSlotBytes / 2);
+          sm100::tma_load_3d(dst, &tm_kv, &full[c], c * 64, 0, blk, pol_kv);
+          if (i + 1 < n_tiles) {
+            const int nblk = block_of(t0 + (i + 1) * kKeys + half * 64);
+            if (nblk >= 0) sm100::tma_prefetch_3d(&tm_kv, c * 64, 0, nblk);
           }
         }
       }
@@ -590,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       // ---------------------------------------------------------------- MMA
       // QK(i) over the 9 resident chunks, then (once P(i) is published) PV(i)
       // reading V^T MN-major from chunk slots 2dc, 2dc+1 and P^T from the rope
-      // slot; each slot is released to every cluster CTA as soon as PV(i) no
+      // slot; each slot is released to the producers as soon as PV(i) no
       // longer needs it, so tile i+1 loads overlap PV(i). Descriptors are
       // formed once and advanced by constants (16-byte units in the start
       // address field): the issue loop must stay far below one MMA's time.
@@ -600,10 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
       const uint64_t d_q = desc_kmajor(smem_base + kQOff);
       const uint64_t d_vt = desc_mnmajor(smem_base + kSlotOff, kSlotBytes);
       const uint64_t d_p = desc_kmajor(p_base);
-      auto release = [&](int c) {
-        if (C > 1) sm100::tc_commit_mc(&empty[c], peers);
-        else sm100::tc_commit(&empty[c]);
-      };
+      auto release = [&](int c) { sm100::tc_commit(&empty[c]); };
       bool ok = sm100::mbar_wait(qbar, 0, abort);
       auto issue_qk = [&](int i) -> bool {
         const int buf = i % kSBufs;
@@ -662,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
     sm100::tc_fence_after();
     sm100::tmem_dealloc(tmem, kTmemCols);
   }
-  if (C > 1) sm100::cluster_sync();   // no peer may still multicast into, or arrive on, this CTA
 }
 
 // ----------------------------------------------------------------------------
@@ -1158,11 +1141,9 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   p.n_splits = pl.n_splits;
   p.scale_log2 = a.sm_scale * kLog2e;
   const int row_blocks = (rows + kRows - 1) / kRows;
-  // Row blocks pair up: the CTA-pair kernel; otherwise single-CTA MMAs, with
-  // clusters of up to kMaxCluster row blocks sharing each fill by multicast.
+  // Row blocks pair up: the CTA-pair kernel; otherwise one CTA per row block.
   const bool paired = row_blocks % 2 == 0;
-  int C = paired ? 2 : kMaxCluster;
-  while (row_blocks % C) --C;
+  const int C = paired ? 2 : 1;
   p.cluster = C;
   p.groups = row_blocks / C;
   const int n_items = pl.n_splits * a.B * p.groups;
