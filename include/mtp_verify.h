@@ -260,8 +260,11 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* args, void* stream);
  * than the array, e.g. sampling requests with a large M * V) is rejected with
  * MTP_INVALID_ARG and a message. Nothing here allocates: no cudaMalloc,
  * cudaFree or allocating library routine.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current). Every call on a device shares the one
+ * The first call on a device looks up the array's device address, with that
+ * device current; it does so again on the first call after the device's
+ * context was replaced (cudaDeviceReset), since the array then sits at a new
+ * address. Make that first call before any stream capture begins on the
+ * device. Every call on a device shares the one
  * array and leaves its contents behind; each call writes all the scratch it
  * reads before reading it, so nothing needs clearing in between. Calls whose
  * kernels overlap on the GPU (e.g. on two streams) race on the array: issue
@@ -346,7 +349,12 @@ int mtp_tree_kv_compact(const mtp_kv_compact_args* args, void* stream);
  * keep their K/V). Every block index i with ceil((ctx+n+1)/64) <= i <=
  * (ctx+D)/64 is appended to free_list at position *free_count (request-major,
  * block index ascending) and block_table[b][i] is set to -1; *free_count is
- * advanced. Writes beyond free_capacity set MTP_ERR_FREE_LIST and are skipped.
+ * advanced. A request is rolled back whole or not at all: when free_list
+ * cannot take all of its freed blocks after those of every earlier request
+ * (position + count > free_capacity), its table row and seq_lens entry are
+ * left as they were (seq_lens[b] still equals ctx, so the caller can find it)
+ * and MTP_ERR_FREE_LIST is raised; requests that free no block are still
+ * rolled back, and *free_count ends one past the last block appended.
  *   block_table [B, max_blocks] int32 (in/out); seq_lens [B] int32 (in/out)
  *   num_accepted [B] int32; free_list [free_capacity] int32; free_count [1] int32
  */

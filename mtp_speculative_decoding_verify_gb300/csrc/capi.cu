@@ -13,6 +13,7 @@
 #include "kernels.h"
 
 namespace mtp {
+unsigned long long current_context_id();
 int lmhead_simt_slices(int V, int sm_count);
 int lmhead_tc_slices(int V, int M, int sm_count);
 bool lmhead_tc_supported(const mtp_lmhead_args& a);
@@ -38,7 +39,7 @@ __device__ unsigned g_error_word;
 
 constexpr int kMaxDevices = 64;
 struct DeviceCtx {
-  bool ready = false;
+  unsigned long long ctx_id = 0;   // context the entries below belong to (0: not set up)
   unsigned* err = nullptr;
   int sm_count = 0;
 };
@@ -61,7 +62,9 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 // Per-device context: the device address of the error word (host code may
-// not use the symbol itself) and the SM count. Set up once per device.
+// not use the symbol itself) and the SM count. Set up on the first call on a
+// device, and again whenever the device's context is not the one the address
+// came from (after cudaDeviceReset the module is loaded anew, at a new address).
 int device_ctx(DeviceCtx** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -69,14 +72,15 @@ int device_ctx(DeviceCtx** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(MTP_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceCtx& c = g_dev[dev];
-  if (!c.ready) {
+  const unsigned long long id = mtp::current_context_id();
+  if (id == 0 || c.ctx_id != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_error_word);
+    e = cudaGetSymbolAddress(&p, g_error_word);   // also makes the primary context current
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
     e = cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     c.err = static_cast<unsigned*>(p);
-    c.ready = true;
+    c.ctx_id = mtp::current_context_id();
   }
   *out = &c;
   return MTP_OK;

@@ -19,6 +19,7 @@
 #include "kernels.h"
 
 namespace mtp {
+unsigned long long current_context_id();
 int check_lmhead_args(const mtp_lmhead_args* a);
 int device_context(unsigned** err, int* sm_count);
 int set_error(int code, const char* msg);
@@ -34,25 +35,34 @@ constexpr size_t kNoAllocScratchBytes = MTP_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;   // context the address belongs to (0: not looked up yet)
+  void* ptr = nullptr;
+};
+ScratchSlot g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
 // Device address of the scratch array on the current device. Host code must
 // not use the symbol itself: on the host it names a stand-in, not device
-// memory. Looked up once per device, with that device current.
+// memory. Looked up with the device current, on the first call on that
+// device and again whenever the device's context is not the one the address
+// came from (a cudaDeviceReset loads the module anew, at a new address).
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return mtp::set_error(MTP_UNSUPPORTED, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  const unsigned long long id = mtp::current_context_id();
+  if (id == 0 || slot.ctx_id != id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaGetSymbolAddress(no-alloc scratch)");
-    g_scratch_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = mtp::current_context_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return MTP_OK;
 }
 
