@@ -10,6 +10,13 @@
 // Blocks that held verify slots but no kept slot return to the free list in
 // request order, then block order. One CTA walks the batch in chunks of its
 // thread count with a block-wide exclusive scan of the per-request counts.
+//
+// A request is rolled back whole or not at all: if the free list cannot take
+// all of its freed blocks (counting every earlier request's blocks), its
+// table row and length stay as they were and MTP_ERR_FREE_LIST is raised.
+// The running count is monotone, so past the first request that does not fit
+// only requests that free nothing are still rolled back; *free_count ends at
+// the last block actually appended.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,9 +33,10 @@ __global__ void __launch_bounds__(kThreads) kv_rollback_kernel(int32_t* __restri
                                                                int32_t* __restrict__ free_count, int B, int D,
                                                                int max_blocks, int capacity, unsigned* err) {
   __shared__ int s_warp[kThreads / kWarp];
-  __shared__ int s_base;
+  __shared__ int s_base;   // free-list position of the chunk's first block (all earlier requests counted)
+  __shared__ int s_end;    // one past the last block appended
   const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-  if (tid == 0) s_base = *free_count;
+  if (tid == 0) s_base = s_end = *free_count;
   __syncthreads();
   for (int start = 0; start < B; start += kThreads) {
     const int b = start + tid;
@@ -71,23 +79,24 @@ __global__ void __launch_bounds__(kThreads) kv_rollback_kernel(int32_t* __restri
     const int excl = incl - cnt + (warp > 0 ? s_warp[warp - 1] : 0);
     const int total = s_warp[kWarp - 1];
     if (b < B && kept >= 0) {
-      int32_t* row = block_table + (int64_t)b * max_blocks;
-      for (int i = 0; i < cnt; ++i) {
-        const int pos = s_base + excl + i;
-        if (pos < capacity) {
-          free_list[pos] = row[first + i];
+      const int pos0 = s_base + excl;
+      if (cnt == 0 || (pos0 >= 0 && (long long)pos0 + cnt <= (long long)capacity)) {
+        int32_t* row = block_table + (int64_t)b * max_blocks;
+        for (int i = 0; i < cnt; ++i) {
+          free_list[pos0 + i] = row[first + i];
           row[first + i] = -1;
-        } else {
-          raise_error(err, MTP_ERR_FREE_LIST);
         }
+        seq_lens[b] = kept;
+        if (cnt > 0) atomicMax(&s_end, pos0 + cnt);
+      } else {
+        raise_error(err, MTP_ERR_FREE_LIST);   // left as it was: table row, length
       }
-      seq_lens[b] = kept;
     }
     __syncthreads();
     if (tid == 0) s_base += total;
     __syncthreads();
   }
-  if (tid == 0) *free_count = min(s_base, capacity);
+  if (tid == 0) *free_count = s_end;
 }
 
 cudaError_t launch_rollback(const mtp_rollback_args& a, unsigned* err, cudaStream_t s) {

@@ -23,8 +23,9 @@ if not torch.cuda.is_available():  # collected on CPU hosts too; the marker keep
 import oracle  # noqa: E402
 import mtp_speculative_decoding_verify_gb300 as mv  # noqa: E402
 from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
-from gpu_util import (A, TOL_LOGITS, attention_excess, TOL_LSE_REL, check_invariants, compare_accept,  # noqa: E402
-                      gpu_attention, gpu_lmhead, gpu_rollback, oracle_attention, oracle_lmhead)
+from gpu_util import (A, TOL_ATTN, TOL_LOGITS, attention_excess, attention_over_plain, TOL_LSE_REL,  # noqa: E402
+                      check_invariants, compare_accept, gpu_attention, gpu_lmhead, gpu_rollback, oracle_attention,
+                      oracle_lmhead)
 from philox_py import philox_vec, race_exponential_vec  # noqa: E402
 
 DEV = torch.device("cuda:0")
@@ -75,12 +76,16 @@ def _oracle_attn_parallel(w, att, reqs):
 
 
 def _check_attention(w, att, out, reqs):
-    ref = _oracle_attn_parallel(w, att, reqs)
+    """Every element within the attention bound of the oracle's exact value;
+    the count above the plain bound (the share that only the output's own
+    rounding carries over it) is printed."""
+    exact = _oracle_attn_parallel(w, att, reqs)
     got = out.index_select(0, torch.tensor(list(reqs), device=DEV)).float().cpu().numpy()
-    ref = ref.astype(np.float32) if ref.dtype == np.float32 else \
-        torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy()
-    err = float(np.abs(got - ref).max())
-    assert attention_excess(got, ref, w.dtype) <= 0.0, err
+    err = float(np.abs(got - exact).max())
+    n_over, frac = attention_over_plain(got, exact, w.dtype)
+    print("attention %s: max |err| %.3g, %d element(s) (%.2g) above the plain %g" %
+          (w.name, err, n_over, frac, TOL_ATTN[w.dtype]))
+    assert attention_excess(got, exact, w.dtype) <= 0.0, err
     return err
 
 
@@ -298,12 +303,29 @@ def test_rollback_many_requests_and_capacity():
     oracle.kv_rollback(t_h, s_h, n, fl, fc, D=w.D, block_size=64)
     assert (g_seq.cpu().numpy() == s_h).all() and (g_table.cpu().numpy() == t_h).all()
     assert int(g_fc.item()) == int(fc[0]) and (g_fl.cpu().numpy() == fl).all()
-    # A free list that is too short is reported, not overrun.
-    g_table, g_seq, g_fl, g_fc = gpu_rollback(w, t_d, c_d, n_d, capacity=10)
-    with pytest.raises(mv.MtpError) as ei:
-        mv.sync_status()
-    assert ei.value.code == 4
-    assert int(g_fc.item()) == 10
+    # A free list that is too short is reported, not overrun, and no request
+    # is left half rolled back: the requests before the first one whose blocks
+    # do not fit are rolled back (as the oracle does them), later requests that
+    # free nothing get their new length, and the others are left untouched.
+    for cap in (10, 11, 257):
+        g_table, g_seq, g_fl, g_fc = gpu_rollback(w, t_d, c_d, n_d, capacity=cap)
+        with pytest.raises(mv.MtpError) as ei:
+            mv.sync_status()
+        assert ei.value.code == 4
+        cnt = np.maximum((ctx + w.D) // 64 - (ctx + n + 1 + 63) // 64 + 1, 0)
+        f = int(np.argmax(np.cumsum(cnt) > cap))
+        t_h, s_h = table.copy(), ctx.copy()
+        fl = np.full(int(cnt[:f].sum()), -1, np.int32)
+        fc = np.zeros(1, np.int32)
+        t_pre, s_pre = t_h[:f].copy(), s_h[:f].copy()
+        oracle.kv_rollback(t_pre, s_pre, n[:f].copy(), fl, fc, D=w.D, block_size=64)
+        t_h[:f], s_h[:f] = t_pre, s_pre
+        zero = np.arange(w.B) >= f
+        zero &= cnt == 0
+        s_h[zero] = ctx[zero] + n[zero] + 1
+        assert (g_seq.cpu().numpy() == s_h).all() and (g_table.cpu().numpy() == t_h).all()
+        assert int(g_fc.item()) == int(fc[0]) <= cap
+        assert (g_fl.cpu().numpy()[:int(fc[0])] == fl).all()
 
 
 def test_device_range_checks_report_and_recover():
