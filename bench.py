@@ -477,36 +477,6 @@ def decode_baseline(args, w, dev):
     return t0.elapsed_time(t1) / args.steps
 
 
-def oracle_request(w, att, lm, W, table, ctx, b):
-    """The oracle's whole verify step for request b: append + attention, LM
-    head + acceptance, KV compaction (tree drafts) and rollback."""
-    import oracle
-    from gpu_util import oracle_attention, oracle_lmhead  # noqa: E402
-    parents = lm.get("parents")
-    _, kc, vc, sub_table = oracle_attention(w, att, [b], parents, return_cache=True)
-    r = oracle_lmhead(w, lm, [b], W)
-    if parents is not None:
-        oracle.tree_kv_compact(kc, vc, sub_table, ctx[b:b + 1], r["accepted_nodes"], r["num_accepted"], D=w.D,
-                               Hkv=1 if w.is_mla else w.Hkv, d_qk=w.d_qk, d_v=w.d_v, block_size=64,
-                               is_mla=w.is_mla)
-    fl = np.zeros(w.D // 64 + 4, np.int32)
-    fc = np.zeros(1, np.int32)
-    oracle.kv_rollback(table[b:b + 1].copy(), ctx[b:b + 1].copy(), r["num_accepted"], fl, fc, D=w.D, block_size=64)
-
-
-def draft_oracle_request(w, inp, W, b):
-    """The oracle's D greedy draft steps of request b (argmax rows)."""
-    import oracle
-    toks = np.zeros((1, 1), np.int32)
-    mode = np.zeros(1, np.uint8)
-    out = []
-    for k in range(w.D):
-        h = synth.as_oracle_array(inp["hidden"][k, b:b + 1])
-        r = oracle.lmhead_accept(h, W, toks, mode, None, None, 0)
-        out.append(int(r["argmax"][0, 0]))
-    return out
-
-
 def _timed_requests(fn, n_items, seconds, threads):
     """Run fn(i) for i = 0, 1, ... (at most n_items) on `threads` threads until
     `seconds` have passed (each thread finishes the request it is in); returns
@@ -537,12 +507,12 @@ def cpu_baseline(w, seconds, dev=None, draft=False):
     + rollback, or the D draft steps), first on one thread, then on every host
     core (one unmodified single-threaded oracle call per request and thread;
     the calls release the interpreter lock)."""
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import requests as oreq
     gen_dev = dev if dev is not None else torch.device("cpu")
     if draft:
         inp = synth.make_draft_inputs(w, gen_dev)
         W = synth.as_oracle_array(inp["lm_head"])
-        fn = lambda i: draft_oracle_request(w, inp, W, i % w.B)  # noqa: E731
+        fn = lambda i: oreq.draft_request(w, inp, W, i % w.B)  # noqa: E731
         what = "%d greedy draft steps each" % w.D
     else:
         att = synth.make_attention_inputs(w, gen_dev)
@@ -550,7 +520,7 @@ def cpu_baseline(w, seconds, dev=None, draft=False):
         W = synth.as_oracle_array(lm["lm_head"])
         table = synth.as_oracle_array(att["block_table"])
         ctx = synth.as_oracle_array(att["ctx_lens"])
-        fn = lambda i: oracle_request(w, att, lm, W, table, ctx, i % w.B)  # noqa: E731
+        fn = lambda i: oreq.whole_request(w, att, lm, W, table, ctx, i % w.B)  # noqa: E731
         what = "attention + LM head + acceptance + rollback"
     n1, el1 = _timed_requests(fn, 4 * w.B, seconds, 1)
     cores = os.cpu_count() or 1
@@ -573,13 +543,13 @@ def run_reference(args, w, rank, world):
     if rank != 0:
         return
     import concurrent.futures as cf
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import requests as oreq
     gen_dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if torch.cuda.is_available() else "cpu"
     draft = is_draft(args.workload)
     if draft:
         inp = synth.make_draft_inputs(w, gen_dev)
         Wd = synth.as_oracle_array(inp["lm_head"])
-        one = lambda b: draft_oracle_request(w, inp, Wd, b)  # noqa: E731
+        one = lambda b: oreq.draft_request(w, inp, Wd, b)  # noqa: E731
         what = "%d greedy draft steps" % w.D
     else:
         att = synth.make_attention_inputs(w, gen_dev)
@@ -587,7 +557,7 @@ def run_reference(args, w, rank, world):
         W = synth.as_oracle_array(lm["lm_head"])
         table = synth.as_oracle_array(att["block_table"])
         ctx = synth.as_oracle_array(att["ctx_lens"])
-        one = lambda b: oracle_request(w, att, lm, W, table, ctx, b)  # noqa: E731
+        one = lambda b: oreq.whole_request(w, att, lm, W, table, ctx, b)  # noqa: E731
         what = "attention + LM head + acceptance + rollback"
     cores = os.cpu_count() or 1
     with cf.ThreadPoolExecutor(cores) as ex:

@@ -25,7 +25,7 @@ def lib():
         i32, u32, u64, f32 = ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox4x32_10.restype = None
-        L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 9
+        L.oracle_verify_attention.argtypes = [i32] * 9 + [i32, f32, i32] + [P] * 10
         L.oracle_verify_attention.restype = i32
         L.oracle_lmhead_accept.argtypes = [i32] * 5 + [P] * 6 + [u64] + [P] * 7 + [i32, ctypes.c_float, P, P]
         L.oracle_lmhead_accept.restype = i32
@@ -96,9 +96,11 @@ def race(w, E):
 
 
 def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *, D, Hq, Hkv,
-                     d_qk, d_v, block_size, is_mla, sm_scale, parents=None):
-    """Append + verify attention. k_cache / v_cache are updated in place; returns out.
-    parents [B, R] int32 (None: chains) gives tree drafts."""
+                     d_qk, d_v, block_size, is_mla, sm_scale, parents=None, want_exact=False):
+    """Append + verify attention. k_cache / v_cache are updated in place; returns out
+    (rounded to the input dtype), or (out, exact) with want_exact, exact being
+    the float64 result before that rounding. parents [B, R] int32 (None:
+    chains) gives tree drafts."""
     q, dt = _storage(q)
     k_new, _ = _storage(k_new)
     v_new = None if v_new is None else _storage(v_new)[0]
@@ -108,14 +110,15 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, *
     B = ctx.shape[0]
     R = D + 1
     out = np.zeros((B, R, Hq, d_v), dtype=q.dtype)
+    exact = np.zeros((B, R, Hq, d_v), dtype=np.float64) if want_exact else None
     num_blocks = k_cache.shape[0]
     rc = lib().oracle_verify_attention(B, D, Hq, Hkv, d_qk, d_v, block_size, bt.shape[1], num_blocks,
                                        int(is_mla), float(sm_scale), dt, _ptr(q), _ptr(k_new), _ptr(v_new),
                                        _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(ctx), _ptr(out),
-                                       _ptr(None if parents is None else _c(parents, np.int32)))
+                                       _ptr(None if parents is None else _c(parents, np.int32)), _ptr(exact))
     if rc != 0:
         raise ValueError("oracle_verify_attention returned %d" % rc)
-    return out
+    return (out, exact) if want_exact else out
 
 
 def lmhead_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, *, want_logits=False,

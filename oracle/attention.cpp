@@ -19,7 +19,9 @@
  * continues. The chain is the tree with parents[k] = k - 1.
  *
  * Scores, softmax and the weighted sum are evaluated in double; the result is
- * rounded once to the output dtype.
+ * rounded once to the output dtype (and, on request, also returned unrounded,
+ * so a caller can measure another implementation's error against the exact
+ * value rather than against a second rounding of it).
  */
 #include <math.h>
 #include <stdlib.h>
@@ -33,7 +35,7 @@ extern "C" int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, 
                                        const void* q, const void* k_new, const void* v_new,
                                        void* k_cache, void* v_cache,
                                        const int32_t* block_table, const int32_t* ctx_lens,
-                                       void* out, const int32_t* parents) {
+                                       void* out, const int32_t* parents, double* out_exact) {
   if (B < 0 || D < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d_qk <= 0 || d_v <= 0 ||
       block_size <= 0 || max_blocks <= 0 || num_blocks <= 0 || (dtype != 0 && dtype != 1))
     return ORACLE_BAD_ARG;
@@ -123,7 +125,10 @@ extern "C" int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, 
           const void* vsrc = is_mla ? (const void*)k_cache : (const void*)v_cache;
           for (int e = 0; e < d_v; ++e) acc[e] += score[i] * oracle_load(vsrc, dtype, v0 + e);
         }
-        for (int e = 0; e < d_v; ++e) oracle_store(out, dtype, obase + e, acc[e] / z);
+        for (int e = 0; e < d_v; ++e) {
+          oracle_store(out, dtype, obase + e, acc[e] / z);
+          if (out_exact) out_exact[obase + e] = acc[e] / z;
+        }
       }
     }
   }

@@ -62,6 +62,8 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
  *            Fig. 9), parents[b][0] = -1 and 0 <= parents[b][k] < k; row j
  *            then sees the context and the verify keys of the nodes on the
  *            path from the root to node j (itself included)
+ *   out_exact [B, R, Hq, d_v] double or NULL: the same result before it is
+ *            rounded to the output dtype
  * Returns ORACLE_BAD_INDEX if a block id needed is outside [0, num_blocks). */
 int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
                             int block_size, int max_blocks, int num_blocks,
@@ -69,7 +71,7 @@ int oracle_verify_attention(int B, int D, int Hq, int Hkv, int d_qk, int d_v,
                             const void* q, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache,
                             const int32_t* block_table, const int32_t* ctx_lens,
-                            void* out, const int32_t* parents);
+                            void* out, const int32_t* parents, double* out_exact);
 
 /* LM head + row statistics + acceptance ([K3] steps 4-6; [VLLM] §三 stages 3-4;
  * [SDMTP] §2.3, §4.4).

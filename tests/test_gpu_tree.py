@@ -42,7 +42,7 @@ def _out_np(w, t):
 
 
 def _ref_np(ref):
-    if ref.dtype == np.float32:
+    if ref.dtype in (np.float32, np.float64):
         return ref
     return torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy()
 
