@@ -5,12 +5,15 @@ A step is the whole verify path for one batch: mtp_verify_attention (KV
 append + multi-query verify attention), mtp_verify_logits_accept (LM head
 with streaming softmax statistics + acceptance) and kv_rollback, on seeded
 synthetic inputs already resident in HBM. The default workload is the
-DeepSeek-V3-shaped greedy MTP batch (B=32 requests, D=3 drafts, absorbed MLA
-128 heads x 576/512, contexts 512-4096, hidden 7168, vocab 129280, bf16).
+largest one-GPU batch: B=256 requests, D=3 drafts, GQA 32 query / 8 KV heads
+x 128, contexts 1k-32k tokens in 64-token pages (17.7 GB of KV cache), hidden
+4096, vocabulary 151936, bf16; half the requests greedy, half rejection
+sampling at temperature 0.7.
 
 Output: one JSON line on rank 0 with requests/s (value), accepted tokens/s,
-the roofline of the dominant kernel, an end-to-end number through the C ABI
-with host buffers, and a CPU baseline (the oracle on a bounded sample).
+the roofline of the dominant kernel (and of the other large one), an
+end-to-end number through the C ABI with host buffers, and a CPU baseline
+(the oracle on a bounded sample).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
 
@@ -40,6 +43,7 @@ from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
 METRIC = "verify-step requests/s and accepted tokens/s on 1 GB300; % of HBM/TC roofline"
 DRAFT_METRIC = "draft-step requests/s (D sequential greedy LM-head calls) on 1 GB300; % of HBM/TC roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal
 
 
 def workloads():
@@ -71,6 +75,9 @@ def workloads():
         "profile_tree_gqa_B16": synth.CFG3.with_(name="profiling case: large-batch mixed GQA, trees of 15 drafts, "
                                                       "B=16, vocab 32768", B=16, D=15, tree="full", sampling="none",
                                                  V=32768),
+        "profile_lm_cfg3_V64k": synth.CFG3.with_(
+            name="profiling case: large-batch mixed LM head M=1024 (B=256 D=3), vocab 65536, contexts 64-128",
+            V=65536, ctx=(64, 128)),
         "profile_sampling_V32k": synth.CFG2.with_(
             name="profiling case: Llama-70B-shaped rejection sampling B=64 D=5, vocab 32768", V=32768),
         # MTP-Eagle draft steps: D sequential greedy top-1 calls over the shared LM head, B rows each.
@@ -96,12 +103,40 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-# DRAM bytes per launch of the LM-head kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), by workload. The capture ran
-# a reduced vocabulary (32768) of the same kernel and shapes; traffic grows in
-# proportion to the vocabulary, so it is scaled to the full one. Only valid
-# while the kernel is unchanged since the capture (profiles/ names the file).
-LMHEAD_TRAFFIC_PER_VOCAB_ROW = {"cfg1_D3": (471.696896e6 + 2.870272e6) / 32768}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of a workload's large kernels, from one ncu capture of a reduced case of the
+# same kernel and shapes, scaled to the full workload by the units it
+# processes (the traffic of both kernels grows in proportion to them: every
+# W tile and every KV page is read once). Each entry names the kernel's
+# source files and their SHA-256 (first 16 hex digits) at capture time; once
+# a source changes, the figure no longer describes the kernel and is dropped.
+#   workload -> kernel -> (bytes per unit, unit, sources, digest, capture)
+TRAFFIC = {}
+
+KERNEL_SOURCES = {
+    "lm_head": ["lmhead_tc.cu", "common.cuh", "sm100.cuh"],
+    "attention": ["attention_mma.cu", "common.cuh", "sm100.cuh", "mma_sync.cuh"],
+}
+
+
+def source_digest(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "mtp_speculative_decoding_verify_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(workload, kernel, units):
+    """(DRAM bytes of one launch, note) or (None, why not)."""
+    e = TRAFFIC.get(workload, {}).get(kernel)
+    if e is None:
+        return None, "no capture for this workload"
+    per_unit, unit, files, digest, capture = e
+    if source_digest(files) != digest:
+        return None, "kernel source changed since the capture (%s)" % capture
+    return per_unit * units, "%s, scaled by %s" % (capture, unit)
 
 
 def elem_bytes(w):
@@ -248,11 +283,26 @@ class Step:
         self.launches = n
 
     def host_inputs(self):
-        """Device tensors that carry a step's inputs (copied from host memory in the e2e timing)."""
+        """Device tensors that carry a step's inputs (copied from host memory in
+        the e2e timing): the verify rows' queries, keys and values, the context
+        lengths, the hidden states, tokens, modes and temperatures, the tree
+        parents, and the draft distributions q of the rejection-sampling
+        requests (the rows of other requests are never read: only those
+        requests' slice is copied when they are contiguous)."""
         d = {"q": self.att["q"], "k_new": self.att["k_new"], "ctx_lens": self.att["ctx_lens"],
-             "hidden": self.lm["hidden"], "tokens": self.lm["tokens"]}
+             "hidden": self.lm["hidden"], "tokens": self.lm["tokens"], "mode": self.lm["mode"],
+             "temperature": self.lm["temperature"]}
+        if self.att["v_new"] is not None:
+            d["v_new"] = self.att["v_new"]
         if self.parents is not None:
             d["parents"] = self.parents
+        q = self.lm["q_draft"]
+        if q is not None:
+            samp = np.nonzero(self.lm["mode"].cpu().numpy() == 1)[0]
+            if len(samp) and samp[-1] - samp[0] + 1 == len(samp):
+                d["q_draft"] = q[int(samp[0]):int(samp[-1]) + 1]
+            elif len(samp):
+                d["q_draft"] = q
         return d
 
     def results(self):
@@ -395,6 +445,7 @@ def run_gpu(args, w, rank, world, dev):
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn) if not is_draft(args.workload) else 0.0
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_lm)
     n_acc, ctx, emitted = step.summary()
+    ties = step.ties.cpu().numpy() if hasattr(step, "ties") else np.zeros(0, np.uint8)
 
     # End to end through the public API with host buffers: each step copies its
     # inputs from pinned host memory, runs the calls and reads the results back.
@@ -444,7 +495,7 @@ def run_gpu(args, w, rank, world, dev):
     ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, emitted, world, dev)
     ms_eager, _, _ = combine_ranks(ms_eager, 0.0, 0.0, world, dev)
     return dict(ms=ms, ms_eager=ms_eager, graph=graph_ms is not None, e2e_graph=g_e2e is not None, e2e_ms=e2e_ms, attn_ms=attn_ms, lm_ms=lm_ms, emitted=emitted, n_acc=n_acc, ctx=ctx,
-                clocks=clocks, launches=launches, h2d=h2d, d2h=d2h)
+                clocks=clocks, launches=launches, h2d=h2d, d2h=d2h, ties=ties)
 
 
 def decode_baseline(args, w, dev):
@@ -475,6 +526,49 @@ def decode_baseline(args, w, dev):
     torch.cuda.synchronize()
     step.B.sync_status()
     return t0.elapsed_time(t1) / args.steps
+
+
+def read_ceiling(dev, gib=4, reps=5):
+    """Read-only bandwidth of this GPU (GB/s): the library's read probe
+    streaming a buffer far larger than L2, timed with CUDA events, best over
+    launch shapes and repetitions."""
+    from mtp_speculative_decoding_verify_gb300 import _binding as B
+    buf = torch.empty(gib << 30, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    best = 0.0
+    for ctas in (1, 2, 4):
+        for k in range(3 + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            B.hbm_read_probe(buf, sink, ctas, stream)
+            b.record(stream)
+            b.synchronize()
+            if k >= 3:
+                best = max(best, buf.numel() / (a.elapsed_time(b) * 1e-3) / 1e9)
+    B.sync_status()
+    del buf
+    return best
+
+
+def cpu_model():
+    """Host CPU model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def _timed_requests(fn, n_items, seconds, threads):
@@ -525,7 +619,7 @@ def cpu_baseline(w, seconds, dev=None, draft=False):
     n1, el1 = _timed_requests(fn, 4 * w.B, seconds, 1)
     cores = os.cpu_count() or 1
     nc, elc = _timed_requests(fn, 4 * w.B, seconds, cores)
-    return dict(value=nc / elc, unit="requests/s", cores=cores, kind="oracle",
+    return dict(value=nc / elc, unit="requests/s", cores=cores, cpu_model=cpu_model(), kind="oracle",
                 sample="%d request(s) of the %d-request batch (%s), the single-threaded oracle on %d threads, one "
                        "request per thread at a time, %.1f s" % (nc, w.B, what, cores, elc),
                 single_thread=dict(value=n1 / el1, unit="requests/s", cores=1,
@@ -576,13 +670,13 @@ def run_reference(args, w, rank, world):
               n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=el * 1e3 / args.steps,
               higher_is_better=True, scaling="weak", vs_baseline=None, dtype=w.dtype, data="synthetic",
               config=config_of(w, args),
-              cpu_baseline=dict(value=rps, unit="requests/s", cores=cores, kind="oracle", sample=sample),
+              cpu_baseline=dict(value=rps, unit="requests/s", cores=cores, cpu_model=cpu_model(), kind="oracle",
+                                sample=sample),
               e2e=dict(value=rps, unit="requests/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
 def config_of(w, args):
     return {"workload": w.name, "B": w.B, "D": w.D, "parallelism": "request-sharded replicas",
-            "cuda_graph": not getattr(args, "no_graph", False) and getattr(args, "impl", "gb300") == "gb300",
             "l2": "inputs larger than L2 (LM-head weights %.2f GB streamed every step)" % (w.V * w.H * elem_bytes(w) / 1e9)}
 
 
@@ -591,7 +685,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="cfg1_D3", choices=sorted(workloads()))
+    ap.add_argument("--workload", default="cfg3", choices=sorted(workloads()))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -626,25 +720,49 @@ def main():
     alg = algorithmic(w, r["ctx"], draft)
     hbm = float(peaks["hbm_gbs"])
     tc_peak = float(peaks["bf16_tflops"])
-    # Dominant kernel: the LM head (HBM-bound on W below M ~ 290 rows, tensor-bound above).
-    ridge = tc_peak * 1e12 / (hbm * 1e9)
-    lm_intensity = alg["lm_flops"] / alg["w_bytes"]
+    ceiling = read_ceiling(dev)
     calls = alg["calls"]   # LM-head launches per step; the events time one of them
-    if lm_intensity < ridge or w.dtype == "f32":
-        roof = dict(kernel="lm_head", bound="hbm", achieved=alg["w_bytes"] / calls / (r["lm_ms"] * 1e-3) / 1e9,
-                    peak=hbm, unit="GB/s", peak_source=src + " (hbm_gbs)")
+
+    def hbm_roof(kernel, nbytes, ms, units, unit_name):
+        a = nbytes / (ms * 1e-3) / 1e9
+        t, note = traffic_of(args.workload, kernel, units)
+        return dict(kernel=kernel, bound="hbm", achieved=a, peak=hbm, unit="GB/s", frac=a / hbm,
+                    peak_source=src + " (hbm_gbs: device-to-device copy)",
+                    read_ceiling=ceiling, frac_of_read_ceiling=a / ceiling,
+                    frac_of_nominal=a / HBM_NOMINAL_GBS, algorithmic_bytes=nbytes,
+                    unit_of_work=unit_name, traffic=t, traffic_note=note, avg_launch_ms=ms)
+
+    def tc_roof(kernel, flops, ms, units, unit_name):
+        a = flops / (ms * 1e-3) / 1e12
+        t, note = traffic_of(args.workload, kernel, units)
+        return dict(kernel=kernel, bound="tensor", achieved=a, peak=tc_peak, unit="TFLOP/s", frac=a / tc_peak,
+                    peak_source=src + " (bf16_tflops burst)", algorithmic_flops=flops, unit_of_work=unit_name,
+                    traffic=t, traffic_note=note, avg_launch_ms=ms)
+
+    # LM head: HBM-bound on W below M ~ 290 rows, tensor-bound above.
+    ridge = tc_peak * 1e12 / (hbm * 1e9)
+    w_call = alg["w_bytes"] / calls
+    if alg["lm_flops"] / alg["w_bytes"] < ridge or w.dtype == "f32":
+        lm_roof = hbm_roof("lm_head", w_call, r["lm_ms"], w.V, "vocabulary rows (W bytes V*H*2 per launch)")
     else:
-        roof = dict(kernel="lm_head", bound="tensor",
-                    achieved=alg["lm_flops"] / calls / (r["lm_ms"] * 1e-3) / 1e12,
-                    peak=tc_peak, unit="TFLOP/s", peak_source=src + " (bf16_tflops burst)")
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    per_row = LMHEAD_TRAFFIC_PER_VOCAB_ROW.get(args.workload)
-    roof["traffic"] = per_row * w.V if per_row and not draft else None
-    roof["traffic_note"] = ("ncu capture of the same kernel at vocab 32768, scaled to the full vocabulary"
-                            if per_row else "no capture for this workload")
-    roof["avg_launch_ms"] = r["lm_ms"]
+        lm_roof = tc_roof("lm_head", alg["lm_flops"] / calls, r["lm_ms"], w.V,
+                          "vocabulary rows (2*M*H flop each)")
+    roofs = {"lm_head": lm_roof}
+    if not draft:
+        if w.is_mla:
+            roofs["attention"] = tc_roof("attention", alg["attn_flops"], r["attn_ms"], alg["kv_bytes"],
+                                         "(row, visible key) pairs (2*(d_qk+d_v)*Hq flop each)")
+        else:
+            roofs["attention"] = hbm_roof("attention", alg["kv_bytes"], r["attn_ms"], alg["kv_bytes"],
+                                          "KV-cache bytes ((ctx+R)*Hkv*(d_qk+d_v)*2 per request)")
+    dominant = max(roofs, key=lambda k: roofs[k]["avg_launch_ms"])
+    roof = roofs[dominant]
     step_bound_s = max((alg["kv_bytes"] + alg["w_bytes"]) / (hbm * 1e9),
                        (alg["lm_flops"] + alg["attn_flops"]) / (tc_peak * 1e12))
+    per_kernel_s = (alg["kv_bytes"] / (hbm * 1e9) if not w.is_mla else alg["attn_flops"] / (tc_peak * 1e12)) + \
+        (lm_roof["algorithmic_bytes"] / (hbm * 1e9) if lm_roof["bound"] == "hbm"
+         else lm_roof["algorithmic_flops"] / (tc_peak * 1e12)) * calls
+    ties = r["ties"]
     value = world * w.B / (r["ms"] * 1e-3)
     if draft:
         kernels = dict(lm_head_ms_per_call=r["lm_ms"], calls_per_step=calls)
@@ -656,10 +774,18 @@ def main():
                 data="synthetic (seeded; random-init weights of the named shapes)", config=config_of(w, args),
                 accepted_tokens_per_s=r["emitted"] / (r["ms"] * 1e-3),
                 mean_drafts_accepted=float(np.mean(r["n_acc"])),
+                cuda_graph=r["graph"],
                 roofline=roof,
+                roofline_kernels=roofs,
                 step_roofline=dict(bound_ms=step_bound_s * 1e3, frac=step_bound_s * 1e3 / r["ms"],
+                                   sum_of_kernel_bounds_ms=per_kernel_s * 1e3,
+                                   frac_of_sum_of_kernel_bounds=per_kernel_s * 1e3 / r["ms"],
                                    kv_gb=alg["kv_bytes"] / 1e9, w_gb=alg["w_bytes"] / 1e9,
                                    gflop=(alg["lm_flops"] + alg["attn_flops"]) / 1e9),
+                near_ties=dict(requests=int(len(ties)), accept_or_relaxed_band=int(((ties & 1) != 0).sum()),
+                               race=int(((ties & 2) != 0).sum()),
+                               note="requests whose decision the tie flags mark as within the near-tie band "
+                                    "(bit-exact comparison with the oracle excludes them)"),
                 kernels=kernels,
                 e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
                          d2h_bytes_per_step=r["d2h"], ms_per_step=r["e2e_ms"],

@@ -398,6 +398,19 @@ int mtp_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t 
                   uint32_t* word0, float* race_e, float* accept_u, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Read-bandwidth probe (measurement aid, not on the verify path; the pages
+ * have no counterpart).
+ *
+ * Reads `bytes` of device memory at `buf` once, with 16-byte streaming loads
+ * from sm_count * ctas_per_sm CTAs, and XORs every 32-bit word into *sink
+ * (device, 4 bytes; its final value has no meaning beyond keeping the loads
+ * live). Timed with events around it, it gives the read-only bandwidth that
+ * bounds the step's read streams (KV cache, LM-head weights). buf and bytes
+ * must be multiples of 16 bytes; ctas_per_sm in [1, 4]; MTP_INVALID_ARG
+ * otherwise. Asynchronous on `stream`; bytes = 0 is a no-op. */
+int mtp_hbm_read_probe(const void* buf, size_t bytes, uint32_t* sink, int32_t ctas_per_sm, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status and introspection. */
 
 /* Message for the last failing call on this thread ("" if none). */

@@ -97,3 +97,30 @@ def test_tree_path_lengths():
     assert list(pl[0]) == [1, 2, 2, 2, 3, 3, 3, 3, 3, 3, 4, 4, 4, 4, 4, 4]
     v = bench.workloads()["cfg1_D3"]
     assert (bench.path_lengths(v) == [1, 2, 3, 4]).all()
+
+
+def test_traffic_scaled_and_dropped_when_the_kernel_changes():
+    sys.path.insert(0, ROOT)
+    import bench
+    files = bench.KERNEL_SOURCES["lm_head"]
+    good = bench.source_digest(files)
+    saved = dict(bench.TRAFFIC)
+    try:
+        bench.TRAFFIC["w"] = {"lm_head": (10.0, "vocabulary rows", files, good, "capture X")}
+        t, note = bench.traffic_of("w", "lm_head", 3)
+        assert t == 30.0 and "capture X" in note
+        bench.TRAFFIC["w"] = {"lm_head": (10.0, "vocabulary rows", files, "0" * 16, "capture X")}
+        t, note = bench.traffic_of("w", "lm_head", 3)
+        assert t is None and "changed" in note
+        assert bench.traffic_of("w", "attention", 3)[0] is None
+    finally:
+        bench.TRAFFIC.clear()
+        bench.TRAFFIC.update(saved)
+
+
+def test_workload_config_names_no_run_options():
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+    cfg = bench.config_of(bench.workloads()["cfg3"], argparse.Namespace(no_graph=False, impl="gb300"))
+    assert "cuda_graph" not in cfg and cfg["B"] == 256 and cfg["D"] == 3
