@@ -38,9 +38,10 @@ SMALL = {
     "cfg3_small_mixed": synth.CFG3.with_(name="GQA bf16 mixed small", B=8, Hq=8, Hkv=2, ctx=(64, 700), H=256,
                                          V=7001),
     "mha_bf16_d64": synth.CFG0.with_(name="MHA bf16 d64", dtype="bf16", ctx=(0, 200), B=5, H=128, V=999),
-    # MLA with 4 and 3 row blocks per request: clusters sharing KV tiles by multicast
+    # MLA with 4, 3 and 1 row blocks per request: CTA pairs, and single CTAs for odd counts
     "mla_cluster4": synth.CFG1.with_(name="MLA 4 row blocks", B=3, Hq=64, ctx=(60, 700), H=256, V=2000),
     "mla_cluster3": synth.CFG1.with_(name="MLA 3 row blocks", B=2, Hq=48, ctx=(130, 400), H=128, V=777),
+    "mla_single_row_block": synth.CFG1.with_(name="MLA 1 row block", B=3, Hq=16, ctx=(100, 900), H=128, V=777),
     # LM head on CTA pairs (M >= 193 rows): ragged row group (M=200 -> N=224) and vocabulary tail
     "lm_pair_ragged_sampling": synth.CFG2.with_(name="LM head pairs, sampling", B=50, D=3, Hq=8, Hkv=2,
                                                 ctx=(40, 90), H=256, V=5003),
@@ -171,6 +172,17 @@ def test_full_size_sampled_requests(name):
     flagged = _full_check_lm(w, lm, gpu, reqs)
     assert flagged <= 1
     check_invariants(w, lm, gpu)
+    # The same call with the debug logits: identical results, and the sampled
+    # rows' logits within the bf16 bound of the oracle's.
+    dbg = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    for k in ("out_tokens", "num_accepted", "tie_flags", "lse", "argmax"):
+        assert torch.equal(gpu[k], dbg[k]), k
+    _full_check_lm(w, lm, dbg, reqs, logits=True)
+    ties = gpu["tie_flags"].cpu().numpy()
+    print("%s: near-ties flagged by the GPU: accept/relaxed band %d, race %d of %d requests" %
+          (name, int(((ties & 1) != 0).sum()), int(((ties & 2) != 0).sum()), w.B))
+    del dbg
     if w.sampling == "none" or w.sampling == "half":
         # Planted targets: greedy rows' argmax is the planted token.
         greedy = [b for b in range(w.B) if int(lm["mode"][b]) == 0]
@@ -307,12 +319,14 @@ def test_rollback_many_requests_and_capacity():
     # is left half rolled back: the requests before the first one whose blocks
     # do not fit are rolled back (as the oracle does them), later requests that
     # free nothing get their new length, and the others are left untouched.
-    for cap in (10, 11, 257):
+    cnt = np.maximum((ctx + w.D) // 64 - (ctx + n + 1 + 63) // 64 + 1, 0)
+    total = int(cnt.sum())
+    assert total > 12
+    for cap in (10, 11, total - 1):
         g_table, g_seq, g_fl, g_fc = gpu_rollback(w, t_d, c_d, n_d, capacity=cap)
         with pytest.raises(mv.MtpError) as ei:
             mv.sync_status()
         assert ei.value.code == 4
-        cnt = np.maximum((ctx + w.D) // 64 - (ctx + n + 1 + 63) // 64 + 1, 0)
         f = int(np.argmax(np.cumsum(cnt) > cap))
         t_h, s_h = table.copy(), ctx.copy()
         fl = np.full(int(cnt[:f].sum()), -1, np.int32)

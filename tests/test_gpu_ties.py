@@ -1,0 +1,149 @@
+"""GPU tie rules against the oracle, on exactly equal values planted where the
+kernels split the work.
+
+"MTP in TensorRT-LLM on Blackwell", Fig. 1: each draft is compared with the
+target's own prediction, the argmax of its row. Equal logits are resolved
+to the lowest token id; the library splits the vocabulary over 128-row tiles
+and CTAs (and the exponential race over vocabulary slices), so the rule has
+to hold across those splits:
+
+  * argmax: one W row copied to token ids 5, V/2 + 1 and V - 3 (different
+    tiles and CTAs) gives those three exactly equal logits; rows planted on
+    that direction must report argmax 5 on the single-CTA and CTA-pair
+    tensor-core LM heads and on the fp32 SIMT one, and drafts of V - 3 must be
+    rejected with 5 as the correction;
+  * relaxed acceptance: the draft's rank counts equal logits of lower ids
+    before it, so the same duplicates decide top-N membership;
+  * the race: two vocabulary ids whose Philox words are equal get equal
+    exponentials; with equal weights their keys are equal and the draw must
+    be the lower id (and be flagged as a near-tie on both sides).
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU hosts too; the marker keeps them out of -m "not gpu"
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import mtp_speculative_decoding_verify_gb300 as mv  # noqa: E402
+from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
+from gpu_util import gpu_lmhead, oracle_lmhead  # noqa: E402
+from philox_py import philox_vec  # noqa: E402
+
+DEV = torch.device("cuda:0")
+TAG_BONUS = 3
+
+
+def _plant_duplicates(lm, ids, scale, rows):
+    """W[ids] := one unit vector u (norm 1, far above the other rows' ~0.02*sqrt(H));
+    hidden rows `rows` := scale * u, so those rows' largest logits are the
+    duplicates', exactly equal on both sides."""
+    W = lm["lm_head"]
+    H = W.shape[1]
+    g = torch.Generator(device="cpu").manual_seed(123)
+    u = torch.randn(H, generator=g, dtype=torch.float64)
+    u = (u / u.norm()).to(W.dtype).to(W.device)
+    for v in ids:
+        W[v] = u
+    for m in rows:
+        lm["hidden"][m] = (scale * u.double()).to(W.dtype)
+
+
+LM_CASES = {
+    "tc_single_cta": dict(dtype="bf16", B=4, D=3, H=128),      # M = 16: single-CTA tensor-core LM head
+    "tc_cta_pairs": dict(dtype="bf16", B=50, D=3, H=128),      # M = 200: CTA pairs
+    "tc_two_row_groups": dict(dtype="bf16", B=100, D=3, H=64),  # M = 400: two row groups on CTA pairs
+    "simt_fp32": dict(dtype="f32", B=4, D=3, H=64),            # fp32 SIMT LM head
+}
+
+
+@pytest.mark.parametrize("name", list(LM_CASES))
+def test_argmax_ties_lowest_id_across_tiles_and_ctas(name):
+    c = LM_CASES[name]
+    V = 5003
+    w = synth.CFG0.with_(name="argmax ties " + name, V=V, sampling="none", **c)
+    lm = synth.make_lmhead_inputs(w, DEV)
+    dup = [5, V // 2 + 1, V - 3]
+    planted_rows = [b * w.R + j for b in range(w.B) for j in range(0, w.R, 2)]
+    _plant_duplicates(lm, dup, 20.0, planted_rows)
+    tok = lm["tokens"]
+    for b in range(w.B):
+        for j in range(0, w.D, 2):
+            tok[b, j + 1] = 5 if b % 2 == 0 else V - 3
+    gpu = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    logits = gpu["logits"].cpu().numpy()
+    for m in planted_rows:   # the premise: bitwise equal logits at the duplicates
+        assert logits[m, dup[0]] == logits[m, dup[1]] == logits[m, dup[2]], m
+        assert logits[m, dup[0]] == logits[m].max()
+    amax = gpu["argmax"].cpu().numpy().reshape(-1)
+    assert (amax[planted_rows] == 5).all()
+    ref = oracle_lmhead(w, lm, range(w.B))
+    assert (gpu["argmax"].cpu().numpy() == ref["argmax"]).all()
+    assert (gpu["out_tokens"].cpu().numpy() == ref["out_tokens"]).all()
+    assert (gpu["num_accepted"].cpu().numpy() == ref["num_accepted"]).all()
+    n = gpu["num_accepted"].cpu().numpy()
+    out = gpu["out_tokens"].cpu().numpy()
+    for b in range(1, w.B, 2):   # a draft of V - 3 at row 0 is rejected, corrected to 5
+        assert n[b] == 0 and out[b, 0] == 5
+
+
+@pytest.mark.parametrize("topk", [1, 2, 3])
+def test_relaxed_rank_counts_equal_logits_of_lower_ids_first(topk):
+    V = 5003
+    w = synth.CFG0.with_(name="relaxed ties", V=V, dtype="bf16", B=6, D=1, H=128, sampling="none")
+    lm = synth.make_lmhead_inputs(w, DEV)
+    dup = [5, V // 2 + 1, V - 3]
+    _plant_duplicates(lm, dup, 20.0, [b * w.R for b in range(w.B)])
+    for b in range(w.B):
+        lm["tokens"][b, 1] = dup[b % 3]      # ranks 0, 1, 2 among the tied top logits
+    lm["mode"].fill_(2)
+    lm = dict(lm, relaxed_topk=topk, relaxed_delta=1.0)
+    gpu = gpu_lmhead(w, lm)
+    mv.sync_status()
+    ref = oracle_lmhead(w, lm, range(w.B))
+    n = gpu["num_accepted"].cpu().numpy()
+    assert (n == ref["num_accepted"]).all() and (gpu["out_tokens"].cpu().numpy() == ref["out_tokens"]).all()
+    assert (gpu["tie_flags"].cpu().numpy() == ref["tie_flags"]).all()
+    assert list(n) == [int(b % 3 < topk) for b in range(w.B)]
+
+
+def _philox_collision(V, b, j, tag, seeds):
+    """First (seed, v1, v2) with v1 < v2 whose race counters give the same Philox word."""
+    v = np.arange(V, dtype=np.uint64)
+    for seed in seeds:
+        x = philox_vec(np.full(V, b), np.full(V, j), v, np.full(V, tag), seed & 0xFFFFFFFF, seed >> 32)[0]
+        order = np.argsort(x, kind="stable")
+        xs = x[order]
+        hit = np.nonzero(xs[1:] == xs[:-1])[0]
+        if len(hit):
+            v1, v2 = sorted((int(order[hit[0]]), int(order[hit[0] + 1])))
+            return seed, v1, v2
+    return None
+
+
+def test_race_equal_keys_draw_the_lower_id():
+    """Bonus draw (every draft accepted) over p_D, whose mass sits on two ids
+    v1 < v2 with equal logits and equal Philox words: equal race keys."""
+    V, D = 65536 + 37, 1
+    found = _philox_collision(V, 0, D, TAG_BONUS, range(1, 200))
+    assert found is not None
+    seed, v1, v2 = found
+    w = synth.CFG0.with_(name="race ties", V=V, dtype="bf16", B=2, D=D, H=64, sampling="all")
+    lm = synth.make_lmhead_inputs(w, DEV)
+    _plant_duplicates(lm, [v1, v2], 50.0, [0, 1])   # request 0: both rows on the tied pair
+    lm["tokens"][0, 1] = v1
+    q = lm["q_draft"]
+    q[0].fill_(1.0 / V)
+    q[0, 0, v1] = 1e-6                                # p(v1) ~ 0.5 >= U q: the draft is accepted
+    lm = dict(lm, seed=seed)
+    gpu = gpu_lmhead(w, lm, debug_logits=True)
+    mv.sync_status()
+    lg = gpu["logits"].cpu().numpy()
+    assert lg[1, v1] == lg[1, v2] == lg[1].max()
+    ref = oracle_lmhead(w, lm, [0])
+    assert int(gpu["num_accepted"][0]) == int(ref["num_accepted"][0]) == 1
+    assert int(gpu["out_tokens"][0, 1]) == int(ref["out_tokens"][0, 1]) == v1
+    assert int(gpu["tie_flags"][0]) & 2 and int(ref["tie_flags"][0]) & 2
