@@ -111,12 +111,25 @@ def load_peaks():
 # source files and their SHA-256 (first 16 hex digits) at capture time; once
 # a source changes, the figure no longer describes the kernel and is dropped.
 #   workload -> kernel -> (bytes per unit, unit, sources, digest, capture)
-TRAFFIC = {}
-
 KERNEL_SOURCES = {
     "lm_head": ["lmhead_tc.cu", "common.cuh", "sm100.cuh"],
     "attention": ["attention_mma.cu", "common.cuh", "sm100.cuh", "mma_sync.cuh"],
 }
+
+TRAFFIC = {
+    "cfg3": {
+        # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.25 MB read + 4.60 MB
+        # written for 987.60 MB of KV cache
+        "attention": (994850560 / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"], "79232e59d56890e8",
+                      "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
+        # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 840.68 MB read
+        # + 101.20 MB written
+        "lm_head": ((840.679424e6 + 101.199616e6) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "292d26cf5444f530", "ncu capture of lmhead_tc_kernel at M=1024, vocabulary 65536 "
+                                        "(profile_lm_cfg3_V64k)"),
+    },
+}
+
 
 
 def source_digest(files):

@@ -116,7 +116,8 @@ def compare_accept(gpu, ref, reqs):
 
 
 def check_invariants(w, lm, gpu):
-    """Properties that hold for every request at any size."""
+    """Properties that hold for every request at any size (chains; for tree
+    drafts the emitted prefix is the accepted path's drafts)."""
     tok = lm["tokens"].cpu().numpy()
     out = gpu["out_tokens"].cpu().numpy()
     n = gpu["num_accepted"].cpu().numpy()
@@ -124,6 +125,18 @@ def check_invariants(w, lm, gpu):
     mode = lm["mode"].cpu().numpy()
     temp = lm["temperature"].cpu().numpy()
     assert ((n >= 0) & (n <= w.D)).all()
+    if lm.get("parents") is not None:
+        nodes = gpu["accepted_nodes"].cpu().numpy()
+        par = lm["parents"].cpu().numpy()
+        for b in range(w.B):
+            k = int(n[b])
+            path = nodes[b, :k + 1]
+            assert path[0] == 0 and (nodes[b, k + 1:] == -1).all()
+            assert all(par[b, path[i + 1]] == path[i] for i in range(k))
+            assert (out[b, :k] == tok[b, path[1:]]).all() and (out[b, k + 1:] == -1).all()
+            assert all(amax[b, path[i]] == tok[b, path[i + 1]] for i in range(k))   # greedy per edge
+            assert out[b, k] == amax[b, path[k]]
+        return
     for b in range(w.B):
         k = int(n[b])
         assert (out[b, :k] == tok[b, 1:k + 1]).all()

@@ -12,8 +12,10 @@ to hold across those splits:
     that direction must report argmax 5 on the single-CTA and CTA-pair
     tensor-core LM heads and on the fp32 SIMT one, and drafts of V - 3 must be
     rejected with 5 as the correction;
-  * relaxed acceptance: the draft's rank counts equal logits of lower ids
-    before it, so the same duplicates decide top-N membership;
+  * relaxed acceptance: tokens tied above the draft count before it and a
+    rejection is corrected to the lowest-id argmax; a draft exactly tied
+    with others is a near-tie (flagged on both sides), since the library
+    takes the draft's own logit from a pre-pass;
   * the race: two vocabulary ids whose Philox words are equal get equal
     exponentials; with equal weights their keys are equal and the draw must
     be the lower id (and be flagged as a near-tie on both sides).
@@ -91,23 +93,62 @@ def test_argmax_ties_lowest_id_across_tiles_and_ctas(name):
 
 
 @pytest.mark.parametrize("topk", [1, 2, 3])
-def test_relaxed_rank_counts_equal_logits_of_lower_ids_first(topk):
+def test_relaxed_exact_tie_at_the_draft_is_a_near_tie(topk):
+    """Draft logit exactly equal to two other tokens' (the lowest-id rule
+    decides its rank). The library computes the draft's logit in a pre-pass
+    with its own summation order, so where the tied group straddles the top-N
+    boundary the decision is a near-tie by construction and both sides flag
+    it; the outcome must still be valid, and a rejection is corrected to the
+    lowest-id argmax. With N = 3 every tied token is inside: no flag, and the
+    GPU equals the oracle."""
     V = 5003
     w = synth.CFG0.with_(name="relaxed ties", V=V, dtype="bf16", B=6, D=1, H=128, sampling="none")
     lm = synth.make_lmhead_inputs(w, DEV)
     dup = [5, V // 2 + 1, V - 3]
     _plant_duplicates(lm, dup, 20.0, [b * w.R for b in range(w.B)])
     for b in range(w.B):
-        lm["tokens"][b, 1] = dup[b % 3]      # ranks 0, 1, 2 among the tied top logits
+        lm["tokens"][b, 1] = dup[b % 3]
     lm["mode"].fill_(2)
     lm = dict(lm, relaxed_topk=topk, relaxed_delta=1.0)
     gpu = gpu_lmhead(w, lm)
     mv.sync_status()
     ref = oracle_lmhead(w, lm, range(w.B))
+    g_tie = gpu["tie_flags"].cpu().numpy()
     n = gpu["num_accepted"].cpu().numpy()
-    assert (n == ref["num_accepted"]).all() and (gpu["out_tokens"].cpu().numpy() == ref["out_tokens"]).all()
-    assert (gpu["tie_flags"].cpu().numpy() == ref["tie_flags"]).all()
-    assert list(n) == [int(b % 3 < topk) for b in range(w.B)]
+    out = gpu["out_tokens"].cpu().numpy()
+    assert (g_tie == ref["tie_flags"]).all()
+    if topk < len(dup):   # the tied group straddles the top-N boundary: flagged
+        assert (g_tie & 1).all()
+        for b in range(w.B):
+            assert out[b, 0] == (dup[b % 3] if n[b] == 1 else 5)
+    else:                 # every tied token is inside the top N: a sure accept
+        assert (g_tie == 0).all() and (n == 1).all() and (n == ref["num_accepted"]).all()
+        assert (out == ref["out_tokens"]).all()
+
+
+@pytest.mark.parametrize("topk,accepted", [(2, 0), (3, 1)])
+def test_relaxed_rank_past_tied_top_tokens(topk, accepted):
+    """Two tokens tie at the top (ids 5 and V - 3), the draft ranks third with
+    a clear margin: accepted for top-3, rejected for top-2 and corrected to
+    the lowest-id argmax, 5; no near-tie, so the GPU must equal the oracle."""
+    V = 5003
+    w = synth.CFG0.with_(name="relaxed, tied top", V=V, dtype="bf16", B=4, D=1, H=128, sampling="none")
+    lm = synth.make_lmhead_inputs(w, DEV)
+    _plant_duplicates(lm, [5, V - 3], 20.0, [b * w.R for b in range(w.B)])
+    c = 100
+    lm["lm_head"][c] = (0.95 * lm["lm_head"][5].double()).to(lm["lm_head"].dtype)   # logit ~19: third
+    lm["tokens"][:, 1] = c
+    lm["mode"].fill_(2)
+    lm = dict(lm, relaxed_topk=topk, relaxed_delta=1.0)
+    gpu = gpu_lmhead(w, lm)
+    mv.sync_status()
+    ref = oracle_lmhead(w, lm, range(w.B))
+    assert (gpu["tie_flags"].cpu().numpy() == 0).all() and (ref["tie_flags"] == 0).all()
+    assert (gpu["num_accepted"].cpu().numpy() == ref["num_accepted"]).all()
+    assert (gpu["out_tokens"].cpu().numpy() == ref["out_tokens"]).all()
+    assert (gpu["num_accepted"].cpu().numpy() == accepted).all()
+    if not accepted:
+        assert (gpu["out_tokens"].cpu().numpy()[:, 0] == 5).all()
 
 
 def _philox_collision(V, b, j, tag, seeds):
