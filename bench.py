@@ -543,26 +543,28 @@ def decode_baseline(args, w, dev):
 
 def read_ceiling(dev, gib=4, reps=5):
     """Read-only bandwidth of this GPU (GB/s): the library's read probe
-    streaming a buffer far larger than L2, timed with CUDA events, best over
-    launch shapes and repetitions."""
+    streaming a buffer far larger than L2, by loads and by bulk copies, timed
+    with CUDA events; the best over paths, launch shapes and repetitions, and
+    the best of each path."""
     from mtp_speculative_decoding_verify_gb300 import _binding as B
     buf = torch.empty(gib << 30, dtype=torch.uint8, device=dev)
     buf.fill_(1)
     sink = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    best = 0.0
-    for ctas in (1, 2, 4):
+    best = {}
+    for bulk, ctas in ((False, 1), (False, 2), (False, 4), (True, 1)):
+        key = "bulk_copies" if bulk else "loads"
         for k in range(3 + reps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            B.hbm_read_probe(buf, sink, ctas, stream)
+            B.hbm_read_probe(buf, sink, ctas, bulk, stream)
             b.record(stream)
             b.synchronize()
             if k >= 3:
-                best = max(best, buf.numel() / (a.elapsed_time(b) * 1e-3) / 1e9)
+                best[key] = max(best.get(key, 0.0), buf.numel() / (a.elapsed_time(b) * 1e-3) / 1e9)
     B.sync_status()
     del buf
-    return best
+    return max(best.values()), best
 
 
 def cpu_model():
@@ -733,7 +735,7 @@ def main():
     alg = algorithmic(w, r["ctx"], draft)
     hbm = float(peaks["hbm_gbs"])
     tc_peak = float(peaks["bf16_tflops"])
-    ceiling = read_ceiling(dev)
+    ceiling, ceiling_by_path = read_ceiling(dev)
     calls = alg["calls"]   # LM-head launches per step; the events time one of them
 
     def hbm_roof(kernel, nbytes, ms, units, unit_name):
@@ -741,7 +743,7 @@ def main():
         t, note = traffic_of(args.workload, kernel, units)
         return dict(kernel=kernel, bound="hbm", achieved=a, peak=hbm, unit="GB/s", frac=a / hbm,
                     peak_source=src + " (hbm_gbs: device-to-device copy)",
-                    read_ceiling=ceiling, frac_of_read_ceiling=a / ceiling,
+                    read_ceiling=ceiling, read_ceiling_by_path=ceiling_by_path, frac_of_read_ceiling=a / ceiling,
                     frac_of_nominal=a / HBM_NOMINAL_GBS, algorithmic_bytes=nbytes,
                     unit_of_work=unit_name, traffic=t, traffic_note=note, avg_launch_ms=ms)
 

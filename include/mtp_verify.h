@@ -401,14 +401,19 @@ int mtp_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t 
 /* Read-bandwidth probe (measurement aid, not on the verify path; the pages
  * have no counterpart).
  *
- * Reads `bytes` of device memory at `buf` once, with 16-byte streaming loads
- * from sm_count * ctas_per_sm CTAs, and XORs every 32-bit word into *sink
- * (device, 4 bytes; its final value has no meaning beyond keeping the loads
- * live). Timed with events around it, it gives the read-only bandwidth that
- * bounds the step's read streams (KV cache, LM-head weights). buf and bytes
- * must be multiples of 16 bytes; ctas_per_sm in [1, 4]; MTP_INVALID_ARG
+ * Reads `bytes` of device memory at `buf` once and XORs words of it into
+ * *sink (device, 4 bytes; its final value has no meaning beyond keeping the
+ * reads live). bulk = 0: 16-byte streaming loads from sm_count * ctas_per_sm
+ * CTAs, every word folded in; bulk = 1: bulk copies (the copy engine the
+ * verify kernels read through) of 32 KB chunks into a six-deep shared-memory
+ * ring, one CTA per SM (ctas_per_sm ignored); a copy that does not complete
+ * within 2 s sets MTP_ERR_TIMEOUT in the device error word. Timed with
+ * events around it, it gives the read-only bandwidth that bounds the step's
+ * read streams (KV cache, LM-head weights). buf and bytes must be multiples
+ * of 16 bytes, ctas_per_sm in [1, 4], bulk 0 or 1; MTP_INVALID_ARG
  * otherwise. Asynchronous on `stream`; bytes = 0 is a no-op. */
-int mtp_hbm_read_probe(const void* buf, size_t bytes, uint32_t* sink, int32_t ctas_per_sm, void* stream);
+int mtp_hbm_read_probe(const void* buf, size_t bytes, uint32_t* sink, int32_t ctas_per_sm, int32_t bulk,
+                       void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status and introspection. */

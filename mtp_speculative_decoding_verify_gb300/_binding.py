@@ -107,7 +107,7 @@ def lib():
         L.mtp_draft_argmax.restype = ctypes.c_int
         L.mtp_tree_kv_compact.argtypes = [ctypes.POINTER(KvCompactArgs), _P]
         L.mtp_tree_kv_compact.restype = ctypes.c_int
-        L.mtp_hbm_read_probe.argtypes = [_P, ctypes.c_size_t, _P, ctypes.c_int32, _P]
+        L.mtp_hbm_read_probe.argtypes = [_P, ctypes.c_size_t, _P, ctypes.c_int32, ctypes.c_int32, _P]
         L.mtp_hbm_read_probe.restype = ctypes.c_int
         L.mtp_abi_version.argtypes = []
         L.mtp_abi_version.restype = ctypes.c_int
@@ -389,8 +389,9 @@ def wait_selftest(timeout_ns, stream=None):
     _check(lib().mtp_wait_selftest(int(timeout_ns), _stream_handle(stream)))
 
 
-def hbm_read_probe(buf, sink, ctas_per_sm=2, stream=None):
-    """Stream the bytes of device tensor `buf` once (read-bandwidth probe);
-    `sink` is a 1-element int32 device tensor that receives their XOR."""
+def hbm_read_probe(buf, sink, ctas_per_sm=2, bulk=False, stream=None):
+    """Stream the bytes of device tensor `buf` once (read-bandwidth probe), by
+    16-byte loads or (bulk=True) bulk copies into shared memory; `sink` is a
+    1-element int32 device tensor that receives an XOR of the data."""
     _check(lib().mtp_hbm_read_probe(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), int(ctas_per_sm),
-                                    _stream_handle(stream)))
+                                    int(bool(bulk)), _stream_handle(stream)))

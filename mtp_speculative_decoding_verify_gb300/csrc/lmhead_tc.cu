@@ -395,23 +395,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             atomicAdd(&row_cnt[3 * rr + 1], c1);
             atomicAdd(&row_cnt[3 * rr + 2], c2);
           }
-          float* dst_s = (samp && p.samp_logits) ? p.samp_logits + (int64_t)m * p.V + vbase : nullptr;
-          float* dst_d = p.logits_debug ? p.logits_debug + (int64_t)m * p.V + vbase : nullptr;
-          if (dst_s || dst_d) {
-            if (nvalid == 32 && (p.V & 3) == 0) {
-#pragma unroll
-              for (int x = 0; x < 32; x += 4) {
-                const float4 v4 = make_float4(rowv[x], rowv[x + 1], rowv[x + 2], rowv[x + 3]);
-                // streaming stores: the rows are read once, later, by the race
-                // kernel; W tiles shared by the row groups stay in L2
-                if (dst_s) __stcs(reinterpret_cast<float4*>(dst_s + x), v4);
-                if (dst_d) *reinterpret_cast<float4*>(dst_d + x) = v4;
-              }
-            } else {
-              for (int x = 0; x < nvalid; ++x) {
-                if (dst_s) dst_s[x] = rowv[x];
-                if (dst_d) dst_d[x] = rowv[x];
-              }
+          if (!(nvalid == 32 && (p.V & 3) == 0)) {   // ragged vocabulary tail: this lane writes its row
+            float* dst_s = (samp && p.samp_logits) ? p.samp_logits + (int64_t)m * p.V + vbase : nullptr;
+            float* dst_d = p.logits_debug ? p.logits_debug + (int64_t)m * p.V + vbase : nullptr;
+            for (int x = 0; x < nvalid; ++x) {
+              if (dst_s) dst_s[x] = rowv[x];
+              if (dst_d) dst_d[x] = rowv[x];
+            }
+          }
+        }
+        // Whole 32-entry slices: the warp writes the chunk's rows from the
+        // transpose buffer, eight lanes per row, so every store instruction
+        // fills four whole 128-byte lines (a lane writing its own row would
+        // touch 32 lines per instruction, and that L1 traffic competes with
+        // the MMAs' operand reads for the same shared-memory bandwidth).
+        if (nvalid == 32 && (p.V & 3) == 0 &&
+            __any_sync(0xffffffffu, row0 + c * 32 + lane < p.M && (p.logits_debug || (p.samp_logits && row_samp[c * 32 + lane])))) {
+          __syncwarp();
+          const int x0 = 4 * (lane & 7);
+#pragma unroll 1
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const int m2 = row0 + c * 32 + r;
+            if (m2 < p.M) {
+              const float* src = tb + r * 33 + x0;
+              const float4 v4 = make_float4(src[0], src[1], src[2], src[3]);
+              const int64_t o = (int64_t)m2 * p.V + vbase + x0;
+              // streaming stores: the rows are read once, later, by the race
+              // kernel; W tiles shared by the row groups stay in L2
+              if (p.samp_logits && row_samp[c * 32 + r]) __stcs(reinterpret_cast<float4*>(p.samp_logits + o), v4);
+              if (p.logits_debug) *reinterpret_cast<float4*>(p.logits_debug + o) = v4;
             }
           }
         }
