@@ -391,7 +391,8 @@ int mtp_wait_selftest(uint64_t timeout_ns, void* stream);
  * For i in [0, n) with v = v0 + i, writes (device arrays of n entries, any
  * may be NULL):
  *   word0[i]    = output word 0 for key (seed lo, seed hi), counter (b, j, v, tag)
- *   race_e[i]   = the race exponential -log1p(-word0 * 2^-32) of that counter
+ *   race_e[i]   = the race exponential -log1p(-x * 2^-32) of vocabulary index
+ *                 v in row j, x = output word v % 4 of counter (b, j, v / 4, tag)
  *   accept_u[i] = the accept uniform of request b, row v (counter (b, v, 0, 1))
  * Returns MTP_INVALID_ARG if n < 0. */
 int mtp_rng_debug(uint64_t seed, uint32_t b, uint32_t j, uint32_t tag, uint32_t v0, int32_t n,

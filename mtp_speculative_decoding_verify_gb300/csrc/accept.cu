@@ -238,6 +238,18 @@ __global__ void __launch_bounds__(kThreads) accept_race_kernel(
     const float w = expf(l - lse) - q;
     if (w > 0.0f) race_add(resid, w / race_exponential(seed, (uint32_t)b, (uint32_t)n, (uint32_t)v, tag), v);
   };
+  // Entries 4g .. 4g+3 share one generator call (their race words are the
+  // four words of counter (b, n, g, tag)), made only if one of them has a
+  // positive weight.
+  auto visit4 = [&](const float4& l, const float4& q, int g) {
+    const float w[4] = {expf(l.x - lse) - q.x, expf(l.y - lse) - q.y, expf(l.z - lse) - q.z, expf(l.w - lse) - q.w};
+    if (!(w[0] > 0.0f || w[1] > 0.0f || w[2] > 0.0f || w[3] > 0.0f)) return;
+    const uint4 x = philox4(seed, (uint32_t)b, (uint32_t)n, (uint32_t)g, tag);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (w[k] > 0.0f) race_add(resid, w[k] / race_variate(xs[k]), 4 * g + k);
+  };
   if ((V & 3) == 0) {
     // Rows start 16-byte aligned: each thread takes 4 consecutive entries per
     // step (ascending within the thread, as race_add expects) and keeps two
@@ -250,16 +262,8 @@ __global__ void __launch_bounds__(kThreads) accept_race_kernel(
       const bool two = g2 < v1 / 4;
       const float4 la = __ldg(l4 + g), qa = qrow ? __ldg(q4 + g) : zero;
       const float4 lb = two ? __ldg(l4 + g2) : zero, qb = (two && qrow) ? __ldg(q4 + g2) : zero;
-      visit(la.x, qa.x, 4 * g);
-      visit(la.y, qa.y, 4 * g + 1);
-      visit(la.z, qa.z, 4 * g + 2);
-      visit(la.w, qa.w, 4 * g + 3);
-      if (two) {
-        visit(lb.x, qb.x, 4 * g2);
-        visit(lb.y, qb.y, 4 * g2 + 1);
-        visit(lb.z, qb.z, 4 * g2 + 2);
-        visit(lb.w, qb.w, 4 * g2 + 3);
-      }
+      visit4(la, qa, g);
+      if (two) visit4(lb, qb, g2);
     }
   } else {
     for (int v = v0 + threadIdx.x; v < v1; v += kThreads) visit(lrow[v], qrow ? qrow[v] : 0.0f, v);

@@ -9,10 +9,12 @@
  * Stream layout (the pages do not fix one; this is the library's contract):
  *   key     = (seed low 32 bits, seed high 32 bits)
  *   counter = (request b, row j, vocab index v, tag)
- *   tag 1   accept uniform of row j           (v = 0)
+ *   tag 1   accept uniform of row j: word 0 of counter (b, j, 0, 1)
  *   tag 2   race exponential, residual sample at the first rejection
  *   tag 3   race exponential, bonus sample when every draft is accepted
- * Only output word 0 is used.
+ * The race variate of vocabulary index v takes output word v mod 4 of
+ * counter (b, j, floor(v / 4), tag): each generator call yields four
+ * independent words, one per consecutive vocabulary entry.
  */
 #include <math.h>
 #include "oracle.h"
@@ -61,7 +63,11 @@ extern "C" float oracle_accept_uniform(uint64_t seed, uint32_t b, uint32_t j) {
  * nearest), evaluated as -log1p(-u) in binary32: an Exp(1) variate whose
  * resolution near 0 (the race winners) is 2^-32. */
 extern "C" float oracle_race_exponential(uint64_t seed, uint32_t b, uint32_t j, uint32_t v, uint32_t tag) {
-  uint32_t x = philox_word0(seed, b, j, v, tag);
+  uint32_t ctr[4] = {b, j, v / 4u, tag};
+  uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  uint32_t x = out[v % 4u];
   float u = (float)x * 0x1p-32f;
   return -log1pf(-u);
 }

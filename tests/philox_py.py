@@ -42,9 +42,16 @@ def accept_uniform(seed, b, j):
     return np.float32(x >> 8) * np.float32(2.0 ** -24)
 
 
-def race_exponential_vec(seed, b, j, v, tag):
-    """E = -log1p(-u), u = float32(x) * 2^-32, in float32 (numpy)."""
+def race_words_vec(seed, b, j, v, tag):
+    """Race word of vocabulary index v: word v % 4 of counter (b, j, v // 4, tag)."""
     v = np.asarray(v, dtype=np.uint64)
-    x = philox_vec(np.full_like(v, b), np.full_like(v, j), v, np.full_like(v, tag), seed & MASK, seed >> 32)[0]
+    words = philox_vec(np.full_like(v, b), np.full_like(v, j), v >> np.uint64(2), np.full_like(v, tag), seed & MASK,
+                       seed >> 32)
+    return np.choose((v & np.uint64(3)).astype(np.int64), words)
+
+
+def race_exponential_vec(seed, b, j, v, tag):
+    """E = -log1p(-u), u = float32(x) * 2^-32 of the race word x, in float32 (numpy)."""
+    x = race_words_vec(seed, b, j, v, tag)
     u = x.astype(np.float32) * np.float32(2.0 ** -32)
     return -np.log1p(-u)

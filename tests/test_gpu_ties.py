@@ -16,7 +16,7 @@ to hold across those splits:
     rejection is corrected to the lowest-id argmax; a draft exactly tied
     with others is a near-tie (flagged on both sides), since the library
     takes the draft's own logit from a pre-pass;
-  * the race: two vocabulary ids whose Philox words are equal get equal
+  * the race: two vocabulary ids whose race words are equal get equal
     exponentials; with equal weights their keys are equal and the draw must
     be the lower id (and be flagged as a near-tie on both sides).
 """
@@ -32,7 +32,7 @@ if not torch.cuda.is_available():  # collected on CPU hosts too; the marker keep
 import mtp_speculative_decoding_verify_gb300 as mv  # noqa: E402
 from mtp_speculative_decoding_verify_gb300 import synth  # noqa: E402
 from gpu_util import gpu_lmhead, oracle_lmhead  # noqa: E402
-from philox_py import philox_vec  # noqa: E402
+from philox_py import race_words_vec  # noqa: E402
 
 DEV = torch.device("cuda:0")
 TAG_BONUS = 3
@@ -152,10 +152,10 @@ def test_relaxed_rank_past_tied_top_tokens(topk, accepted):
 
 
 def _philox_collision(V, b, j, tag, seeds):
-    """First (seed, v1, v2) with v1 < v2 whose race counters give the same Philox word."""
+    """First (seed, v1, v2) with v1 < v2 whose race words are equal."""
     v = np.arange(V, dtype=np.uint64)
     for seed in seeds:
-        x = philox_vec(np.full(V, b), np.full(V, j), v, np.full(V, tag), seed & 0xFFFFFFFF, seed >> 32)[0]
+        x = race_words_vec(seed, b, j, v, tag)
         order = np.argsort(x, kind="stable")
         xs = x[order]
         hit = np.nonzero(xs[1:] == xs[:-1])[0]

@@ -70,3 +70,18 @@ def test_race_exponential_is_exp1(orc):
     assert stats.kstest(E, "expon").pvalue > 1e-3
     got = np.array([orc.race_exponential(0, 1, 2, int(x), 2) for x in v[:500]], np.float32)
     np.testing.assert_array_max_ulp(got, E[:500], maxulp=2)
+
+
+def test_race_words_are_the_four_words_of_one_counter(orc):
+    """Vocabulary entries 4g .. 4g+3 take words 0..3 of counter (b, j, g, tag),
+    checked against the known-answer-pinned scalar Philox."""
+    from philox_py import race_words_vec
+    seed, b, j, tag = 0x0123_4567_89AB, 7, 2, 3
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for v in (0, 1, 2, 3, 4, 5, 6, 7, 1001, 151935):
+        want = philox((b, j, v // 4, tag), key)[v % 4]
+        assert int(race_words_vec(seed, b, j, [v], tag)[0]) == want
+        u = np.float32(want) * np.float32(2.0 ** -32)
+        e = np.float32(-np.log1p(-u))
+        got = np.float32(orc.race_exponential(seed, b, j, v, tag))
+        assert abs(float(got) - float(e)) <= 2 * float(np.spacing(e))
