@@ -122,10 +122,10 @@ TRAFFIC = {
         # written for 987.60 MB of KV cache
         "attention": (994850560 / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"], "79232e59d56890e8",
                       "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
-        # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 840.68 MB read
-        # + 101.20 MB written
-        "lm_head": ((840.679424e6 + 101.199616e6) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
-                    "292d26cf5444f530", "ncu capture of lmhead_tc_kernel at M=1024, vocabulary 65536 "
+        # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 648.17 MB read
+        # + 103.08 MB written
+        "lm_head": ((648.171520e6 + 103.081216e6) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1b478f3086f61bb2", "ncu capture of lmhead_tc_kernel at M=1024, vocabulary 65536 "
                                         "(profile_lm_cfg3_V64k)"),
     },
 }

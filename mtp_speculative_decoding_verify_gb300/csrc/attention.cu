@@ -18,6 +18,19 @@
 namespace mtp {
 
 // ------------------------------------------------------------------- append
+// Copy n elements, 16 bytes per access when both rows allow it.
+template <typename T>
+__device__ __forceinline__ void copy_row(const T* __restrict__ src, T* __restrict__ dst, int n) {
+  const int bytes = n * (int)sizeof(T);
+  if ((bytes % 16) == 0 && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) % 16) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int e = threadIdx.x; e < bytes / 16; e += blockDim.x) d4[e] = s4[e];
+  } else {
+    for (int e = threadIdx.x; e < n; e += blockDim.x) dst[e] = src[e];
+  }
+}
+
 // One CTA per (request, verify token): copy that token's K (and V) rows into
 // slot ctx+j of the paged cache.
 template <typename T>
@@ -44,14 +57,10 @@ __global__ void kv_append_kernel(const T* __restrict__ k_new, const T* __restric
   }
   const int64_t cache_row = (int64_t)blk * kBlock + (slot % kBlock);
   const int nk = Hkv * d_qk;
-  const T* ks = k_new + ((int64_t)b * R + j) * nk;
-  T* kd = k_cache + cache_row * nk;
-  for (int e = threadIdx.x; e < nk; e += blockDim.x) kd[e] = ks[e];
+  copy_row(k_new + ((int64_t)b * R + j) * nk, k_cache + cache_row * nk, nk);
   if (v_new != nullptr) {
     const int nv = Hkv * d_v;
-    const T* vs = v_new + ((int64_t)b * R + j) * nv;
-    T* vd = v_cache + cache_row * nv;
-    for (int e = threadIdx.x; e < nv; e += blockDim.x) vd[e] = vs[e];
+    copy_row(v_new + ((int64_t)b * R + j) * nv, v_cache + cache_row * nv, nv);
   }
 }
 
@@ -148,6 +157,10 @@ AttnPlan plan_attention(const mtp_attn_args& a, int sm_count) {
   if (attention_uses_mla_tc(a) || attention_uses_gqa_tc(a)) {   // one int per work item at most
     p.ws_order = p.ws_bytes;
     const size_t items = (size_t)p.n_splits * a.B * row_tiles * (a.is_mla ? 1 : a.Hkv);
+    p.ws_bytes += (items * sizeof(int32_t) + 255) / 256 * 256;
+  } else if (!a.is_mla && a.dtype == MTP_BF16 && attention_mma_supported(a)) {   // mma.sync GQA: its CTA order
+    p.ws_order = p.ws_bytes;
+    const size_t items = (size_t)p.n_splits * a.B * a.Hkv * attention_mma_row_tiles(a);
     p.ws_bytes += (items * sizeof(int32_t) + 255) / 256 * 256;
   }
   return p;

@@ -12,7 +12,8 @@
 // attn_gqa_kernel<D, tree, form>: GQA/MHA, d_qk = d_v = D (64 or 128). CTA =
 // (split, request x KV head, row block): the g*R query rows that share one
 // KV head (up to 112: one row warp per 16 rows), 64-key tiles = one cache
-// block. Forms 1 and 2 add key parts: warps sharing rows take alternate tiles
+// block. CTAs take their work items longest first from an order computed
+// just before the launch (gqa_mma_schedule_kernel). Forms 1 and 2 add key parts: warps sharing rows take alternate tiles
 // and merge their softmax state at the end (see run_gqa). Tree drafts use a
 // per-row root-path mask instead of the causal limit. (Absorbed MLA runs on
 // tcgen05: attention_mla_tc.cu.)
@@ -51,6 +52,8 @@ struct AttnKParams {
   int R, Hq, Hkv, group, rows;  // rows = query rows per (request, KV head)
   int row_warps, key_parts;     // consumer warps = row_warps x key_parts (warps sharing rows split the tiles)
   int max_blocks, num_blocks, split_len, n_splits, stages;
+  int B, row_tiles;              // requests, CTAs per (split, request, KV head)
+  const int32_t* order;          // CTA -> work item, longest first (gqa_mma_schedule_kernel)
   float scale_log2;              // sm_scale * log2(e)
 };
 
@@ -89,9 +92,13 @@ __global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaCo
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_cons = blockDim.x / 32 - 1;
-  const int split = blockIdx.x;
-  const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
-  const int row_base = blockIdx.z * kGqaRowsPerCta;
+  // Work item of this CTA: ((split * B + b) * Hkv + kvh) * row_tiles + row tile.
+  const int item = p.order[blockIdx.x];
+  const int per = p.Hkv * p.row_tiles;
+  const int split = item / (per * p.B);
+  const int b = (item / per) % p.B;
+  const int kvh = (item % per) / p.row_tiles;
+  const int row_base = (item % p.row_tiles) * kGqaRowsPerCta;
   const int ctx = p.ctx_lens[b];
   if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {
     if (threadIdx.x == 0 && split == 0) raise_error(p.err, MTP_ERR_LENGTH);
@@ -421,6 +428,45 @@ int gqa_occupancy(bool tree, int form, int warps, int stages) {
   return c;
 }
 
+constexpr int kMaxOrderTiles = 256;   // split_len <= 16384 keys = 256 cache blocks
+
+// CTA order of the GQA kernel, longest first (counting sort by the number
+// of 64-key tiles, one CTA): the block scheduler starts CTAs in index order,
+// so the long splits of long requests start in the first waves and the short
+// ones fill the tail, instead of whatever request happens to come last. The
+// row tiles and KV heads of one (split, request) stay adjacent: they read the
+// same cache pages (the heads of a token are interleaved in a block).
+__global__ void __launch_bounds__(1024) gqa_mma_schedule_kernel(const int32_t* __restrict__ ctx_lens, int B, int R,
+                                                               int per, int split_len, int n_splits, int max_len,
+                                                               int32_t* __restrict__ order) {
+  __shared__ int hist[kMaxOrderTiles + 1];
+  const int n = n_splits * B;   // groups (split, request); group q = split * B + b holds items q * per + i
+  auto tiles_of = [&](int q) -> int {
+    const int ctx = ctx_lens[q % B];
+    if (ctx < 0 || ctx + R > max_len) return 0;   // the attention kernel reports and skips the request
+    const int t0 = (q / B) * split_len;
+    const int t_end = min(t0 + split_len, ctx + R);
+    return t0 < t_end ? min((t_end - t0 + kBlock - 1) / kBlock, kMaxOrderTiles) : 0;
+  };
+  for (int k = threadIdx.x; k <= kMaxOrderTiles; k += blockDim.x) hist[k] = 0;
+  __syncthreads();
+  for (int q = threadIdx.x; q < n; q += blockDim.x) atomicAdd(&hist[tiles_of(q)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {   // hist[k] becomes the first group position of tile count k
+    int acc = 0;
+    for (int k = kMaxOrderTiles; k >= 0; --k) {
+      const int h = hist[k];
+      hist[k] = acc;
+      acc += h;
+    }
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const int pos = atomicAdd(&hist[tiles_of(q)], 1);
+    for (int i = 0; i < per; ++i) order[pos * per + i] = q * per + i;
+  }
+}
+
 template <int D>
 cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, cudaStream_t s) {
   // Consumer layout: one warp per 16 rows of the CTA. When a KV head has few
@@ -496,12 +542,23 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
   const GqaKernel<D> kern = gqa_kernel<D>(tree, form);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(pl.n_splits, a.B * a.Hkv, (rows + kGqaRowsPerCta - 1) / kGqaRowsPerCta);
-  kern<<<grid, 32 * (warps + 1), smem, s>>>(tk, tv, p);
+  p.B = a.B;
+  p.row_tiles = (rows + kGqaRowsPerCta - 1) / kGqaRowsPerCta;
+  int32_t* order = (int32_t*)((char*)a.workspace + pl.ws_order);
+  p.order = order;
+  const int per = a.Hkv * p.row_tiles;
+  gqa_mma_schedule_kernel<<<1, 1024, 0, s>>>(a.ctx_lens, a.B, R, per, pl.split_len, pl.n_splits,
+                                             a.max_blocks * kBlock, order);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kern<<<pl.n_splits * a.B * per, 32 * (warps + 1), smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int attention_mma_row_tiles(const mtp_attn_args& a) {
+  return (a.Hq / a.Hkv * (a.D + 1) + kGqaRowsPerCta - 1) / kGqaRowsPerCta;
+}
 
 bool attention_mma_supported(const mtp_attn_args& a) {
   if (a.dtype != MTP_BF16 || tensor_map_encoder() == nullptr) return false;

@@ -246,7 +246,8 @@ int mtp_verify_attention(const mtp_attn_args* a, void* stream) {
   if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   e = mtp::launch_attention_combine(*a, p, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention combine launch");
-  g_launches = 2 + (p.n_splits > 1 ? 1 : 0) + (mtp::attention_uses_mla_tc(*a) || mtp::attention_uses_gqa_tc(*a) ? 1 : 0);
+  // + the work-order kernel of every tensor-core attention path (MLA, GQA tcgen05, GQA mma.sync)
+  g_launches = 2 + (p.n_splits > 1 ? 1 : 0) + (a->dtype == MTP_BF16 && mtp::attention_mma_supported(*a) ? 1 : 0);
   return MTP_OK;
 }
 

@@ -32,6 +32,7 @@ bool attention_mma_supported(const mtp_attn_args& a);   // bf16 GQA/MHA (d 64, 1
 bool attention_uses_mla_tc(const mtp_attn_args& a);
 // bf16 GQA/MHA, head dim 128, 49..64 query rows per KV head: tcgen05 kernel
 bool attention_uses_gqa_tc(const mtp_attn_args& a);
+int attention_mma_row_tiles(const mtp_attn_args& a);      // CTAs per (split, request, KV head) of the mma.sync GQA kernel
 cudaError_t launch_attention_gqa_tc(const mtp_attn_args& a, const AttnPlan& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_attention_combine(const mtp_attn_args& a, const AttnPlan& p, cudaStream_t s);
 
