@@ -118,10 +118,10 @@ KERNEL_SOURCES = {
 
 TRAFFIC = {
     "cfg3": {
-        # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.25 MB read + 4.60 MB
+        # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.32 MB read + 4.22 MB
         # written for 987.60 MB of KV cache
-        "attention": (994850560 / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"], "79232e59d56890e8",
-                      "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
+        "attention": ((990315008 + 4223488) / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"],
+                      "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
         # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 648.17 MB read
         # + 103.08 MB written
         "lm_head": ((648.171520e6 + 103.081216e6) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
