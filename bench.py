@@ -114,9 +114,32 @@ def load_peaks():
 KERNEL_SOURCES = {
     "lm_head": ["lmhead_tc.cu", "common.cuh", "sm100.cuh"],
     "attention": ["attention_mma.cu", "common.cuh", "sm100.cuh", "mma_sync.cuh"],
+    "attention_mla": ["attention_mla_tc.cu", "common.cuh", "sm100.cuh"],
 }
 
 TRAFFIC = {
+    "cfg1_D3": {
+        # attn_mla_pair_kernel at the same shapes (profile_mla_V32k): 108.92 MB read + 4.93 MB written for
+        # 87.35 MB of latent KV (the rest: the queries, 18.9 MB, and the outputs)
+        "attention": ((108924416 + 4929024) / 87353856, "KV-cache bytes", KERNEL_SOURCES["attention_mla"],
+                      "f09f170b3ebfcee0", "ncu capture of attn_mla_pair_kernel (profile_mla_V32k)"),
+        # lmhead_tc_kernel<4, false> at M=128 with vocabulary 32768 (profile_mla_V32k): 471.70 MB read
+        # + 0.39 MB written
+        "lm_head": ((471699200 + 391936) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1b478f3086f61bb2",
+                    "ncu capture of lmhead_tc_kernel at M=128, vocabulary 32768 (profile_mla_V32k)"),
+    },
+    "cfg2": {
+        # attn_gqa_kernel<128> form 0 at the same shapes (profile_sampling_V32k): 1097.27 MB read
+        # + 6.63 MB written for 1075.31 MB of KV cache
+        "attention": ((1097269760 + 6626048) / 1075314688, "KV-cache bytes", KERNEL_SOURCES["attention"],
+                      "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel (profile_sampling_V32k)"),
+        # lmhead_tc_kernel<6, true> at M=384 with vocabulary 32768 (profile_sampling_V32k): 543.33 MB read
+        # + 25.43 MB written
+        "lm_head": ((543332608 + 25430784) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1b478f3086f61bb2",
+                    "ncu capture of lmhead_tc_kernel at M=384, vocabulary 32768 (profile_sampling_V32k)"),
+    },
     "cfg3": {
         # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.32 MB read + 4.22 MB
         # written for 987.60 MB of KV cache
@@ -253,10 +276,18 @@ class Step:
         self.out_tokens = torch.empty((w.B, w.R), dtype=torch.int32, device=dev)
         self.num_acc = torch.empty(w.B, dtype=torch.int32, device=dev)
         self.ties = torch.empty(w.B, dtype=torch.uint8, device=dev)
-        self.table_work = att["block_table"].clone()
-        self.seq = att["ctx_lens"].clone()
+        # The rollback edits the block table, the lengths and the free-list
+        # count in place; they live in one buffer so that a single copy from
+        # a pristine image restores them before every step.
+        nt, nb = att["block_table"].numel(), w.B
+        self.book = torch.empty(nt + nb + 1, dtype=torch.int32, device=dev)
+        self.book_init = torch.cat([att["block_table"].reshape(-1), att["ctx_lens"].reshape(-1),
+                                    torch.zeros(1, dtype=torch.int32, device=dev)])
+        self.book.copy_(self.book_init)
+        self.table_work = self.book[:nt].view(att["block_table"].shape)
+        self.seq = self.book[nt:nt + nb]
         self.free_list = torch.full((w.B * 2 + 8,), -1, dtype=torch.int32, device=dev)
-        self.free_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.free_count = self.book[nt + nb:]
         self.parents = lm.get("parents")
         self.acc_nodes = torch.empty((w.B, w.R), dtype=torch.int32, device=dev)
         self.a_attn = B.attn_args(att["q"], att["k_new"], att["v_new"], att["k_cache"], att["v_cache"],
@@ -280,9 +311,7 @@ class Step:
     def run(self, stream):
         h = ctypes.c_void_p(stream.cuda_stream)
         # Reset the rollback's bookkeeping so every step starts from the same state.
-        self.table_work.copy_(self.att["block_table"])
-        self.seq.copy_(self.att["ctx_lens"])
-        self.free_count.zero_()
+        self.book.copy_(self.book_init)
         L, chk = self.L, self.B._check
         chk(L.mtp_verify_attention(ctypes.byref(self.a_attn), h))
         n = L.mtp_last_launch_count()

@@ -170,6 +170,10 @@ def test_relaxed_full_size_cfg1_sampled_requests():
     for k in ("out_tokens", "num_accepted", "tie_flags", "lse", "argmax"):
         assert torch.equal(gpu[k], dbg[k]), k
     flagged, _ = _check(w, lm, dbg, [0, 17, 31])
+    ties = gpu["tie_flags"].cpu().numpy()
+    print("relaxed DeepSeek-V3-shaped step: %d of %d requests inside the relaxed near-tie band (excluded from the "
+          "bit-exact comparison); sampled requests flagged on either side: %d of 3" %
+          (int(((ties & 1) != 0).sum()), w.B, flagged))
     assert flagged <= 1
     check_invariants(w, lm, gpu)
     del lm, gpu, dbg
