@@ -308,13 +308,17 @@ class Step:
             args.timing_events[0] = pair[0].cuda_event if pair else None
             args.timing_events[1] = pair[1].cuda_event if pair else None
 
-    def run(self, stream):
+    def run(self, stream, before_lm=None):
+        """The step's calls on `stream`; before_lm(stream), if given, runs
+        between the attention call and the LM-head call."""
         h = ctypes.c_void_p(stream.cuda_stream)
         # Reset the rollback's bookkeeping so every step starts from the same state.
         self.book.copy_(self.book_init)
         L, chk = self.L, self.B._check
         chk(L.mtp_verify_attention(ctypes.byref(self.a_attn), h))
         n = L.mtp_last_launch_count()
+        if before_lm is not None:
+            before_lm(stream)
         chk(L.mtp_verify_logits_accept(ctypes.byref(self.a_lm), h))
         n += L.mtp_last_launch_count()
         if self.a_cmp is not None:
@@ -323,6 +327,9 @@ class Step:
         chk(L.kv_rollback(ctypes.byref(self.a_rb), h))
         n += L.mtp_last_launch_count()
         self.launches = n
+
+    # Inputs the attention call reads; the others are read from the LM-head call on.
+    ATTENTION_INPUTS = ("q", "k_new", "v_new", "ctx_lens", "parents")
 
     def host_inputs(self):
         """Device tensors that carry a step's inputs (copied from host memory in
@@ -376,8 +383,12 @@ class DraftStep:
         self.args[0].timing_events[0] = lm_pair[0].cuda_event if lm_pair else None
         self.args[0].timing_events[1] = lm_pair[1].cuda_event if lm_pair else None
 
-    def run(self, stream):
+    ATTENTION_INPUTS = ()
+
+    def run(self, stream, before_lm=None):
         h = ctypes.c_void_p(stream.cuda_stream)
+        if before_lm is not None:
+            before_lm(stream)
         n = 0
         for a in self.args:
             self.B._check(self.L.mtp_draft_argmax(ctypes.byref(a), h))
@@ -502,10 +513,23 @@ def run_gpu(args, w, rank, world, dev):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    # A step's inputs cross in two groups: what the attention reads, on the
+    # step's stream before the attention call, and what only the LM head and
+    # acceptance read (hidden states, tokens, draft distributions, ...), on a
+    # second stream that the LM-head call then waits for, so that those
+    # copies overlap the attention of the same step.
+    first = {k: t for k, t in host.items() if k in step.ATTENTION_INPUTS}
+    later = {k: t for k, t in host.items() if k not in step.ATTENTION_INPUTS}
+    copy_stream = torch.cuda.Stream()
+
     def e2e_step(st):
-        for k, t in host.items():
+        for k, t in first.items():
             dev_t[k].copy_(t, non_blocking=True)
-        step.run(st)
+        copy_stream.wait_stream(st)
+        with torch.cuda.stream(copy_stream):
+            for k, t in later.items():
+                dev_t[k].copy_(t, non_blocking=True)
+        step.run(st, before_lm=lambda s2: s2.wait_stream(copy_stream))
         for th, td in zip(res_host, res_dev):
             th.copy_(td, non_blocking=True)
 
@@ -833,7 +857,9 @@ def main():
                 kernels=kernels,
                 e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
                          d2h_bytes_per_step=r["d2h"], ms_per_step=r["e2e_ms"],
-                         path="pinned host inputs -> device, the library calls, results -> pinned host, "
+                         path="pinned host inputs -> device (the attention's inputs first; the LM head's, "
+                              "q of the sampling requests included, on a second stream during the attention), "
+                              "the library calls, results -> pinned host, "
                               + ("captured once as a CUDA graph and replayed" if r["e2e_graph"] else "eager")
                               + ", host wall clock per step including the synchronize"),
                 gpu_launches=r["launches"], clocks=r["clocks"])
