@@ -513,14 +513,18 @@ def run_gpu(args, w, rank, world, dev):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    # A step's inputs cross in two groups: what the attention reads, on the
-    # step's stream before the attention call, and what only the LM head and
-    # acceptance read (hidden states, tokens, draft distributions, ...), on a
-    # second stream that the LM-head call then waits for, so that those
-    # copies overlap the attention of the same step.
+    # A step's inputs cross in three groups: what the attention reads, on the
+    # step's stream before the attention call; what the LM head reads (hidden
+    # states, tokens, modes, ...), on a second stream during the attention,
+    # which the LM-head call waits for; and the draft distributions q, read
+    # only by the acceptance kernels, on that stream after them: the library
+    # waits for their event (q_ready_event) only once the LM-head GEMM has
+    # been launched, so q's copy overlaps the attention and the GEMM.
     first = {k: t for k, t in host.items() if k in step.ATTENTION_INPUTS}
-    later = {k: t for k, t in host.items() if k not in step.ATTENTION_INPUTS}
+    later = {k: t for k, t in host.items() if k not in step.ATTENTION_INPUTS and k != "q_draft"}
+    qcopy = {k: t for k, t in host.items() if k == "q_draft"}
     copy_stream = torch.cuda.Stream()
+    ev_lm, ev_q = torch.cuda.Event(), torch.cuda.Event()
 
     def e2e_step(st):
         for k, t in first.items():
@@ -529,7 +533,14 @@ def run_gpu(args, w, rank, world, dev):
         with torch.cuda.stream(copy_stream):
             for k, t in later.items():
                 dev_t[k].copy_(t, non_blocking=True)
-        step.run(st, before_lm=lambda s2: s2.wait_stream(copy_stream))
+            ev_lm.record(copy_stream)
+            for k, t in qcopy.items():
+                dev_t[k].copy_(t, non_blocking=True)
+            ev_q.record(copy_stream)
+        if hasattr(step, "a_lm"):
+            step.a_lm.q_ready_event = ev_q.cuda_event if qcopy else None
+        step.run(st, before_lm=lambda s2: s2.wait_event(ev_lm if hasattr(step, "a_lm") else ev_q))
+        st.wait_stream(copy_stream)
         for th, td in zip(res_host, res_dev):
             th.copy_(td, non_blocking=True)
 
@@ -557,6 +568,8 @@ def run_gpu(args, w, rank, world, dev):
             e2e_step(stream)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - e2e_t0) * 1e3 / K
+    if hasattr(step, "a_lm"):
+        step.a_lm.q_ready_event = None
 
     ms, e2e_ms, emitted = combine_ranks(ms, e2e_ms, emitted, world, dev)
     ms_eager, _, _ = combine_ranks(ms_eager, 0.0, 0.0, world, dev)
@@ -857,8 +870,9 @@ def main():
                 kernels=kernels,
                 e2e=dict(value=world * w.B / (r["e2e_ms"] * 1e-3), unit="requests/s", h2d_bytes_per_step=r["h2d"],
                          d2h_bytes_per_step=r["d2h"], ms_per_step=r["e2e_ms"],
-                         path="pinned host inputs -> device (the attention's inputs first; the LM head's, "
-                              "q of the sampling requests included, on a second stream during the attention), "
+                         path="pinned host inputs -> device (the attention's inputs first; the LM head's on a "
+                              "second stream during the attention, then q of the sampling requests, which the "
+                              "library waits for after launching the LM-head GEMM), "
                               "the library calls, results -> pinned host, "
                               + ("captured once as a CUDA graph and replayed" if r["e2e_graph"] else "eager")
                               + ", host wall clock per step including the synchronize"),

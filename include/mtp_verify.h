@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MTP_ABI_VERSION 4
+#define MTP_ABI_VERSION 5
 
 typedef enum {
   MTP_OK = 0,
@@ -239,6 +239,12 @@ typedef struct {
   size_t workspace_bytes;
   void* timing_events[2];    /* optional cudaEvent_t pair recorded on `stream` just before and just
                                 after the LM-head GEMM kernel (acceptance kernels excluded) */
+  void* q_ready_event;       /* optional cudaEvent_t: after launching the LM-head GEMM the call makes
+                                `stream` wait for it (cudaStreamWaitEvent) before the first kernel
+                                that reads q_draft, so a caller can still be copying q_draft (e.g.
+                                from host memory on another stream) while the GEMM runs; the event
+                                must have been recorded (or be recorded in the same graph capture)
+                                after that copy. NULL: q_draft is complete when the call is made. */
 } mtp_lmhead_args;
 
 size_t mtp_lmhead_workspace_size(const mtp_lmhead_args* args);

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libmtpverify.so")
 
 MTP_OK, MTP_INVALID_ARG, MTP_UNSUPPORTED, MTP_CUDA_ERROR, MTP_DEVICE_ERROR = range(5)
-ABI_VERSION = 4   # MTP_ABI_VERSION of the header the structs below mirror
+ABI_VERSION = 5   # MTP_ABI_VERSION of the header the structs below mirror
 MTP_F32, MTP_BF16 = 0, 1
 MAX_DRAFTS = 15
 BLOCK_SIZE = 64
@@ -38,7 +38,8 @@ class LmArgs(ctypes.Structure):
                 ("tie_flags", _P), ("lse_out", _P), ("argmax_out", _P), ("logits_debug", _P),
                 ("B", _I), ("D", _I), ("H", _I), ("V", _I), ("dtype", _I), ("any_sampling", _I),
                 ("relaxed_topk", _I), ("relaxed_delta", ctypes.c_float), ("parents", _P), ("accepted_nodes", _P),
-                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2)]
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("timing_events", _P * 2),
+                ("q_ready_event", _P)]
 
 
 class DraftArgs(ctypes.Structure):
@@ -262,7 +263,8 @@ def lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_token
 
 def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted,
                              tie_flags, lse_out=None, argmax_out=None, logits_debug=None, workspace=None,
-                             stream=None, relaxed_topk=0, relaxed_delta=0.0, parents=None, accepted_nodes=None):
+                             stream=None, relaxed_topk=0, relaxed_delta=0.0, parents=None, accepted_nodes=None,
+                             q_ready_event=None):
     """LM head + streaming softmax statistics + greedy / rejection-sampling / relaxed acceptance.
 
     hidden [B*R, H], lm_head [V, H] (float32 or bfloat16), tokens [B, R] int32, mode [B] uint8,
@@ -270,9 +272,12 @@ def mtp_verify_logits_accept(hidden, lm_head, tokens, mode, temperature, q_draft
     outputs out_tokens [B, R] int32, num_accepted [B] int32, tie_flags [B] uint8, optional lse_out / argmax_out
     [B, R] and logits_debug [B*R, V]. relaxed_topk / relaxed_delta: the relaxed rule of mode-2 requests.
     parents [B, R] int32: tree drafts (greedy); accepted_nodes [B, R] int32: optional output, the accepted path.
+    q_ready_event: optional torch.cuda.Event recorded after q_draft's copy; the stream waits for it only
+    after the LM-head GEMM has been launched, so the copy may overlap the GEMM.
     """
     a = lm_args(hidden, lm_head, tokens, mode, temperature, q_draft, seed, out_tokens, num_accepted, tie_flags,
                 lse_out, argmax_out, logits_debug, workspace, relaxed_topk, relaxed_delta, parents, accepted_nodes)
+    a.q_ready_event = None if q_ready_event is None else q_ready_event.cuda_event
     _check(lib().mtp_verify_logits_accept(ctypes.byref(a), _stream_handle(stream)))
 
 

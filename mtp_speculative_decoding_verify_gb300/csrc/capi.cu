@@ -276,6 +276,8 @@ int mtp_verify_logits_accept(const mtp_lmhead_args* a, void* stream) {
   e = p.tc ? mtp::launch_lmhead_tc(*a, p, c->err, s) : mtp::launch_lmhead_simt(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "LM head launch");
   if ((e = record(a->timing_events[1], s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  if (a->q_ready_event && (e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(a->q_ready_event), 0)) != cudaSuccess)
+    return cuda_fail(e, "cudaStreamWaitEvent(q_ready_event)");
   e = mtp::launch_accept(*a, p, c->err, s);
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");
   g_launches = 2 + (a->any_sampling ? 1 : 0) + (a->relaxed_topk > 0 ? 1 : 0);

@@ -97,6 +97,8 @@ extern "C" int mtp_verify_logits_accept_noalloc(const mtp_lmhead_args* args, voi
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "LM head launch");
   e = a.timing_events[1] ? cudaEventRecord(static_cast<cudaEvent_t>(a.timing_events[1]), s) : cudaSuccess;
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaEventRecord");
+  e = a.q_ready_event ? cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(a.q_ready_event), 0) : cudaSuccess;
+  if (e != cudaSuccess) return mtp::set_cuda_error(e, "cudaStreamWaitEvent(q_ready_event)");
   e = mtp::launch_accept(a, p, err, s);
   if (e != cudaSuccess) return mtp::set_cuda_error(e, "accept launch");
   mtp::set_launch_count(2 + (a.any_sampling ? 1 : 0) + (a.relaxed_topk > 0 ? 1 : 0));

@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(mtplib):
 
 def test_struct_layouts_match(mtplib):
     L = mtplib.lib()
-    assert L.mtp_abi_version() == mtplib.ABI_VERSION == 4
+    assert L.mtp_abi_version() == mtplib.ABI_VERSION == 5
     for which, st in enumerate((mtplib.AttnArgs, mtplib.LmArgs, mtplib.RollbackArgs, mtplib.DraftArgs,
                                 mtplib.KvCompactArgs)):
         assert L.mtp_abi_struct_size(which) == ctypes.sizeof(st)

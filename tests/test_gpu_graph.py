@@ -90,3 +90,55 @@ def test_graph_replay_equals_eager(name):
     if lm.get("parents") is not None:
         assert torch.equal(eager["nodes"], replay["nodes"])
     assert torch.equal(att["k_cache"], k_eager)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_q_copy_overlapping_the_lm_head_matches_resident_q(graph):
+    """q_ready_event: the draft distributions still crossing from pinned host
+    memory on another stream when the call is made (the library waits for
+    them only after launching the LM-head GEMM), eagerly and inside a graph
+    capture, give the same tokens, counts and flags as q already resident."""
+    w = synth.CFG2.with_(name="q overlap", B=6, D=3, Hq=16, Hkv=2, ctx=(64, 200), H=256, V=5003, stream=55)
+    lm = synth.make_lmhead_inputs(w, DEV)
+
+    def outs():
+        return dict(tok=torch.full((w.B, w.R), -9, dtype=torch.int32, device=DEV),
+                    n=torch.full((w.B,), -9, dtype=torch.int32, device=DEV),
+                    tie=torch.full((w.B,), 255, dtype=torch.uint8, device=DEV))
+
+    ref = outs()
+    mv.mtp_verify_logits_accept(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
+                                lm["q_draft"], lm["seed"], ref["tok"], ref["n"], ref["tie"])
+    torch.cuda.synchronize()
+    q_host = lm["q_draft"].cpu().pin_memory()
+    q_dev = torch.zeros_like(lm["q_draft"])
+    got = outs()
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+
+    def step():
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            q_dev.copy_(q_host, non_blocking=True)
+            ev.record(side)
+        mv.mtp_verify_logits_accept(lm["hidden"], lm["lm_head"], lm["tokens"], lm["mode"], lm["temperature"],
+                                    q_dev, lm["seed"], got["tok"], got["n"], got["tie"], stream=main,
+                                    q_ready_event=ev)
+        main.wait_stream(side)
+
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        main.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=main):
+            step()
+        q_dev.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        main.wait_stream(torch.cuda.current_stream())
+        step()
+    torch.cuda.synchronize()
+    mv.sync_status()
+    assert (lm["mode"] == 1).all()
+    for k in ("tok", "n", "tie"):
+        assert torch.equal(got[k], ref[k]), k
