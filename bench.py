@@ -123,10 +123,10 @@ TRAFFIC = {
         # 87.35 MB of latent KV (the rest: the queries, 18.9 MB, and the outputs)
         "attention": ((108924416 + 4929024) / 87353856, "KV-cache bytes", KERNEL_SOURCES["attention_mla"],
                       "f09f170b3ebfcee0", "ncu capture of attn_mla_pair_kernel (profile_mla_V32k)"),
-        # lmhead_tc_kernel<4, false> at M=128 with vocabulary 32768 (profile_mla_V32k): 471.70 MB read
-        # + 0.39 MB written
-        "lm_head": ((471699200 + 391936) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
-                    "1b478f3086f61bb2",
+        # lmhead_tc_kernel<4, true> (CTA pairs) at M=128 with vocabulary 32768 (profile_mla_V32k):
+        # 471.69 MB read + 2.82 MB written
+        "lm_head": ((471687168 + 2816256) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1e081f7967bd35e6",
                     "ncu capture of lmhead_tc_kernel at M=128, vocabulary 32768 (profile_mla_V32k)"),
     },
     "cfg2": {
@@ -134,10 +134,10 @@ TRAFFIC = {
         # + 6.63 MB written for 1075.31 MB of KV cache
         "attention": ((1097269760 + 6626048) / 1075314688, "KV-cache bytes", KERNEL_SOURCES["attention"],
                       "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel (profile_sampling_V32k)"),
-        # lmhead_tc_kernel<6, true> at M=384 with vocabulary 32768 (profile_sampling_V32k): 543.33 MB read
-        # + 25.43 MB written
-        "lm_head": ((543332608 + 25430784) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
-                    "1b478f3086f61bb2",
+        # lmhead_tc_kernel<6, true> at M=384 with vocabulary 32768 (profile_sampling_V32k): 543.31 MB read
+        # + 21.74 MB written
+        "lm_head": ((543312896 + 21744896) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1e081f7967bd35e6",
                     "ncu capture of lmhead_tc_kernel at M=384, vocabulary 32768 (profile_sampling_V32k)"),
     },
     "cfg3": {
@@ -145,10 +145,10 @@ TRAFFIC = {
         # written for 987.60 MB of KV cache
         "attention": ((990315008 + 4223488) / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"],
                       "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
-        # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 648.17 MB read
-        # + 103.08 MB written
-        "lm_head": ((648.171520e6 + 103.081216e6) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
-                    "1b478f3086f61bb2", "ncu capture of lmhead_tc_kernel at M=1024, vocabulary 65536 "
+        # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 616.33 MB read
+        # + 102.73 MB written
+        "lm_head": ((616330496 + 102726400) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
+                    "1e081f7967bd35e6", "ncu capture of lmhead_tc_kernel at M=1024, vocabulary 65536 "
                                         "(profile_lm_cfg3_V64k)"),
     },
 }

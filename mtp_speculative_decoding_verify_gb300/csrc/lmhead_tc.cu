@@ -487,7 +487,11 @@ struct TcShape {
   uint32_t tmem_cols;
 };
 
-constexpr int kPairMinRows = 193;   // from here on a 128-lane tile is bound by shared-memory traffic
+// CTA pairs from 33 verify rows on: a pair halves the hidden tile that each
+// SM restages for every vocabulary tile, which relieves shared memory even
+// where W's stream sets the pace (measured on the GB300: 64..192 rows 1-3 %
+// faster, 32 rows unchanged). Fewer rows keep single-CTA tiles.
+constexpr int kPairMinRows = 33;
 
 template <int NCH, bool kPair>
 cudaError_t set_smem(int smem) {

@@ -42,7 +42,9 @@ SMALL = {
     "mla_cluster4": synth.CFG1.with_(name="MLA 4 row blocks", B=3, Hq=64, ctx=(60, 700), H=256, V=2000),
     "mla_cluster3": synth.CFG1.with_(name="MLA 3 row blocks", B=2, Hq=48, ctx=(130, 400), H=128, V=777),
     "mla_single_row_block": synth.CFG1.with_(name="MLA 1 row block", B=3, Hq=16, ctx=(100, 900), H=128, V=777),
-    # LM head on CTA pairs (M >= 193 rows): ragged row group (M=200 -> N=224) and vocabulary tail
+    # LM head on CTA pairs (M >= 33 rows): ragged row groups (M=40 -> N=64, M=200 -> N=224) and vocabulary tails
+    "lm_pair_small_mixed": synth.CFG3.with_(name="LM head pairs, N=64", B=10, D=3, Hq=8, Hkv=2, ctx=(30, 150),
+                                            H=192, V=3001),
     "lm_pair_ragged_sampling": synth.CFG2.with_(name="LM head pairs, sampling", B=50, D=3, Hq=8, Hkv=2,
                                                 ctx=(40, 90), H=256, V=5003),
     "lm_pair_two_groups_mixed": synth.CFG3.with_(name="LM head pairs, 2 groups", B=100, D=3, Hq=8, Hkv=2,

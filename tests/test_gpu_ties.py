@@ -55,6 +55,7 @@ def _plant_duplicates(lm, ids, scale, rows):
 
 LM_CASES = {
     "tc_single_cta": dict(dtype="bf16", B=4, D=3, H=128),      # M = 16: single-CTA tensor-core LM head
+    "tc_cta_pairs_n64": dict(dtype="bf16", B=10, D=3, H=128),  # M = 40: CTA pairs of N = 64
     "tc_cta_pairs": dict(dtype="bf16", B=50, D=3, H=128),      # M = 200: CTA pairs
     "tc_two_row_groups": dict(dtype="bf16", B=100, D=3, H=64),  # M = 400: two row groups on CTA pairs
     "simt_fp32": dict(dtype="f32", B=4, D=3, H=64),            # fp32 SIMT LM head
