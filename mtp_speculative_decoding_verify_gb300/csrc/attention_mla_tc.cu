@@ -661,12 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 // its lazy rescale, the row sums and the normalisation stay local to the CTA.
 // Per 128-key tile a CTA stages 136 KB and reads ~250 KB of operands, against
 // 147 KB and ~410 KB for one 64-row CTA on its own; the MMAs have N = 128/256.
-// The nine K chunks of a tile land on one barrier and are released together
-// once QK has read them, and likewise the eight V boxes: the next tile's keys
-// and values load during the softmax and PV, and the issue loop only waits
-// four times per tile (each wait costs the issuing warp a few hundred clocks
-// even when the phase is already complete). The softmax's reduction scratch
-// shares the P buffer (used only while no PV reads it).
+// The key tile is single-buffered, so the next tile's keys can only load into
+// chunks that QK has finished with: the nine K chunks land and are released
+// in three groups of three, and the eight V boxes in two key halves, so the
+// loads of tile i+1 start while QK(i) (and PV(i-1)) still run. Two warps
+// issue the MMAs: one QK(i) as soon as its key groups land, the other PV(i)
+// as soon as P(i) is written, so QK(i+1) runs during the softmax of tile i
+// instead of waiting behind PV(i) (S is double-buffered; each issuing warp
+// waits only for its own inputs: a wait costs the issuing warp a few hundred
+// clocks even when the phase is already complete). P is single-buffered: the
+// softmax of tile i computes its probabilities in registers, then waits for
+// PV(i-1) before writing them (and before using the reduction scratch, which
+// shares the P buffer).
 namespace pr {
 constexpr int kQOff = 0;                          // 9 x [64 rows x 64 dims]
 constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]
@@ -675,7 +681,8 @@ constexpr int kPOff = kVOff + 8 * 8192;           // P [64 rows x 128 keys]: key
 constexpr int kRedOff = kPOff + 8192;             // red_max[8][64], red_sum[8][64] alias P keys 64..127
 constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, path [64] u32
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
-constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull uses 3 of its 9)
+constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull / kempty use 3 of their 9)
+constexpr int kKGroups = 3;                       // K chunks land and are released in groups of three
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kColO = 0;                     // O of product h at columns 128 h .. +127
@@ -696,10 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   float* m_shift = m_run + 192;
   float* l_run = m_run + 256;
   uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 320);   // per row: path mask (tree) or key limit (chain)
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // leader: both CTAs' 9 K chunks landed
-  uint64_t* kempty = kfull + 9;                                         // both: the K slots are free
-  uint64_t* vfull = kempty + 9;                                         // leader: both CTAs' 8 V boxes landed
-  uint64_t* vempty = vfull + 2;                                         // both: the V slots are free
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // [3] leader: both CTAs' K chunk group landed
+  uint64_t* kempty = kfull + 9;                                         // [3] both: the group's K slots are free
+  uint64_t* vfull = kempty + 9;                                         // [2] leader: both CTAs' V boxes of a key half
+  uint64_t* vempty = vfull + 2;                                         // [2] both: the key half's V slots are free
   uint64_t* qbar = vempty + 2;                                          // leader: both CTAs' Q landed
   uint64_t* s_full = qbar + 1;                                          // [2] both
   uint64_t* s_empty = s_full + 2;                                       // [2] leader, one arrive per CTA
@@ -727,18 +734,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
 
   if (threadIdx.x == 0) {
-    sm100::mbar_init(kfull, 1);
-    sm100::mbar_init(kempty, 1);
-    sm100::mbar_init(vfull, 1);
-    sm100::mbar_init(vempty, 1);
+    for (int g = 0; g < pr::kKGroups; ++g) {
+      sm100::mbar_init(&kfull[g], 1);
+      sm100::mbar_init(&kempty[g], 1);
+    }
     for (int k = 0; k < 2; ++k) {
+      sm100::mbar_init(&vfull[k], 1);
+      sm100::mbar_init(&vempty[k], 1);
       sm100::mbar_init(&s_full[k], 1);
       sm100::mbar_init(&s_empty[k], 2);   // one arrive per CTA
     }
     sm100::mbar_init(qbar, 1);
     sm100::mbar_init(p_full, 2);
     sm100::mbar_init(o_done, 1);
-    sm100::mbar_init(final_bar, 1);
+    sm100::mbar_init(final_bar, 2);   // the QK and the PV issuer each commit once at the end
     *abort = 0;
     sm100::fence_barrier_init();
   }
@@ -806,7 +815,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       const bool any_exceed = softmax_barrier_any(exceed);
       // every softmax warp of this CTA has read S(i) from TMEM: one arrive
       if (st == 0) sm100::mbar_arrive_remote_relaxed(&s_empty[buf], 0);
+      // PV(i-1) reads P (which the reduction scratch shares) and accumulates
+      // into O, and may still run (QK(i) does not wait for it): the O rescale
+      // and the P stores wait for its completion. (The softmax of tile i-1
+      // waited for PV(i-2), so the parity cannot alias an older phase.)
+      bool pv_done = i == 0;
+      auto wait_pv = [&]() {
+        if (!pv_done) {
+          ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (i - 1) & 1, abort) ? 1 : 0);
+          sm100::tc_fence_after();
+          pv_done = true;
+        }
+      };
       if (any_exceed) {
+        wait_pv();
         float mx = d[0];
 #pragma unroll
         for (int x = 1; x < 16; ++x) mx = fmaxf(mx, d[x]);
@@ -852,8 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         }
       }
       // p = 2^d into P [64 rows x 128 keys] (K-major A operand of PV, two
-      // 64-key blocks) and into the partial row sum. (PV(i-1) is complete and
-      // no thread reads red_max any more, which shares the second block.)
+      // 64-key blocks) and into the partial row sum, once PV(i-1) is complete
+      // (no thread reads red_max any more, which shares the second block).
       {
         uint8_t* pb = smem + pr::kPOff + khalf * 8192 + r * 128;
         uint32_t w[8];
@@ -863,6 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
           acc += p0 + p1;
           w[x / 2] = pack_bf16x2(p0, p1);
         }
+        wait_pv();
         const int ch = 2 * sub;   // 16-byte chunks 2 sub, 2 sub + 1 of the row
         *reinterpret_cast<uint4*>(pb + (((ch) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(pb + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -941,14 +964,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
     softmax_role();
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLight));
-    const int pw = (warp >= 1 && lane < 2) ? 2 * (warp - 1) + lane : -1;   // producer 0..5
+    const int pw = (warp >= 2 && lane < 4) ? 4 * (warp - 2) + lane : -1;   // producer 0..7 (warps 2-3, lanes 0-3)
     if (pw >= 0) {
       // ------------------------------------------------------ TMA producers
       // Per tile a CTA loads 17 boxes of [64 keys x 64 dims]: K chunk c of its
-      // own key half (slot c), and V boxes (h, kb, j) = dims 64 (4 h + 2 rank + j)
-      // of key half kb. Both CTAs' boxes complete on the leader's barriers.
-      // Producer pw owns K chunk pw (and pw + 6 for pw < 3); producers 3-5
-      // also own the V boxes: 3 -> (h 0, kb 0), 4 -> (h 1, kb 0), 5 -> kb 1.
+      // own key half (slot c, group c / 3), and V boxes (h, kb, j) = dims
+      // 64 (4 h + 2 rank + j) of key half kb. Both CTAs' boxes complete on the
+      // leader's barriers. Producers 0-5 own K chunk pw (and pw + 6 for
+      // pw < 3), each waiting for its group's slots to be released by the
+      // previous tile's QK; producers 6 and 7 own the V boxes of key half
+      // pw - 6, released by the previous tile's PV.
       const uint64_t pol_kv = sm100::l2_policy_evict_last();
       const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
       auto block_of = [&](int key0) -> int {
@@ -968,42 +993,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         for (int c = 0; c < kQChunks; ++c)   // both CTAs' Q complete on the leader's barrier
           sm100::tma_load_2d_pair(smem + pr::kQOff + c * 8192, &tm_q, qbar, 0, c * 64, b * rows + row_base, pol_q);
       }
+      constexpr int kGroupBytes = 2 * 3 * 8192;   // both CTAs' three K chunks
+      constexpr int kHalfBytes = 2 * 4 * 8192;    // both CTAs' four V boxes of a key half
       bool ok = true;
-      const int kc0 = pw, kc1 = pw + 6;   // K chunks of this producer (kc1 valid for pw < 3)
       for (int i = 0; i < n_tiles && ok; ++i) {
         const uint32_t par = (uint32_t)((i & 1) ^ 1);
-        const int own_key0 = t0 + i * kKeys + 64 * (int)rank;
-        // K chunk kc0 (released after QK)
-        {
-          ok = sm100::mbar_wait_cluster(kempty, par, abort);
+        if (pw < 6) {
+          const int own_key0 = t0 + i * kKeys + 64 * (int)rank;
+          const int blk = block_of(own_key0);
+          for (int c = pw; c < 9; c += 6) {   // chunk pw, then pw + 6 (group 2) for pw < 3
+            const int g = c / 3;
+            ok = sm100::mbar_wait_cluster(&kempty[g], par, abort);
+            if (!ok) break;
+            if (leader && c % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[g], kGroupBytes);
+            sm100::tma_load_3d_pair(smem + pr::kKOff + c * 8192, &tm_kv, &kfull[g], 0, c * 64, 0, blk, pol_kv);
+          }
+        } else {
+          const int kb = pw - 6;
+          ok = sm100::mbar_wait_cluster(&vempty[kb], par, abort);
           if (!ok) break;
-          if (leader && pw == 0) sm100::mbar_arrive_expect_tx(kfull, 2 * 9 * 8192);
-          sm100::tma_load_3d_pair(smem + pr::kKOff + kc0 * 8192, &tm_kv, kfull, 0, kc0 * 64, 0, block_of(own_key0),
-                                  pol_kv);
-        }
-        // V boxes
-        if (pw >= 3) {
-          const int kb = pw == 5 ? 1 : 0;
-          ok = sm100::mbar_wait_cluster(vempty, par, abort);
-          if (!ok) break;
-          if (leader && pw == 3) sm100::mbar_arrive_expect_tx(vfull, 2 * 8 * 8192);
-          const int key0 = t0 + i * kKeys + 64 * kb;
-          const int blk = block_of(key0);
-          for (int h = 0; h < 2; ++h) {
-            if (pw == 3 && h == 1) continue;
-            if (pw == 4 && h == 0) continue;
+          if (leader) sm100::mbar_arrive_expect_tx(&vfull[kb], kHalfBytes);
+          const int blk = block_of(t0 + i * kKeys + 64 * kb);
+          for (int h = 0; h < 2; ++h)
             for (int j = 0; j < 2; ++j) {
               const int slot = (h * 2 + kb) * 2 + j;
               const int dchunk = 4 * h + 2 * (int)rank + j;
-              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, vfull, 0, dchunk * 64, 0, blk,
+              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[kb], 0, dchunk * 64, 0, blk,
                                       pol_kv);
             }
-          }
         }
-        // K chunk kc1 (slots 6, 7, 8)
-        if (kc1 < 9)   // the K slots were free already (same phase)
-          sm100::tma_load_3d_pair(smem + pr::kKOff + kc1 * 8192, &tm_kv, kfull, 0, kc1 * 64, 0, block_of(own_key0),
-                                  pol_kv);
       }
       if (!ok) {
         *abort = 1;
@@ -1012,82 +1030,90 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       // The leader's producers wait (time-limited) for the last fill of each
       // barrier they armed; the odd CTA's copies complete on those barriers.
       if (leader) {
-        if (pw == 0) sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
         const uint32_t last = (uint32_t)((n_tiles - 1) & 1);
-        if (pw == 0) sm100::mbar_wait_timeout(kfull, last, sm100::kWaitTimeoutNs);
-        if (pw == 3) sm100::mbar_wait_timeout(vfull, last, sm100::kWaitTimeoutNs);
+        if (pw == 0) {
+          sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
+          sm100::mbar_wait_timeout(&kfull[0], last, sm100::kWaitTimeoutNs);
+          sm100::mbar_wait_timeout(&kfull[2], last, sm100::kWaitTimeoutNs);
+        }
+        if (pw == 3) sm100::mbar_wait_timeout(&kfull[1], last, sm100::kWaitTimeoutNs);
+        if (pw >= 6) sm100::mbar_wait_timeout(&vfull[pw - 6], last, sm100::kWaitTimeoutNs);
       }
-    } else if (warp == 0 && leader) {
+    } else if (warp <= 1 && leader) {
       // ---------------------------------------------------------------- MMA
-      // The whole warp runs the issue loop (descriptors stay warp-uniform) and
-      // one elected lane issues each product's MMAs back to back.
+      // Warp 0 issues QK(i) group by group as its keys land (S buffer i % 2
+      // free), warp 1 issues PV(i) once P(i) is written, key half by key half
+      // as its values land; each commits its own MMAs. Each whole warp runs
+      // its loop (descriptors stay warp-uniform) and one elected lane issues.
       constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, 256) | (1u << 16);   // B (V) MN-major
-      const uint64_t d_q = desc_kmajor(smem_base + pr::kQOff);
-      const uint64_t d_k = desc_kmajor(smem_base + pr::kKOff);
-      const uint64_t d_p0 = desc_kmajor(smem_base + pr::kPOff);          // P keys 0..63
-      const uint64_t d_p1 = desc_kmajor(smem_base + pr::kPOff + 8192);   // P keys 64..127
-      const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
       auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
         return __all_sync(0xffffffffu, sm100::mbar_poll_cluster(bar, par, abort) ? 1 : 0) != 0;
       };
-      bool ok = wait_all(qbar, 0);
-      auto issue_qk = [&](int i) -> bool {
-        const int buf = i & 1;
-        const uint32_t par = (uint32_t)(i & 1);
-        if (!wait_all(&s_empty[buf], ((i >> 1) & 1) ^ 1u)) return false;
-        if (!wait_all(kfull, par)) return false;
-        sm100::tc_fence_after();
-        const uint32_t d = tmem + pr::kColS + buf * 64;
-        if (sm100::elect_one()) {
+      bool ok = true;
+      if (warp == 0) {
+        const uint64_t d_q = desc_kmajor(smem_base + pr::kQOff);
+        const uint64_t d_k = desc_kmajor(smem_base + pr::kKOff);
+        ok = wait_all(qbar, 0);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          const int buf = i & 1;
+          const uint32_t par = (uint32_t)(i & 1);
+          ok = wait_all(&s_empty[buf], ((i >> 1) & 1) ^ 1u);
+          const uint32_t d = tmem + pr::kColS + buf * 64;
+          for (int g = 0; g < pr::kKGroups && ok; ++g) {
+            ok = wait_all(&kfull[g], par);
+            if (!ok) break;
+            sm100::tc_fence_after();
+            if (sm100::elect_one()) {
 #pragma unroll 1
-          for (int c = 0; c < 9; ++c) {
-            const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
-            sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
+              for (int c = 3 * g; c < 3 * g + 3; ++c) {
+                const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
+                sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
-          }
-          sm100::tc_commit_pair_mc(kempty, 3);
-          sm100::tc_commit_pair_mc(&s_full[buf], 3);
-        }
-        __syncwarp();
-        return true;
-      };
-      auto issue_pv = [&](int i) -> bool {
-        const uint32_t par = (uint32_t)(i & 1);
-        if (!wait_all(p_full, par)) return false;
-        if (!wait_all(vfull, par)) return false;
-        sm100::tc_fence_after();
-        if (sm100::elect_one()) {
-#pragma unroll 1
-          for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
-                                        d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
-                                        (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
+              }
+              sm100::tc_commit_pair_mc(&kempty[g], 3);   // this group's K slots free once read
+              if (g == pr::kKGroups - 1) sm100::tc_commit_pair_mc(&s_full[buf], 3);
             }
+            __syncwarp();
           }
-          sm100::tc_commit_pair_mc(vempty, 3);
-          sm100::tc_commit_pair_mc(o_done, 3);
         }
-        __syncwarp();
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        ok = issue_pv(i);
-        if (ok && i + 1 < n_tiles) ok = issue_qk(i + 1);
+      } else {
+        const uint64_t d_p0 = desc_kmajor(smem_base + pr::kPOff);          // P keys 0..63
+        const uint64_t d_p1 = desc_kmajor(smem_base + pr::kPOff + 8192);   // P keys 64..127
+        const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+          const uint32_t par = (uint32_t)(i & 1);
+          ok = wait_all(p_full, par);
+          for (int kb = 0; kb < 2 && ok; ++kb) {
+            ok = wait_all(&vfull[kb], par);
+            if (!ok) break;
+            sm100::tc_fence_after();
+            if (sm100::elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
+                                          d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
+                                          (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+              }
+              sm100::tc_commit_pair_mc(&vempty[kb], 3);   // this key half's V slots free once read
+              if (kb == 1) sm100::tc_commit_pair_mc(o_done, 3);
+            }
+            __syncwarp();
+          }
+        }
       }
       if (!ok && lane == 0) {
         *abort = 1;
         raise_error(p.err, MTP_ERR_TIMEOUT);
       }
+      // Every MMA this warp issued has completed before TMEM is released:
+      // both issuers commit to the final barrier, warp 0 waits for both.
       if (sm100::elect_one()) sm100::tc_commit_pair_mc(final_bar, 3);
       __syncwarp();
-      sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
+      if (warp == 0) sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
     } else if (warp == 0 && lane == 0) {
       // odd CTA: the leader's MMAs write this CTA's TMEM; wait for the last one
       sm100::mbar_wait_timeout(final_bar, 0, sm100::kWaitTimeoutNs);
