@@ -663,8 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 // 147 KB and ~410 KB for one 64-row CTA on its own; the MMAs have N = 128/256.
 // The key tile is single-buffered, so the next tile's keys can only load into
 // chunks that QK has finished with: the nine K chunks land and are released
-// in three groups of three, and the eight V boxes in two key halves, so the
-// loads of tile i+1 start while QK(i) (and PV(i-1)) still run. Two warps
+// in three groups of three, and the eight V boxes in four quarters (key half
+// x dv half, PV's four quarters in turn), so the loads of tile i+1 start
+// while QK(i) and PV(i) still run. Two warps
 // issue the MMAs: one QK(i) as soon as its key groups land, the other PV(i)
 // as soon as P(i) is written, so QK(i+1) runs during the softmax of tile i
 // instead of waiting behind PV(i) (S is double-buffered; each issuing warp
@@ -681,7 +682,7 @@ constexpr int kPOff = kVOff + 8 * 8192;           // P [64 rows x 128 keys]: key
 constexpr int kRedOff = kPOff + 8192;             // red_max[8][64], red_sum[8][64] alias P keys 64..127
 constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, path [64] u32
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
-constexpr int kNumBars = 9 + 9 + 2 + 2 + 1 + 2 + 2 + 1 + 1 + 1;   // (kfull / kempty use 3 of their 9)
+constexpr int kNumBars = 3 + 3 + 4 + 4 + 1 + 2 + 2 + 1 + 1 + 1;
 constexpr int kKGroups = 3;                       // K chunks land and are released in groups of three
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -704,10 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   float* l_run = m_run + 256;
   uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 320);   // per row: path mask (tree) or key limit (chain)
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // [3] leader: both CTAs' K chunk group landed
-  uint64_t* kempty = kfull + 9;                                         // [3] both: the group's K slots are free
-  uint64_t* vfull = kempty + 9;                                         // [2] leader: both CTAs' V boxes of a key half
-  uint64_t* vempty = vfull + 2;                                         // [2] both: the key half's V slots are free
-  uint64_t* qbar = vempty + 2;                                          // leader: both CTAs' Q landed
+  uint64_t* kempty = kfull + 3;                                         // [3] both: the group's K slots are free
+  uint64_t* vfull = kempty + 3;                                         // [4] leader: both CTAs' V boxes of a quarter
+  uint64_t* vempty = vfull + 4;                                         // [4] both: the quarter's V slots are free
+  uint64_t* qbar = vempty + 4;                                          // leader: both CTAs' Q landed
   uint64_t* s_full = qbar + 1;                                          // [2] both
   uint64_t* s_empty = s_full + 2;                                       // [2] leader, one arrive per CTA
   uint64_t* p_full = s_empty + 2;                                       // leader, one arrive per CTA
@@ -738,9 +739,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       sm100::mbar_init(&kfull[g], 1);
       sm100::mbar_init(&kempty[g], 1);
     }
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 4; ++k) {
       sm100::mbar_init(&vfull[k], 1);
       sm100::mbar_init(&vempty[k], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
       sm100::mbar_init(&s_full[k], 1);
       sm100::mbar_init(&s_empty[k], 2);   // one arrive per CTA
     }
@@ -973,7 +976,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       // leader's barriers. Producers 0-5 own K chunk pw (and pw + 6 for
       // pw < 3), each waiting for its group's slots to be released by the
       // previous tile's QK; producers 6 and 7 own the V boxes of key half
-      // pw - 6, released by the previous tile's PV.
+      // pw - 6, quarter (key half, dv half h) by quarter, each released by
+      // the previous tile's PV.
       const uint64_t pol_kv = sm100::l2_policy_evict_last();
       const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
       auto block_of = [&](int key0) -> int {
@@ -994,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
           sm100::tma_load_2d_pair(smem + pr::kQOff + c * 8192, &tm_q, qbar, 0, c * 64, b * rows + row_base, pol_q);
       }
       constexpr int kGroupBytes = 2 * 3 * 8192;   // both CTAs' three K chunks
-      constexpr int kHalfBytes = 2 * 4 * 8192;    // both CTAs' four V boxes of a key half
+      constexpr int kQuarterBytes = 2 * 2 * 8192;   // both CTAs' two V boxes of a quarter
       bool ok = true;
       for (int i = 0; i < n_tiles && ok; ++i) {
         const uint32_t par = (uint32_t)((i & 1) ^ 1);
@@ -1010,17 +1014,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
           }
         } else {
           const int kb = pw - 6;
-          ok = sm100::mbar_wait_cluster(&vempty[kb], par, abort);
-          if (!ok) break;
-          if (leader) sm100::mbar_arrive_expect_tx(&vfull[kb], kHalfBytes);
           const int blk = block_of(t0 + i * kKeys + 64 * kb);
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h) {
+            const int q = kb * 2 + h;
+            ok = sm100::mbar_wait_cluster(&vempty[q], par, abort);
+            if (!ok) break;
+            if (leader) sm100::mbar_arrive_expect_tx(&vfull[q], kQuarterBytes);
             for (int j = 0; j < 2; ++j) {
               const int slot = (h * 2 + kb) * 2 + j;
               const int dchunk = 4 * h + 2 * (int)rank + j;
-              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[kb], 0, dchunk * 64, 0, blk,
+              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[q], 0, dchunk * 64, 0, blk,
                                       pol_kv);
             }
+          }
         }
       }
       if (!ok) {
@@ -1037,12 +1043,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
           sm100::mbar_wait_timeout(&kfull[2], last, sm100::kWaitTimeoutNs);
         }
         if (pw == 3) sm100::mbar_wait_timeout(&kfull[1], last, sm100::kWaitTimeoutNs);
-        if (pw >= 6) sm100::mbar_wait_timeout(&vfull[pw - 6], last, sm100::kWaitTimeoutNs);
+        if (pw >= 6)
+          for (int h = 0; h < 2; ++h) sm100::mbar_wait_timeout(&vfull[(pw - 6) * 2 + h], last, sm100::kWaitTimeoutNs);
       }
     } else if (warp <= 1 && leader) {
       // ---------------------------------------------------------------- MMA
       // Warp 0 issues QK(i) group by group as its keys land (S buffer i % 2
-      // free), warp 1 issues PV(i) once P(i) is written, key half by key half
+      // free), warp 1 issues PV(i) once P(i) is written, quarter by quarter
       // as its values land; each commits its own MMAs. Each whole warp runs
       // its loop (descriptors stay warp-uniform) and one elected lane issues.
       constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, 128);
@@ -1085,21 +1092,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
         for (int i = 0; i < n_tiles && ok; ++i) {
           const uint32_t par = (uint32_t)(i & 1);
           ok = wait_all(p_full, par);
-          for (int kb = 0; kb < 2 && ok; ++kb) {
-            ok = wait_all(&vfull[kb], par);
+          for (int q = 0; q < 4 && ok; ++q) {   // quarter (key half kb, dv half h) = O columns of h over kb's keys
+            const int kb = q >> 1, h = q & 1;
+            ok = wait_all(&vfull[q], par);
             if (!ok) break;
             sm100::tc_fence_after();
             if (sm100::elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                  sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
-                                          d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
-                                          (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
-              }
-              sm100::tc_commit_pair_mc(&vempty[kb], 3);   // this key half's V slots free once read
-              if (kb == 1) sm100::tc_commit_pair_mc(o_done, 3);
+              for (int kk = 0; kk < 4; ++kk)
+                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
+                                        d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
+                                        (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+              sm100::tc_commit_pair_mc(&vempty[q], 3);   // this quarter's V slots free once read
+              if (q == 3) sm100::tc_commit_pair_mc(o_done, 3);
             }
             __syncwarp();
           }
