@@ -38,6 +38,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -95,6 +96,7 @@ struct Params {
   int B, R, Hq, max_blocks, num_blocks, split_len, n_splits;
   int groups;           // work groups per request: row blocks (single CTA) or row-block pairs (CTA pairs)
   int cluster;          // CTAs per work group: 1, or 2 for the CTA-pair kernel
+  int n_items;          // work items in the order (the persistent CTA-pair kernel walks them)
   float scale_log2;
 };
 
@@ -116,7 +118,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 __device__ __forceinline__ void softmax_barrier() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-// Named barrier 1 over the 256 softmax threads that also returns whether any
+// Named barrier 1 over the 512 softmax threads that also returns whether any
 // of them passed true.
 __device__ __forceinline__ bool softmax_barrier_any(bool v) {
   uint32_t r;
@@ -680,10 +682,12 @@ constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]
 constexpr int kVOff = kKOff + 9 * 8192;           // 8 x [64 keys x 64 dv]: slot (h * 2 + kb) * 2 + j
 constexpr int kPOff = kVOff + 8 * 8192;           // P [64 rows x 128 keys]: keys 0..63, then 64..127
 constexpr int kRedOff = kPOff + 8192;             // red_max[8][64], red_sum[8][64] alias P keys 64..127
-constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32, path [64] u32
+constexpr int kRowOff = kPOff + 2 * 8192;         // m_run, m_ref, rscale, m_shift, l_run [64] f32 (+ 64 spare)
 constexpr int kBarOff = kRowOff + 6 * 64 * 4;
-constexpr int kNumBars = 3 + 3 + 4 + 4 + 1 + 2 + 2 + 1 + 1 + 1;
-constexpr int kKGroups = 3;                       // K chunks land and are released in groups of three
+constexpr int kKGroups = 3;                       // the nine K chunks land and are released in this many groups
+constexpr int kKPerGroup = 9 / kKGroups;
+static_assert(kKGroups * kKPerGroup == 9, "K groups must split the nine chunks evenly");
+constexpr int kNumBars = 2 * kKGroups + 4 + 4 + 2 + 2 + 2 + 1 + 1 + 1 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 constexpr uint32_t kColO = 0;                     // O of product h at columns 128 h .. +127
@@ -703,36 +707,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   float* rscale = m_run + 128;
   float* m_shift = m_run + 192;
   float* l_run = m_run + 256;
-  uint32_t* path = reinterpret_cast<uint32_t*>(m_run + 320);   // per row: path mask (tree) or key limit (chain)
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + pr::kBarOff);   // [3] leader: both CTAs' K chunk group landed
-  uint64_t* kempty = kfull + 3;                                         // [3] both: the group's K slots are free
-  uint64_t* vfull = kempty + 3;                                         // [4] leader: both CTAs' V boxes of a quarter
+  uint64_t* kempty = kfull + pr::kKGroups;                              // [3] both: the group's K slots are free
+  uint64_t* vfull = kempty + pr::kKGroups;                              // [4] leader: both CTAs' V boxes of a quarter
   uint64_t* vempty = vfull + 4;                                         // [4] both: the quarter's V slots are free
-  uint64_t* qbar = vempty + 4;                                          // leader: both CTAs' Q landed
-  uint64_t* s_full = qbar + 1;                                          // [2] both
+  uint64_t* qbar = vempty + 4;                                          // leader: both CTAs' Q of an item landed
+  uint64_t* qempty = qbar + 1;                                          // both: an item's last QK read Q
+  uint64_t* s_full = qempty + 1;                                        // [2] both
   uint64_t* s_empty = s_full + 2;                                       // [2] leader, one arrive per CTA
   uint64_t* p_full = s_empty + 2;                                       // leader, one arrive per CTA
   uint64_t* o_done = p_full + 1;                                        // both
-  uint64_t* final_bar = o_done + 1;                                     // both
+  uint64_t* o_free = o_done + 1;                                        // leader, one arrive per CTA: O read out
+  uint64_t* final_bar = o_free + 1;                                     // both
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pr::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + pr::kMiscOff + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = sm100::cluster_ctarank();
   const bool leader = rank == 0;
-  const Item item = decode_item(p.order[blockIdx.x / 2], p.B, p.groups);
-  const int split = item.split, b = item.b;
   const int rows = p.R * p.Hq;
-  const int row_base = (item.g * 2 + (int)rank) * kRows;
-  const int ctx = p.ctx_lens[b];
-  if (ctx < 0 || ctx + p.R > p.max_blocks * kBlock) {   // uniform over the pair (same request)
-    if (threadIdx.x == 0 && split == 0 && row_base == 0) raise_error(p.err, MTP_ERR_LENGTH);
-    return;
-  }
-  const int t0 = split * p.split_len;
-  const int t_end = item_key_end(item, ctx, p.R, p.Hq, rows, 2, p.split_len);
-  if (t0 >= t_end) return;
-  const int n_tiles = (t_end - t0 + kKeys - 1) / kKeys;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  // The pair's work items: round k takes order slot k * n_pairs + pair, or
+  // its mirror image for odd k, so the longest items (first in the order)
+  // share a pair with the shortest ones. Every role walks the same list.
+  struct Work {
+    int split, b, row_base, ctx, t0, t_end, n_tiles;
+    bool bad_len;
+  };
+  auto work = [&](int k, Work& w) -> bool {
+    const int slot = k * n_pairs + ((k & 1) ? n_pairs - 1 - pair : pair);
+    if (slot >= p.n_items) return false;
+    const Item it = decode_item(p.order[slot], p.B, p.groups);
+    w.split = it.split;
+    w.b = it.b;
+    w.row_base = (it.g * 2 + (int)rank) * kRows;
+    w.ctx = p.ctx_lens[it.b];
+    w.t0 = it.split * p.split_len;
+    w.t_end = w.t0;
+    w.n_tiles = 0;
+    w.bad_len = w.ctx < 0 || w.ctx + p.R > p.max_blocks * kBlock;   // uniform over the pair (same request)
+    if (!w.bad_len) {
+      w.t_end = item_key_end(it, w.ctx, p.R, p.Hq, rows, 2, p.split_len);
+      if (w.t0 < w.t_end) w.n_tiles = (w.t_end - w.t0 + kKeys - 1) / kKeys;
+    }
+    return true;
+  };
 
   if (threadIdx.x == 0) {
     for (int g = 0; g < pr::kKGroups; ++g) {
@@ -748,8 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       sm100::mbar_init(&s_empty[k], 2);   // one arrive per CTA
     }
     sm100::mbar_init(qbar, 1);
+    sm100::mbar_init(qempty, 1);
     sm100::mbar_init(p_full, 2);
     sm100::mbar_init(o_done, 1);
+    sm100::mbar_init(o_free, 2);
     sm100::mbar_init(final_bar, 2);   // the QK and the PV issuer each commit once at the end
     *abort = 0;
     sm100::fence_barrier_init();
@@ -757,12 +779,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
   if (warp == 0) {
     sm100::tmem_alloc_pair(tmem_slot, kTmemCols);
     sm100::tmem_relinquish_pair();
-  }
-  if (threadIdx.x < kRows) {
-    const int rr = min(row_base + (int)threadIdx.x, rows - 1);
-    path[threadIdx.x] = kTree ? tree_path_mask(p.parents, b, p.R, rr / p.Hq, p.err) : (uint32_t)(ctx + rr / p.Hq);
-    m_run[threadIdx.x] = -INFINITY;
-    m_ref[threadIdx.x] = 0.0f;
   }
   sm100::tc_fence_before();
   __syncthreads();
@@ -782,182 +798,247 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
     const int part = khalf * 4 + sub;                 // which of the row's 8 partials this thread holds
     const int st = sw * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q) << 16;
-    const uint32_t path_r = path[r];
-    const int mask_from = kTree ? ctx : ctx + row_base / p.Hq + 1;   // first key some row may not see
-    float acc = 0.0f;                                 // partial row sum over this thread's keys
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int buf = i & 1;
-      ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(&s_full[buf], (i >> 1) & 1, abort) ? 1 : 0);
-      float d[16];
-      const float mr = m_ref[r];
-      if (ok) {
-        sm100::tc_fence_after();
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColS + buf * 64 + sub * 16, v);
-        sm100::tmem_ld_wait();
-#pragma unroll
-        for (int x = 0; x < 16; ++x) d[x] = fmaf(__uint_as_float(v[x]), p.scale_log2, -mr);
-        sm100::tc_fence_before();
-      } else {
-#pragma unroll
-        for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
+    int T = 0;                                        // tiles of this pair before the current item
+    Work w, wn;
+    bool has = work(0, w);
+    for (int k = 0; has; ++k, w = wn) {
+      has = work(k + 1, wn);   // the next item's record loads while this one runs
+      if (w.n_tiles == 0) {
+        if (w.bad_len && st == 0 && w.split == 0 && w.row_base == 0) raise_error(p.err, MTP_ERR_LENGTH);
+        continue;
       }
-      const int tile0 = t0 + i * kKeys;
-      if (tile0 + kKeys - 1 >= mask_from || tile0 + kKeys > t_end) {   // causal / split edge inside the tile
-        const int key0 = tile0 + 64 * khalf + 16 * sub;
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          d[x] = (key0 + x >= t_end || (kTree ? tree_hidden(key0 + x, ctx, path_r) : key0 + x > (int)path_r))
-                     ? -INFINITY
-                     : d[x];
+      const int rr0 = min(w.row_base + r, rows - 1);
+      const uint32_t path_r = kTree ? tree_path_mask(p.parents, w.b, p.R, rr0 / p.Hq, p.err)
+                                    : (uint32_t)(w.ctx + rr0 / p.Hq);   // root-path mask, or the key limit
+      const int mask_from = kTree ? w.ctx : w.ctx + w.row_base / p.Hq + 1;   // first key some row may not see
+      if (st < kRows) {
+        m_run[st] = -INFINITY;
+        m_ref[st] = 0.0f;
       }
-      bool exceed = (i == 0);
-#pragma unroll
-      for (int x = 0; x < 16; ++x) exceed |= d[x] > kLazyRescale;
-      const bool any_exceed = softmax_barrier_any(exceed);
-      // every softmax warp of this CTA has read S(i) from TMEM: one arrive
-      if (st == 0) sm100::mbar_arrive_remote_relaxed(&s_empty[buf], 0);
-      // PV(i-1) reads P (which the reduction scratch shares) and accumulates
-      // into O, and may still run (QK(i) does not wait for it): the O rescale
-      // and the P stores wait for its completion. (The softmax of tile i-1
-      // waited for PV(i-2), so the parity cannot alias an older phase.)
-      bool pv_done = i == 0;
-      auto wait_pv = [&]() {
-        if (!pv_done) {
-          ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (i - 1) & 1, abort) ? 1 : 0);
+      softmax_barrier();
+      float acc = 0.0f;                               // partial row sum over this thread's keys
+      for (int i = 0; i < w.n_tiles; ++i) {
+        const int ti = T + i;                         // the pair's tile counter sets the barrier phases
+        const int buf = ti & 1;
+        ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(&s_full[buf], (ti >> 1) & 1, abort) ? 1 : 0);
+        float d[16];
+        const float mr = m_ref[r];
+        if (ok) {
           sm100::tc_fence_after();
-          pv_done = true;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColS + buf * 64 + sub * 16, v);
+          sm100::tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) d[x] = fmaf(__uint_as_float(v[x]), p.scale_log2, -mr);
+          sm100::tc_fence_before();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) d[x] = -INFINITY;
         }
-      };
-      if (any_exceed) {
-        wait_pv();
-        float mx = d[0];
+        const int tile0 = w.t0 + i * kKeys;
+        if (tile0 + kKeys - 1 >= mask_from || tile0 + kKeys > w.t_end) {   // causal / split edge inside the tile
+          const int key0 = tile0 + 64 * khalf + 16 * sub;
 #pragma unroll
-        for (int x = 1; x < 16; ++x) mx = fmaxf(mx, d[x]);
-        red_max[part * 64 + r] = mx + mr;
-        softmax_barrier();
-        if (st < kRows) {
-          float mt = red_max[st];
+          for (int x = 0; x < 16; ++x)
+            d[x] = (key0 + x >= w.t_end || (kTree ? tree_hidden(key0 + x, w.ctx, path_r) : key0 + x > (int)path_r))
+                       ? -INFINITY
+                       : d[x];
+        }
+        bool exceed = (i == 0);
 #pragma unroll
-          for (int k = 1; k < 8; ++k) mt = fmaxf(mt, red_max[k * 64 + st]);
-          const float mo = m_run[st];
-          float mn = mo, sc = 1.0f;
-          if (mt > mo + kLazyRescale) {
-            mn = mt;
-            sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+        for (int x = 0; x < 16; ++x) exceed |= d[x] > kLazyRescale;
+        const bool any_exceed = softmax_barrier_any(exceed);
+        // every softmax warp of this CTA has read S from TMEM: one arrive
+        if (st == 0) sm100::mbar_arrive_remote_relaxed(&s_empty[buf], 0);
+        // The previous PV reads P (which the reduction scratch shares) and
+        // accumulates into O, and may still run (QK does not wait for it): the
+        // O rescale and the P stores wait for its completion. (The softmax of
+        // the previous tile waited for the PV before it, so the parity cannot
+        // alias an older phase; before an item's first tile the previous
+        // item's epilogue has already waited for its last PV.)
+        bool pv_done = i == 0;
+        auto wait_pv = [&]() {
+          if (!pv_done) {
+            ok = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (ti - 1) & 1, abort) ? 1 : 0);
+            sm100::tc_fence_after();
+            pv_done = true;
           }
-          m_run[st] = mn;
-          const float ref = mn == -INFINITY ? 0.0f : mn;   // rows with no visible key yet: p = 2^-inf = 0
-          m_shift[st] = m_ref[st] - ref;
-          m_ref[st] = ref;
-          rscale[st] = sc;
-        }
-        softmax_barrier();
-        const float sc = rscale[r];
-        acc *= sc;
-        const float sh = m_shift[r];
+        };
+        if (any_exceed) {
+          wait_pv();
+          float mx = d[0];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) d[x] += sh;
-        // O of these rows holds PV up to tile i-1 (complete): rescale it. This
-        // warp owns 64 of the 256 O columns of its TMEM lanes.
-        if (ok && i > 0 && __any_sync(0xffffffffu, sc != 1.0f)) {
-          const int h = sub >> 1, c0 = (sub & 1) * 64;
+          for (int x = 1; x < 16; ++x) mx = fmaxf(mx, d[x]);
+          red_max[part * 64 + r] = mx + mr;
+          softmax_barrier();
+          if (st < kRows) {
+            float mt = red_max[st];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) mt = fmaxf(mt, red_max[j * 64 + st]);
+            const float mo = m_run[st];
+            float mn = mo, sc = 1.0f;
+            if (mt > mo + kLazyRescale) {
+              mn = mt;
+              sc = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
+            }
+            m_run[st] = mn;
+            const float ref = mn == -INFINITY ? 0.0f : mn;   // rows with no visible key yet: p = 2^-inf = 0
+            m_shift[st] = m_ref[st] - ref;
+            m_ref[st] = ref;
+            rscale[st] = sc;
+          }
+          softmax_barrier();
+          const float sc = rscale[r];
+          acc *= sc;
+          const float sh = m_shift[r];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) d[x] += sh;
+          // O of these rows holds PV up to the previous tile (complete): rescale
+          // it. This warp owns 64 of the 256 O columns of its TMEM lanes.
+          if (ok && i > 0 && __any_sync(0xffffffffu, sc != 1.0f)) {
+            const int h = sub >> 1, c0 = (sub & 1) * 64;
+#pragma unroll 1
+            for (int t = 0; t < 4; ++t) {
+              uint32_t v[16];
+              const uint32_t ta = tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16;
+              tmem_ld_32x32b_x16(ta, v);
+              sm100::tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 16; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * sc);
+              tmem_st_32x32b_x16(ta, v);
+            }
+            tmem_st_wait();
+          }
+        }
+        // p = 2^d into P [64 rows x 128 keys] (K-major A operand of PV, two
+        // 64-key blocks) and into the partial row sum, once the previous PV is
+        // complete (no thread reads red_max any more, which shares the second
+        // block).
+        {
+          uint8_t* pb = smem + pr::kPOff + khalf * 8192 + r * 128;
+          uint32_t wv[8];
+#pragma unroll
+          for (int x = 0; x < 16; x += 2) {
+            const float p0 = fast_exp2(d[x]), p1 = fast_exp2(d[x + 1]);
+            acc += p0 + p1;
+            wv[x / 2] = pack_bf16x2(p0, p1);
+          }
+          wait_pv();
+          const int ch = 2 * sub;   // 16-byte chunks 2 sub, 2 sub + 1 of the row
+          *reinterpret_cast<uint4*>(pb + (((ch) ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(pb + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        }
+        // Every writer makes its P stores visible to the async proxy, then the
+        // named barrier orders all of them before the one arrive; a release at
+        // cluster scope would add about a microsecond here (measured) without
+        // ordering anything the fence and the barrier have not.
+        fence_async_smem();
+        sm100::tc_fence_before();
+        softmax_barrier();   // all of this CTA's P is written
+        if (st == 0 && ok) sm100::mbar_arrive_remote_relaxed(p_full, 0);
+      }
+      // ------------------------------------------------------ epilogue
+      // The item's last PV is complete (so P, which red_sum shares, is free).
+      const bool done_w = ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (T + w.n_tiles - 1) & 1,
+                                                                                  abort) ? 1 : 0);
+      const bool done = !softmax_barrier_any(!done_w);   // uniform: the stores below use named barriers
+      red_sum[part * 64 + r] = acc;
+      softmax_barrier();
+      if (st < kRows) {
+        float l = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l += red_sum[j * 64 + st];
+        l_run[st] = l;
+      }
+      softmax_barrier();
+      if (done) {
+        sm100::tc_fence_after();
+        const int h = sub >> 1, c0 = (sub & 1) * 64;
+        const int rr = w.row_base + r;
+        const float l = l_run[r];
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const int dv0 = 256 * h + 128 * khalf + c0;     // this thread's TMEM lane 32 q + lane: dv half q / 2
+        if (p.n_splits == 1) {
+          // Each thread holds one 128-byte block of its row (64 dv, block
+          // dv0 / 64). A thread writing its own row would touch 32 lines per
+          // store instruction; instead two blocks of every row at a time go
+          // through the P buffer (free now; 16-byte granule g of row r at
+          // g ^ (r & 7), conflict-free both ways) and leave as whole lines.
+          uint8_t* stage = smem + pr::kPOff;   // [64 rows][256 B]
+          const int blk = dv0 >> 6;
+          // The thread's 64 values, normalised and packed to bf16 pairs (two
+          // TMEM loads in flight per wait).
+          uint32_t pk[32];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v0[16], v1[16];
+            tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColO + h * 128 + c0 + hh * 32, v0);
+            tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColO + h * 128 + c0 + hh * 32 + 16, v1);
+            sm100::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; x += 2) {
+              pk[hh * 16 + x / 2] = pack_bf16x2(__uint_as_float(v0[x]) * inv, __uint_as_float(v0[x + 1]) * inv);
+              pk[hh * 16 + 8 + x / 2] = pack_bf16x2(__uint_as_float(v1[x]) * inv, __uint_as_float(v1[x + 1]) * inv);
+            }
+          }
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {   // dv blocks 2j, 2j + 1 of every row
+            if ((blk >> 1) == j) {
+              uint8_t* row = stage + r * 256;
+#pragma unroll
+              for (int gg = 0; gg < 8; ++gg) {   // 16-byte granules (blk & 1) * 8 + gg of the row's 256 B
+                const int g = (blk & 1) * 8 + gg;
+                *reinterpret_cast<uint4*>(row + ((g ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * gg], pk[4 * gg + 1], pk[4 * gg + 2], pk[4 * gg + 3]);
+              }
+            }
+            softmax_barrier();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {   // 1024 granules: 16 per row, consecutive threads along a row
+              const int G = st + 512 * u;
+              const int row = G >> 4, g = G & 15;
+              if (w.row_base + row < rows) {
+                const uint4 val = *reinterpret_cast<const uint4*>(stage + row * 256 + ((g ^ (row & 7)) << 4));
+                const int64_t orow = (int64_t)w.b * rows + w.row_base + row;
+                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.out + orow * kDV + 128 * j) + g * 16) = val;
+              }
+            }
+            softmax_barrier();
+          }
+        } else {
 #pragma unroll 1
           for (int t = 0; t < 4; ++t) {
             uint32_t v[16];
-            const uint32_t ta = tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16;
-            tmem_ld_32x32b_x16(ta, v);
+            tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16, v);
             sm100::tmem_ld_wait();
+            if (rr < rows) {
+              const int64_t orow = (int64_t)w.b * rows + rr;
+              float* dst = p.part_o + (orow * p.n_splits + w.split) * kDV + dv0 + t * 16;
 #pragma unroll
-            for (int x = 0; x < 16; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * sc);
-            tmem_st_32x32b_x16(ta, v);
+              for (int x = 0; x < 16; x += 4)
+                *reinterpret_cast<float4*>(dst + x) =
+                    make_float4(__uint_as_float(v[x]) * inv, __uint_as_float(v[x + 1]) * inv,
+                                __uint_as_float(v[x + 2]) * inv, __uint_as_float(v[x + 3]) * inv);
+            }
           }
-          tmem_st_wait();
+        }
+        if (p.n_splits > 1 && st < kRows && w.row_base + st < rows) {
+          const float l2 = l_run[st];
+          const int64_t orow = (int64_t)w.b * rows + w.row_base + st;
+          p.part_lse[orow * p.n_splits + w.split] = l2 > 0.0f ? (m_run[st] + log2f(l2)) * kLn2 : -INFINITY;
         }
       }
-      // p = 2^d into P [64 rows x 128 keys] (K-major A operand of PV, two
-      // 64-key blocks) and into the partial row sum, once PV(i-1) is complete
-      // (no thread reads red_max any more, which shares the second block).
-      {
-        uint8_t* pb = smem + pr::kPOff + khalf * 8192 + r * 128;
-        uint32_t w[8];
-#pragma unroll
-        for (int x = 0; x < 16; x += 2) {
-          const float p0 = fast_exp2(d[x]), p1 = fast_exp2(d[x + 1]);
-          acc += p0 + p1;
-          w[x / 2] = pack_bf16x2(p0, p1);
-        }
-        wait_pv();
-        const int ch = 2 * sub;   // 16-byte chunks 2 sub, 2 sub + 1 of the row
-        *reinterpret_cast<uint4*>(pb + (((ch) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(pb + (((ch + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-      // Every writer makes its P stores visible to the async proxy, then the
-      // named barrier orders all of them before the one arrive; a release at
-      // cluster scope would add about a microsecond here (measured) without
-      // ordering anything the fence and the barrier have not.
-      fence_async_smem();
+      // O is read out (and the row state is free): the PV warp may start the
+      // pair's next item, which overwrites O.
       sm100::tc_fence_before();
-      softmax_barrier();   // all of this CTA's P is written
-      if (st == 0 && ok) sm100::mbar_arrive_remote_relaxed(p_full, 0);
+      softmax_barrier();
+      if (st == 0 && ok) sm100::mbar_arrive_remote_relaxed(o_free, 0);
+      T += w.n_tiles;
     }
     if (!ok && lane == 0) {
       *abort = 1;
       raise_error(p.err, MTP_ERR_TIMEOUT);
-    }
-    // -------------------------------------------------------- epilogue
-    // The last PV is complete (so P, which red_sum shares, is free).
-    const bool done =
-        ok && __all_sync(0xffffffffu, sm100::mbar_wait_cluster(o_done, (n_tiles - 1) & 1, abort) ? 1 : 0);
-    softmax_barrier();
-    red_sum[part * 64 + r] = acc;
-    softmax_barrier();
-    if (st < kRows) {
-      float l = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) l += red_sum[k * 64 + st];
-      l_run[st] = l;
-    }
-    softmax_barrier();
-    if (done) {
-      sm100::tc_fence_after();
-      const int h = sub >> 1, c0 = (sub & 1) * 64;
-      const int rr = row_base + r;
-      const float l = l_run[r];
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      const int dv0 = 256 * h + 128 * khalf + c0;     // this thread's TMEM lane 32 q + lane: dv half q / 2
-#pragma unroll 1
-      for (int t = 0; t < 4; ++t) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_addr + pr::kColO + h * 128 + c0 + t * 16, v);
-        sm100::tmem_ld_wait();
-        if (rr < rows) {
-          const int64_t orow = (int64_t)b * rows + rr;
-          const int dv = dv0 + t * 16;
-          if (p.n_splits == 1) {
-            uint32_t w[8];
-#pragma unroll
-            for (int x = 0; x < 16; x += 2)
-              w[x / 2] = pack_bf16x2(__uint_as_float(v[x]) * inv, __uint_as_float(v[x + 1]) * inv);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDV + dv);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            float* dst = p.part_o + (orow * p.n_splits + split) * kDV + dv;
-#pragma unroll
-            for (int x = 0; x < 16; x += 4)
-              *reinterpret_cast<float4*>(dst + x) =
-                  make_float4(__uint_as_float(v[x]) * inv, __uint_as_float(v[x + 1]) * inv,
-                              __uint_as_float(v[x + 2]) * inv, __uint_as_float(v[x + 3]) * inv);
-          }
-        }
-      }
-      if (p.n_splits > 1 && st < kRows && row_base + st < rows) {
-        const float l2 = l_run[st];
-        const int64_t orow = (int64_t)b * rows + row_base + st;
-        p.part_lse[orow * p.n_splits + split] = l2 > 0.0f ? (m_run[st] + log2f(l2)) * kLn2 : -INFINITY;
-      }
     }
   };
 
@@ -977,57 +1058,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       // pw < 3), each waiting for its group's slots to be released by the
       // previous tile's QK; producers 6 and 7 own the V boxes of key half
       // pw - 6, quarter (key half, dv half h) by quarter, each released by
-      // the previous tile's PV.
+      // the previous tile's PV. Producer 0 also loads each item's Q once the
+      // previous item's last QK has read the Q buffer, so the next item's
+      // loads overlap the end of the current one.
       const uint64_t pol_kv = sm100::l2_policy_evict_last();
-      const int32_t* tbl = p.block_table + (int64_t)b * p.max_blocks;
-      auto block_of = [&](int key0) -> int {
-        if (key0 >= t_end) return -1;
-        const int blk = tbl[key0 / kBlock];
-        if (blk < 0 || blk >= p.num_blocks) {
-          raise_error(p.err, MTP_ERR_BLOCK_ID);
-          return -1;
-        }
-        return blk;
-      };
+      const uint64_t pol_q = sm100::l2_policy_evict_first();
       if (pw == 0) {
         sm100::tma_prefetch_desc(&tm_q);
         sm100::tma_prefetch_desc(&tm_kv);
-        if (leader) sm100::mbar_arrive_expect_tx(qbar, 2 * kQChunks * 8192);
-        const uint64_t pol_q = sm100::l2_policy_evict_first();
-        for (int c = 0; c < kQChunks; ++c)   // both CTAs' Q complete on the leader's barrier
-          sm100::tma_load_2d_pair(smem + pr::kQOff + c * 8192, &tm_q, qbar, 0, c * 64, b * rows + row_base, pol_q);
       }
-      constexpr int kGroupBytes = 2 * 3 * 8192;   // both CTAs' three K chunks
-      constexpr int kQuarterBytes = 2 * 2 * 8192;   // both CTAs' two V boxes of a quarter
+      constexpr int kGroupBytes = 2 * pr::kKPerGroup * 8192;   // both CTAs' K chunks of a group
+      constexpr int kQuarterBytes = 2 * 2 * 8192;              // both CTAs' two V boxes of a quarter
       bool ok = true;
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const uint32_t par = (uint32_t)((i & 1) ^ 1);
-        if (pw < 6) {
-          const int own_key0 = t0 + i * kKeys + 64 * (int)rank;
-          const int blk = block_of(own_key0);
-          for (int c = pw; c < 9; c += 6) {   // chunk pw, then pw + 6 (group 2) for pw < 3
-            const int g = c / 3;
-            ok = sm100::mbar_wait_cluster(&kempty[g], par, abort);
-            if (!ok) break;
-            if (leader && c % 3 == 0) sm100::mbar_arrive_expect_tx(&kfull[g], kGroupBytes);
-            sm100::tma_load_3d_pair(smem + pr::kKOff + c * 8192, &tm_kv, &kfull[g], 0, c * 64, 0, blk, pol_kv);
+      int T = 0, kq = 0;   // tiles and items with tiles so far
+      Work w;
+      for (int k = 0; ok && work(k, w); ++k) {
+        if (w.n_tiles == 0) continue;
+        const int32_t* tbl = p.block_table + (int64_t)w.b * p.max_blocks;
+        auto block_of = [&](int key0) -> int {
+          if (key0 >= w.t_end) return -1;
+          const int blk = tbl[key0 / kBlock];
+          if (blk < 0 || blk >= p.num_blocks) {
+            raise_error(p.err, MTP_ERR_BLOCK_ID);
+            return -1;
           }
-        } else {
-          const int kb = pw - 6;
-          const int blk = block_of(t0 + i * kKeys + 64 * kb);
-          for (int h = 0; h < 2; ++h) {
-            const int q = kb * 2 + h;
-            ok = sm100::mbar_wait_cluster(&vempty[q], par, abort);
-            if (!ok) break;
-            if (leader) sm100::mbar_arrive_expect_tx(&vfull[q], kQuarterBytes);
-            for (int j = 0; j < 2; ++j) {
-              const int slot = (h * 2 + kb) * 2 + j;
-              const int dchunk = 4 * h + 2 * (int)rank + j;
-              sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[q], 0, dchunk * 64, 0, blk,
-                                      pol_kv);
+          return blk;
+        };
+        if (pw == 0) {
+          if (kq > 0) ok = sm100::mbar_wait_cluster(qempty, (uint32_t)((kq - 1) & 1), abort);
+          if (!ok) break;
+          if (leader) sm100::mbar_arrive_expect_tx(qbar, 2 * kQChunks * 8192);
+          for (int c = 0; c < kQChunks; ++c)   // both CTAs' Q complete on the leader's barrier
+            sm100::tma_load_2d_pair(smem + pr::kQOff + c * 8192, &tm_q, qbar, 0, c * 64, w.b * rows + w.row_base,
+                                    pol_q);
+        }
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+          const int ti = T + i;
+          const uint32_t par = (uint32_t)((ti & 1) ^ 1);
+          if (pw < 6) {
+            const int blk = block_of(w.t0 + i * kKeys + 64 * (int)rank);
+            for (int c = pw; c < 9; c += 6) {   // chunk pw, then pw + 6 (group 2) for pw < 3
+              const int g = c / pr::kKPerGroup;
+              ok = sm100::mbar_wait_cluster(&kempty[g], par, abort);
+              if (!ok) break;
+              if (leader && c % pr::kKPerGroup == 0) sm100::mbar_arrive_expect_tx(&kfull[g], kGroupBytes);
+              sm100::tma_load_3d_pair(smem + pr::kKOff + c * 8192, &tm_kv, &kfull[g], 0, c * 64, 0, blk, pol_kv);
+            }
+          } else {
+            const int kb = pw - 6;
+            const int blk = block_of(w.t0 + i * kKeys + 64 * kb);
+            for (int h = 0; h < 2; ++h) {
+              const int qq = kb * 2 + h;
+              ok = sm100::mbar_wait_cluster(&vempty[qq], par, abort);
+              if (!ok) break;
+              if (leader) sm100::mbar_arrive_expect_tx(&vfull[qq], kQuarterBytes);
+              for (int j = 0; j < 2; ++j) {
+                const int slot = (h * 2 + kb) * 2 + j;
+                const int dchunk = 4 * h + 2 * (int)rank + j;
+                sm100::tma_load_3d_pair(smem + pr::kVOff + slot * 8192, &tm_kv, &vfull[qq], 0, dchunk * 64, 0, blk,
+                                        pol_kv);
+              }
             }
           }
         }
+        T += w.n_tiles;
+        ++kq;
       }
       if (!ok) {
         *abort = 1;
@@ -1035,79 +1130,100 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
       }
       // The leader's producers wait (time-limited) for the last fill of each
       // barrier they armed; the odd CTA's copies complete on those barriers.
-      if (leader) {
-        const uint32_t last = (uint32_t)((n_tiles - 1) & 1);
-        if (pw == 0) {
-          sm100::mbar_wait_timeout(qbar, 0, sm100::kWaitTimeoutNs);
-          sm100::mbar_wait_timeout(&kfull[0], last, sm100::kWaitTimeoutNs);
-          sm100::mbar_wait_timeout(&kfull[2], last, sm100::kWaitTimeoutNs);
-        }
-        if (pw == 3) sm100::mbar_wait_timeout(&kfull[1], last, sm100::kWaitTimeoutNs);
+      if (leader && T > 0) {
+        const uint32_t last = (uint32_t)((T - 1) & 1);
+        if (pw == 0) sm100::mbar_wait_timeout(qbar, (uint32_t)((kq - 1) & 1), sm100::kWaitTimeoutNs);
+        if (pw < 6)
+          for (int c = pw; c < 9; c += 6)   // the groups this producer armed
+            if (c % pr::kKPerGroup == 0)
+              sm100::mbar_wait_timeout(&kfull[c / pr::kKPerGroup], last, sm100::kWaitTimeoutNs);
         if (pw >= 6)
           for (int h = 0; h < 2; ++h) sm100::mbar_wait_timeout(&vfull[(pw - 6) * 2 + h], last, sm100::kWaitTimeoutNs);
       }
     } else if (warp <= 1 && leader) {
       // ---------------------------------------------------------------- MMA
-      // Warp 0 issues QK(i) group by group as its keys land (S buffer i % 2
-      // free), warp 1 issues PV(i) once P(i) is written, quarter by quarter
-      // as its values land; each commits its own MMAs. Each whole warp runs
-      // its loop (descriptors stay warp-uniform) and one elected lane issues.
+      // Warp 0 issues QK group by group as its keys land (S buffer free),
+      // warp 1 issues PV once P is written, quarter by quarter as its values
+      // land (and, for an item's first tile, once the previous item's O has
+      // been read out); each commits its own MMAs. Each whole warp runs its
+      // loop (descriptors stay warp-uniform) and one elected lane issues.
       constexpr uint32_t idesc_qk = sm100::idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_pv = sm100::idesc_bf16_f32(128, 256) | (1u << 16);   // B (V) MN-major
       auto wait_all = [&](uint64_t* bar, uint32_t par) -> bool {
         return __all_sync(0xffffffffu, sm100::mbar_poll_cluster(bar, par, abort) ? 1 : 0) != 0;
       };
       bool ok = true;
+      int T = 0, kq = 0;
+      Work w;
       if (warp == 0) {
         const uint64_t d_q = desc_kmajor(smem_base + pr::kQOff);
         const uint64_t d_k = desc_kmajor(smem_base + pr::kKOff);
-        ok = wait_all(qbar, 0);
-        for (int i = 0; i < n_tiles && ok; ++i) {
-          const int buf = i & 1;
-          const uint32_t par = (uint32_t)(i & 1);
-          ok = wait_all(&s_empty[buf], ((i >> 1) & 1) ^ 1u);
-          const uint32_t d = tmem + pr::kColS + buf * 64;
-          for (int g = 0; g < pr::kKGroups && ok; ++g) {
-            ok = wait_all(&kfull[g], par);
-            if (!ok) break;
-            sm100::tc_fence_after();
-            if (sm100::elect_one()) {
+        for (int k = 0; ok && work(k, w); ++k) {
+          if (w.n_tiles == 0) continue;
+          ok = wait_all(qbar, (uint32_t)(kq & 1));
+          for (int i = 0; i < w.n_tiles && ok; ++i) {
+            const int ti = T + i;
+            const int buf = ti & 1;
+            const uint32_t par = (uint32_t)(ti & 1);
+            ok = wait_all(&s_empty[buf], ((ti >> 1) & 1) ^ 1u);
+            const uint32_t d = tmem + pr::kColS + buf * 64;
+            for (int g = 0; g < pr::kKGroups && ok; ++g) {
+              ok = wait_all(&kfull[g], par);
+              if (!ok) break;
+              sm100::tc_fence_after();
+              if (sm100::elect_one()) {
 #pragma unroll 1
-              for (int c = 3 * g; c < 3 * g + 3; ++c) {
-                const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
-                sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
+                for (int c = pr::kKPerGroup * g; c < pr::kKPerGroup * (g + 1); ++c) {
+                  const uint64_t a = d_q + (uint64_t)(c * 512), bk = d_k + (uint64_t)(c * 512);
+                  sm100::tc_mma_bf16_pair(d, a, bk, idesc_qk, c > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
+                  for (int kk = 1; kk < 4; ++kk) sm100::tc_mma_bf16_pair(d, a + 2 * kk, bk + 2 * kk, idesc_qk, 1u);
+                }
+                sm100::tc_commit_pair_mc(&kempty[g], 3);   // this group's K slots free once read
+                if (g == pr::kKGroups - 1) {
+                  sm100::tc_commit_pair_mc(&s_full[buf], 3);
+                  if (i == w.n_tiles - 1) sm100::tc_commit_pair_mc(qempty, 3);   // the item's Q is no longer read
+                }
               }
-              sm100::tc_commit_pair_mc(&kempty[g], 3);   // this group's K slots free once read
-              if (g == pr::kKGroups - 1) sm100::tc_commit_pair_mc(&s_full[buf], 3);
+              __syncwarp();
             }
-            __syncwarp();
           }
+          T += w.n_tiles;
+          ++kq;
         }
       } else {
         const uint64_t d_p0 = desc_kmajor(smem_base + pr::kPOff);          // P keys 0..63
         const uint64_t d_p1 = desc_kmajor(smem_base + pr::kPOff + 8192);   // P keys 64..127
         const uint64_t d_v = desc_mnmajor(smem_base + pr::kVOff, 8192);
-        for (int i = 0; i < n_tiles && ok; ++i) {
-          const uint32_t par = (uint32_t)(i & 1);
-          ok = wait_all(p_full, par);
-          for (int q = 0; q < 4 && ok; ++q) {   // quarter (key half kb, dv half h) = O columns of h over kb's keys
-            const int kb = q >> 1, h = q & 1;
-            ok = wait_all(&vfull[q], par);
+        for (int k = 0; ok && work(k, w); ++k) {
+          if (w.n_tiles == 0) continue;
+          if (kq > 0) {   // the previous item's O has been read out
+            ok = wait_all(o_free, (uint32_t)((kq - 1) & 1));
             if (!ok) break;
             sm100::tc_fence_after();
-            if (sm100::elect_one()) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
-                                        d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
-                                        (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
-              sm100::tc_commit_pair_mc(&vempty[q], 3);   // this quarter's V slots free once read
-              if (q == 3) sm100::tc_commit_pair_mc(o_done, 3);
-            }
-            __syncwarp();
           }
+          for (int i = 0; i < w.n_tiles && ok; ++i) {
+            const uint32_t par = (uint32_t)((T + i) & 1);
+            ok = wait_all(p_full, par);
+            for (int qq = 0; qq < 4 && ok; ++qq) {   // quarter (key half kb, dv half h) = O columns of h over kb's keys
+              const int kb = qq >> 1, h = qq & 1;
+              ok = wait_all(&vfull[qq], par);
+              if (!ok) break;
+              sm100::tc_fence_after();
+              if (sm100::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  sm100::tc_mma_bf16_pair(tmem + pr::kColO + h * 128, (kb == 0 ? d_p0 : d_p1) + (uint64_t)(kk * 2),
+                                          d_v + (uint64_t)(((h * 2 + kb) * 2) * 512 + kk * 128), idesc_pv,
+                                          (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
+                sm100::tc_commit_pair_mc(&vempty[qq], 3);   // this quarter's V slots free once read
+                if (qq == 3) sm100::tc_commit_pair_mc(o_done, 3);
+              }
+              __syncwarp();
+            }
+          }
+          T += w.n_tiles;
+          ++kq;
         }
       }
       if (!ok && lane == 0) {
@@ -1131,6 +1247,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_pair_kernel(const __grid
     sm100::tc_fence_after();
     sm100::tmem_dealloc_pair(tmem, kTmemCols);
   }
+}
+
+// Resident 2-CTA clusters of the pair kernel per device (the persistent grid
+// must not exceed it), queried once.
+int pair_clusters(bool tree) {
+  static std::mutex mu;
+  static int cache[64][2];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& row : cache) row[0] = row[1] = -1;
+    init = true;
+  }
+  int& n = cache[dev][tree ? 1 : 0];
+  if (n < 0) {
+    auto kern = tree ? attn_mla_pair_kernel<true> : attn_mla_pair_kernel<false>;
+    n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pr::kSmemBytes) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = pr::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+  }
+  return n;
 }
 
 }  // namespace
@@ -1178,6 +1330,15 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   p.cluster = C;
   p.groups = row_blocks / C;
   const int n_items = pl.n_splits * a.B * p.groups;
+  p.n_items = n_items;
+  // CTA pairs are persistent: one pair per resident cluster slot (at most one
+  // per item) walks its share of the order.
+  int n_pairs = n_items;
+  if (paired) {
+    const int slots = pair_clusters(a.parents != nullptr);
+    if (slots <= 0) return cudaErrorInvalidConfiguration;
+    n_pairs = std::min(n_items, slots);
+  }
   mla_schedule_kernel<<<1, 1024, 0, s>>>(a.ctx_lens, a.B, R, a.Hq, C, p.groups, pl.split_len, pl.n_splits,
                                          a.max_blocks * kBlock, (int32_t*)((char*)a.workspace + pl.ws_order));
   cudaError_t e = cudaGetLastError();
@@ -1189,7 +1350,7 @@ cudaError_t launch_attention_mla_tc(const mtp_attn_args& a, const AttnPlan& pl, 
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_items * C, 1, 1);
+  cfg.gridDim = dim3(n_pairs * C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
