@@ -364,6 +364,32 @@ def test_device_range_checks_report_and_recover():
     mv.sync_status()
 
 
+def test_mla_pair_range_checks_report_and_spare_other_requests():
+    """The CTA pairs of the MLA kernel are persistent and walk many requests'
+    items in turn: one request's first block id lies beyond the cache and
+    another's context exceeds its block table. Both are reported (the block
+    reads as zeros, the long request is skipped), the pairs go on to their
+    next items, and the other requests still match the oracle."""
+    # 40 requests x 2 pair groups x 2 key splits: more items than CTA pairs
+    w = synth.CFG1.with_(name="MLA pairs, range checks", B=40, Hq=64, ctx=(60, 700), H=256, V=2000)
+    att = synth.make_attention_inputs(w, DEV)
+    keep = [b for b in range(w.B) if b not in (1, 3)]
+    exact = np.concatenate(_par(lambda b: oracle_attention(w, att, [b]), keep))
+    att["block_table"][1, 0] = 10 ** 6
+    att["ctx_lens"][3] = w.max_blocks * 64
+    out = gpu_attention(w, att)
+    with pytest.raises(mv.MtpError) as ei:
+        mv.sync_status()
+    assert ei.value.code == 4 and "block-id" in str(ei.value) and "length" in str(ei.value)
+    got = out.index_select(0, torch.tensor(keep, device=DEV)).float().cpu().numpy()
+    assert attention_excess(got, exact, w.dtype) <= 0.0
+    w2 = SMALL["cfg1_small_mla"]
+    att2 = synth.make_attention_inputs(w2, DEV)
+    out2 = gpu_attention(w2, att2)
+    mv.sync_status()
+    _check_attention(w2, att2, out2, range(w2.B))
+
+
 def test_bounded_wait_gives_up_and_context_survives():
     """The kernels' time-limited mbarrier wait, on a barrier nothing arrives on
     (no fault, no trap): it returns after the limit and flags a timeout that
