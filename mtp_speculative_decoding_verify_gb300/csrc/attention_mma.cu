@@ -64,6 +64,10 @@ constexpr int kGqaRowsPerCta = 112;   // up to 7 row warps x 16 rows
 // form with 8 consumers (4 row warps x 2 key parts) puts 3 warps on one
 // sub-partition and so has at most 168 registers a thread.
 constexpr int kGqaConsumers = 7, kGqaConsumersWide = 8;
+// The narrow form: at most 3 row warps (48 rows) and no key parts, compiled
+// for three CTAs per SM (at most 170 registers a thread), so that three CTAs
+// of two stages each share an SM instead of two of three stages.
+constexpr int kGqaConsumersNarrow = 3;
 
 template <int D>
 struct GqaCfg {
@@ -77,9 +81,11 @@ struct GqaCfg {
 // a causal prefix; the chain instantiation keeps the plain limit test.
 // kForm: 0 one warp per 16 rows, each reading every tile (the loop keeps a
 // running stage / phase); 1 key parts on up to 7 consumers; 2 the wide form,
-// 8 consumers.
+// 8 consumers; 3 form 0 for at most 3 row warps at three CTAs per SM.
 template <int D, bool kTree, int kForm>
-__global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaConsumers) + 1), 1) attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
+__global__ void __launch_bounds__(kForm == 3 ? 32 * (kGqaConsumersNarrow + 1)
+                                             : 32 * ((kForm == 2 ? kGqaConsumersWide : kGqaConsumers) + 1),
+                                  kForm == 3 ? 3 : 1) attn_gqa_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                        const __grid_constant__ CUtensorMap tm_v,
                                                        const AttnKParams p) {
   using C = GqaCfg<D>;
@@ -170,7 +176,8 @@ __global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaCo
   // Consumer cw takes rows 16 rw .. 16 rw + 15 of the CTA and the tiles i
   // with i % key_parts == kp; the key parts of a row block merge at the end.
   const int cw = warp - 1;
-  const int rw = kForm == 0 ? cw : cw % p.row_warps, kp = kForm == 0 ? 0 : cw / p.row_warps;
+  constexpr bool kOnePart = kForm == 0 || kForm == 3;   // no key parts
+  const int rw = kOnePart ? cw : cw % p.row_warps, kp = kOnePart ? 0 : cw / p.row_warps;
   const int g = lane >> 2, t = lane & 3;
   const int r_lo = row_base + rw * 16 + g, r_hi = r_lo + 8;
   const int rl = min(r_lo, p.rows - 1), rh = min(r_hi, p.rows - 1);   // padding rows compute on the last row
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaCo
     if (lane == 0) sm100::mbar_arrive(&empty[stage]);
     return true;
   };
-  if constexpr (kForm == 0) {
+  if constexpr (kOnePart) {
     int stage = 0;
     uint32_t phase = 0;
     for (int i = 0; i < n_tiles; ++i) {
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(32 * ((kForm == 2 ? kGqaConsumersWide : kGqaCo
       if (!consume(i, i % p.stages, (uint32_t)(i / p.stages) & 1u)) break;
   }
 
-  if constexpr (kForm != 0) {
+  if constexpr (!kOnePart) {
     // Merge the key parts of each row block. Every consumer is past its last
     // tile at the first barrier, so the stage ring is free: parts kp > 0
     // leave their (o, m, l) there, one slot per (warp, lane) (the fragment
@@ -405,6 +412,7 @@ using GqaKernel = void (*)(const CUtensorMap, const CUtensorMap, const AttnKPara
 
 template <int D>
 GqaKernel<D> gqa_kernel(bool tree, int form) {
+  if (form == 3) return tree ? attn_gqa_kernel<D, true, 3> : attn_gqa_kernel<D, false, 3>;
   if (form == 2) return tree ? attn_gqa_kernel<D, true, 2> : attn_gqa_kernel<D, false, 2>;
   if (form == 1) return tree ? attn_gqa_kernel<D, true, 1> : attn_gqa_kernel<D, false, 1>;
   return tree ? attn_gqa_kernel<D, true, 0> : attn_gqa_kernel<D, false, 0>;
@@ -414,7 +422,7 @@ GqaKernel<D> gqa_kernel(bool tree, int form) {
 // reports for its threads and shared memory), cached per form.
 template <int D>
 int gqa_occupancy(bool tree, int form, int warps, int stages) {
-  static int cache[2][3][kGqaConsumersWide + 1][9] = {};
+  static int cache[2][4][kGqaConsumersWide + 1][9] = {};
   int& c = cache[tree][form][warps][stages];
   if (c == 0) {
     const GqaKernel<D> kern = gqa_kernel<D>(tree, form);
@@ -504,6 +512,18 @@ cudaError_t run_gqa(const mtp_attn_args& a, const AttnPlan& pl, unsigned* err, c
         stages = S;
         form = w ? 2 : 1;
       }
+    }
+  }
+  if (form == 0 && row_warps <= kGqaConsumersNarrow) {
+    // The same consumers three to an SM (two stages each) when the whole grid
+    // then runs in one wave and does not at the register-bound two CTAs of
+    // three stages (sweep B=8, D=5: 0.071 -> 0.054 ms). Over several waves the
+    // shallower pipeline loses (Llama-70B shape: 0.196 -> 0.216 ms).
+    const long long occ0 = gqa_occupancy<D>(tree, 0, row_warps, stages);
+    const long long occ3 = gqa_occupancy<D>(tree, 3, row_warps, 2);
+    if (occ3 > occ0 && grid_ctas > occ0 * pl.sm_count && grid_ctas <= occ3 * pl.sm_count) {
+      form = 3;
+      stages = 2;
     }
   }
   const int warps = row_warps * key_parts;
