@@ -130,10 +130,10 @@ TRAFFIC = {
                     "ncu capture of lmhead_tc_kernel at M=128, vocabulary 32768 (profile_mla_V32k)"),
     },
     "cfg2": {
-        # attn_gqa_kernel<128> form 0 at the same shapes (profile_sampling_V32k): 1097.27 MB read
-        # + 6.63 MB written for 1075.31 MB of KV cache
-        "attention": ((1097269760 + 6626048) / 1075314688, "KV-cache bytes", KERNEL_SOURCES["attention"],
-                      "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel (profile_sampling_V32k)"),
+        # attn_gqa_kernel<128> form 0 at the same shapes (profile_sampling_V32k): 1097.26 MB read
+        # + 6.97 MB written for 1075.31 MB of KV cache
+        "attention": ((1097258240 + 6973696) / 1075314688, "KV-cache bytes", KERNEL_SOURCES["attention"],
+                      "6e5b81293843fbdb", "ncu capture of attn_gqa_kernel (profile_sampling_V32k)"),
         # lmhead_tc_kernel<6, true> at M=384 with vocabulary 32768 (profile_sampling_V32k): 543.31 MB read
         # + 21.74 MB written
         "lm_head": ((543312896 + 21744896) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
@@ -141,10 +141,10 @@ TRAFFIC = {
                     "ncu capture of lmhead_tc_kernel at M=384, vocabulary 32768 (profile_sampling_V32k)"),
     },
     "cfg3": {
-        # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.32 MB read + 4.22 MB
+        # attn_gqa_kernel<128> on the same shapes at B=16 (profile_gqa_B16): 990.31 MB read + 4.53 MB
         # written for 987.60 MB of KV cache
-        "attention": ((990315008 + 4223488) / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"],
-                      "7caedea6e6a477aa", "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
+        "attention": ((990305280 + 4533760) / 987598848, "KV-cache bytes", KERNEL_SOURCES["attention"],
+                      "6e5b81293843fbdb", "ncu capture of attn_gqa_kernel at B=16 (profile_gqa_B16)"),
         # lmhead_tc_kernel<8, true> at M=1024 with vocabulary 65536 (profile_lm_cfg3_V64k): 616.33 MB read
         # + 102.73 MB written
         "lm_head": ((616330496 + 102726400) / 65536, "vocabulary rows", KERNEL_SOURCES["lm_head"],
