@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   MTP_OK = 0,
   MTP_INVALID_ARG = 1,   /* null pointer, bad shape, D > MTP_MAX_DRAFTS, block_size != 64, ... */
-  MTP_UNSUPPORTED = 2,   /* dtype / shape combination this build does not provide */
+  MTP_UNSUPPORTED = 2,   /* dtype / shape combination the library does not provide */
   MTP_CUDA_ERROR = 3,    /* a CUDA runtime call or launch failed */
   MTP_DEVICE_ERROR = 4   /* a device-side range check tripped (see mtp_sync_status) */
 } mtp_status;
