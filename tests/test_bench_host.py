@@ -124,3 +124,29 @@ def test_workload_config_names_no_run_options():
     import bench
     cfg = bench.config_of(bench.workloads()["cfg3"], argparse.Namespace(no_graph=False, impl="gb300"))
     assert "cuda_graph" not in cfg and cfg["B"] == 256 and cfg["D"] == 3
+
+
+def test_copy_in_pieces_matches_one_copy():
+    """The end-to-end leg's copies in pieces give the same tensor as one copy,
+    for sizes around and across the piece size, and leave views alone."""
+    sys.path.insert(0, ROOT)
+    import bench
+    saved = bench.COPY_PIECE_BYTES
+    try:
+        bench.COPY_PIECE_BYTES = 64   # 16 float32 per piece
+        g = torch.Generator().manual_seed(7)
+        for n in (1, 15, 16, 17, 160, 161, 1000):
+            src = torch.randn(n, generator=g)
+            dst = torch.zeros(n)
+            bench.copy_in_pieces(dst, src)
+            assert torch.equal(dst, src), n
+        src = torch.randn(7, 9, 5, generator=g)
+        dst = torch.zeros(7, 9, 5)
+        bench.copy_in_pieces(dst, src)
+        assert torch.equal(dst, src)
+        big = torch.zeros(10, 10)
+        view = big[:, :3]                       # not contiguous: one plain copy
+        bench.copy_in_pieces(view, torch.ones(10, 3))
+        assert big[:, :3].eq(1).all() and big[:, 3:].eq(0).all()
+    finally:
+        bench.COPY_PIECE_BYTES = saved
