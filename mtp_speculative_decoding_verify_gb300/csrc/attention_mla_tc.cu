@@ -667,15 +667,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mla_tc_kernel(const __grid_c
 // chunks that QK has finished with: the nine K chunks land and are released
 // in three groups of three, and the eight V boxes in four quarters (key half
 // x dv half, PV's four quarters in turn), so the loads of tile i+1 start
-// while QK(i) and PV(i) still run. Two warps
-// issue the MMAs: one QK(i) as soon as its key groups land, the other PV(i)
-// as soon as P(i) is written, so QK(i+1) runs during the softmax of tile i
-// instead of waiting behind PV(i) (S is double-buffered; each issuing warp
-// waits only for its own inputs: a wait costs the issuing warp a few hundred
-// clocks even when the phase is already complete). P is single-buffered: the
-// softmax of tile i computes its probabilities in registers, then waits for
-// PV(i-1) before writing them (and before using the reduction scratch, which
-// shares the P buffer).
+// while QK(i) and PV(i) still run. Two warps issue the MMAs: one QK(i) as
+// soon as its key groups land, the other PV(i) as soon as P(i) is written, so
+// QK(i+1) runs during the softmax of tile i instead of waiting behind PV(i)
+// (S is double-buffered; each issuing warp waits only for its own inputs: a
+// wait costs the issuing warp a few hundred clocks even when the phase is
+// already complete). P is single-buffered: the softmax of tile i computes its
+// probabilities in registers, then waits for PV(i-1) before writing them (and
+// before using the reduction scratch, which shares the P buffer).
+// The pairs are persistent (one per resident cluster slot) and walk several
+// work items each; the barrier phases run on across items, the next item's Q
+// and first tiles load while the current one ends, and its first PV waits
+// only for the epilogue to have read O out. The epilogue stages the output
+// through the P buffer so that it leaves as whole 128-byte lines.
 namespace pr {
 constexpr int kQOff = 0;                          // 9 x [64 rows x 64 dims]
 constexpr int kKOff = kQOff + 9 * 8192;           // 9 x [64 own keys x 64 dims]
