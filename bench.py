@@ -119,10 +119,10 @@ KERNEL_SOURCES = {
 
 TRAFFIC = {
     "cfg1_D3": {
-        # attn_mla_pair_kernel at the same shapes (profile_mla_V32k): 109.30 MB read + 5.00 MB written for
+        # attn_mla_pair_kernel at the same shapes (profile_mla_V32k): 109.45 MB read + 5.29 MB written for
         # 87.35 MB of latent KV (the rest: the queries, 18.9 MB, and the outputs)
-        "attention": ((109302016 + 5002752) / 87353856, "KV-cache bytes", KERNEL_SOURCES["attention_mla"],
-                      "f55dbf49ce8182c4", "ncu capture of attn_mla_pair_kernel (profile_mla_V32k)"),
+        "attention": ((109451776 + 5287168) / 87353856, "KV-cache bytes", KERNEL_SOURCES["attention_mla"],
+                      "be101fe337e05d0e", "ncu capture of attn_mla_pair_kernel (profile_mla_V32k)"),
         # lmhead_tc_kernel<4, true> (CTA pairs) at M=128 with vocabulary 32768 (profile_mla_V32k):
         # 471.69 MB read + 2.82 MB written
         "lm_head": ((471687168 + 2816256) / 32768, "vocabulary rows", KERNEL_SOURCES["lm_head"],
