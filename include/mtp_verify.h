@@ -44,6 +44,10 @@
  *     call on the same thread). No C++ exception crosses this boundary.
  *   - Tensors are dense and row-major in the shapes given; bf16 tensors hold
  *     IEEE bfloat16 values.
+ *   - The first call on a device allocates the error word and queries kernel
+ *     attributes and occupancies (cached per device); make it outside stream
+ *     capture. Later calls launch kernels only and can be captured into a
+ *     CUDA graph.
  */
 #ifndef MTP_VERIFY_H
 #define MTP_VERIFY_H
